@@ -1,0 +1,439 @@
+"""Benchmark of the paged-KV decode step of a looped transformer on GB300.
+
+One step = one decode token for every request of the batch through every
+(layer, plane) bank of the model: for each bank, append this step's K/V rows
+(rlt_kv_append) and run split-K paged decode attention (rlt_paged_decode_attn);
+workloads whose model draws latent noise (Huginn-shaped) also initialise the new
+tokens' latent state (rlt_latent_noise_init).  All inputs are seeded and
+synthetic; every bank's KV lives in its own region of HBM.
+
+Prints ONE JSON line.  `value` is the step's algorithmic HBM bytes (unique pages
+counted once) divided by the device time of a step, in GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ouro] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attn: achieved HBM GB/s (% of GB300 peak), µs per layer-plane step"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+L2_BYTES = 129 * 2**20
+
+
+# ------------------------------------------------------------------ bytes
+
+def attn_bytes(case: W.PagedCase, unique: bool = True) -> int:
+    """Algorithmic bytes of one paged decode attention call over one bank."""
+    tokens = case.unique_tokens() if unique else case.kv_tokens()
+    kv = tokens * case.num_kv_heads * case.head_dim * 2 * 2
+    qo = case.batch * case.num_q_heads * case.head_dim * 2 * 2
+    meta = sum(case.pages_of(b) for b in range(case.batch)) * 4 + case.batch * 4
+    return kv + qo + meta
+
+
+def append_bytes(case: W.PagedCase) -> int:
+    n = int((case.new_slots >= 0).sum())
+    return n * case.num_kv_heads * case.head_dim * 2 * 2 * 2 + case.batch * 8
+
+
+def noise_bytes(case: W.PagedCase) -> int:
+    nz = case.noise
+    return 0 if nz is None else nz.rows * 16 + nz.rows * nz.channels * 4
+
+
+def layer_planes(case: W.PagedCase):
+    rec = np.asarray(case.recurrent, np.uint8)
+    return [(l, t) for t in range(case.num_planes) for l in range(case.num_layers) if t == 0 or rec[l]]
+
+
+# --------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[4:8]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for_smi(torch, dev) -> str:
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if uuid:
+            return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    return vis.split(",")[dev.index or 0] if vis else str(dev.index or 0)
+
+
+# ------------------------------------------------------------ peaks etc.
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(kernel_src: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on this source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "attn_traffic.txt")
+    try:
+        lines = dict(l.split(":", 1) for l in open(path).read().splitlines() if ":" in l)
+    except OSError:
+        return None
+    digest = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    if lines.get("source_sha256_16", "").strip() != digest:
+        return None
+    try:
+        return float(lines["dram_bytes_per_full_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------ GPU arm
+
+def run_gpu(args, rank, world):
+    import torch
+
+    import paged_kv_looped_gb300 as rlt
+    from paged_kv_looped_gb300 import build as rlt_build
+    rlt_build.build()
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    case = W.config(args.workload)
+    lp = layer_planes(case)
+    bmap, nbanks = rlt.rlt_bank_map(case.recurrent, case.num_planes)
+    assert nbanks == len(lp)
+    assert rlt.rlt_validate_batch(case.page_table, case.seq_lens, case.new_slots, case.num_pages,
+                                  case.page_size) == 0
+
+    # resident state: one pool region per bank, page table, lengths
+    kpool, vpool = W.device_pool(case, nbanks, dev)
+    pool = rlt.KVPool(kpool, vpool)
+    rng = np.random.default_rng(case.seed + 77)
+    B, Hq, Hkv, D = case.batch, case.num_q_heads, case.num_kv_heads, case.head_dim
+    def bf(shape):
+        return torch.from_numpy(W.bf16_normal(rng, shape).view(np.int16)).view(torch.bfloat16)
+    q_h = bf((nbanks, B, Hq, D)).pin_memory()
+    kn_h = bf((nbanks, B, Hkv, D)).pin_memory()
+    vn_h = bf((nbanks, B, Hkv, D)).pin_memory()
+    loc_h = torch.from_numpy(case.new_slots.copy()).pin_memory()
+    pt_h = torch.from_numpy(case.page_table.copy()).pin_memory()
+    sl_h = torch.from_numpy(case.seq_lens.astype(np.int32)).pin_memory()
+    q, kn, vn = q_h.to(dev), kn_h.to(dev), vn_h.to(dev)
+    loc, pt, sl = loc_h.to(dev), pt_h.to(dev), sl_h.to(dev)
+    out = torch.empty((nbanks, B, Hq, D), dtype=torch.bfloat16, device=dev)
+    out_h = torch.empty_like(out, device="cpu").pin_memory()
+    ws_bytes = rlt.rlt_paged_decode_workspace_size(B, Hq, Hkv, D, case.max_seq_len, args.split_tokens)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    nz = case.noise
+    if nz is not None:
+        seeds_h = torch.from_numpy(nz.seeds.view(np.int64).copy()).pin_memory()
+        pos_h = torch.from_numpy(nz.positions.copy()).pin_memory()
+        seeds, pos = seeds_h.to(dev), pos_h.to(dev)
+        noise = torch.empty((nz.rows, nz.channels), dtype=torch.float32, device=dev)
+        noise_h = torch.empty_like(noise, device="cpu").pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    banks = [int(bmap[l, t]) for (l, t) in lp]
+
+    ev_attn = []
+
+    def step(time_attn=False):
+        if nz is not None:
+            rlt.rlt_latent_noise_init(seeds, pos, nz.channels, nz.initializer_range, out=noise, stream=stream)
+        for i, bank in enumerate(banks):
+            rlt.rlt_kv_append(pool, bank, kn[i], vn[i], loc, stream=stream)
+            if time_attn:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            rlt.rlt_paged_decode_attn(pool, bank, q[i], pt, sl, case.max_seq_len, out=out[i], workspace=ws,
+                                      split_tokens=args.split_tokens, stream=stream)
+            if time_attn:
+                e1.record(stream)
+                ev_attn.append((e0, e1))
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    assert rlt.rlt_get_device_error() == 0
+
+    # ---- timed region: inputs resident in HBM; each bank's KV (> L2) is read once per step
+    gpu_id = gpu_id_for_smi(torch, dev)
+    with ClockSampler(gpu_id) as clocks:
+        barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step(time_attn=True)
+        t1.record(stream)
+        barrier()
+    ms_total = t0.elapsed_time(t1)
+    attn_ms = [a.elapsed_time(b) for a, b in ev_attn]
+    assert rlt.rlt_get_device_error() == 0
+
+    # ---- end to end: this step's inputs from pinned host memory, outputs back to the host
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        q.copy_(q_h, non_blocking=True)
+        kn.copy_(kn_h, non_blocking=True)
+        vn.copy_(vn_h, non_blocking=True)
+        loc.copy_(loc_h, non_blocking=True)
+        pt.copy_(pt_h, non_blocking=True)
+        sl.copy_(sl_h, non_blocking=True)
+        if nz is not None:
+            seeds.copy_(seeds_h, non_blocking=True)
+            pos.copy_(pos_h, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        if nz is not None:
+            noise_h.copy_(noise, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, kn_h, vn_h, loc_h, pt_h, sl_h))
+    d2h = out_h.numel() * out_h.element_size()
+    if nz is not None:
+        h2d += seeds_h.numel() * 8 + pos_h.numel() * 8
+        d2h += noise_h.numel() * 4
+    combine = ws_bytes > 0
+    launches = args.steps * (len(banks) * (3 if combine else 2) + (1 if nz is not None else 0))
+    return dict(case=case, banks=banks, ms_total=ms_total, attn_ms=attn_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+                clocks=clocks.summary(), launches=launches, combine=combine, ws_bytes=ws_bytes)
+
+
+# ------------------------------------------------------------ CPU oracle
+
+class OracleSample:
+    """A bounded sample of the workload for the CPU oracle: k random requests of one
+    bank on a compact host pool, generated once; each pass is append + attention."""
+
+    def __init__(self, case: W.PagedCase, k: int, seed: int = 0):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        rng = np.random.default_rng(seed)
+        rows = rng.choice(case.batch, min(k, case.batch), replace=False)
+        self.sub = W.subcase(case, rows)
+        self.h = W.host_tensors(self.sub, seed=seed + 1)
+        self.bytes = attn_bytes(self.sub) + append_bytes(self.sub)
+        self.desc = (f"oracle (plain C, fp64, 1 thread): append + paged decode attention of {len(rows)} random "
+                     f"requests ({self.sub.kv_tokens()} cached tokens) of one bank of the {case.name} workload; "
+                     f"GB/s of the same algorithmic bytes")
+
+    def run(self) -> float:
+        """One pass; returns its wall time in seconds."""
+        h, sub, o = self.h, self.sub, self.oracle
+        kp, vp = h.k_pool.copy(), h.v_pool.copy()
+        t = time.perf_counter()
+        o.kv_append(kp, vp, h.k_new, h.v_new, sub.new_slots)
+        o.decode_attn(h.q, kp, vp, sub.page_table, sub.seq_lens)
+        return time.perf_counter() - t
+
+
+def oracle_sample(case: W.PagedCase, budget_s: float, seed: int = 0):
+    """Time the oracle (as it stands, one thread) on a sample of the workload for about
+    budget_s of CPU work; returns (GB/s of algorithmic bytes, description, seconds)."""
+    s = OracleSample(case, 8, seed)
+    spent, passes = 0.0, 0
+    while spent < budget_s or passes == 0:
+        spent += s.run()
+        passes += 1
+    return s.bytes * passes / spent / 1e9, s.desc + f"; {passes} passes, {spent:.1f} s", spent
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands on the host cores, on the bench's workload, metric and unit."""
+    if rank != 0:
+        return None
+    case = W.config(args.workload)
+    sample = OracleSample(case, 8, seed=1)
+    for _ in range(args.warmup):
+        sample.run()
+    times = [sample.run() for _ in range(args.steps)]
+    value = sample.bytes * len(times) / sum(times) / 1e9
+    nlp = len(layer_planes(case))
+    step_bytes = attn_bytes(case) * nlp + append_bytes(case) * nlp + noise_bytes(case)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_bytes / (value * 1e9) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(case, args),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample.desc + f"; each step one pass, {args.steps} steps, "
+                                                 f"{sum(times):.1f} s"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def config_dict(case, args):
+    return {"workload": f"{case.name}: {case.num_layers} layers x {case.num_planes} planes "
+                        f"({len(layer_planes(case))} layer-plane banks), B={case.batch}, Hq={case.num_q_heads}, "
+                        f"Hkv={case.num_kv_heads}, head_dim={case.head_dim}, page_size={case.page_size}, "
+                        f"L in [{int(case.seq_lens.min())}, {int(case.seq_lens.max())}]",
+            "batch": case.batch, "kv_tokens_per_layer_plane": case.kv_tokens(),
+            "unique_kv_tokens_per_layer_plane": case.unique_tokens(),
+            "split_tokens": args.split_tokens or "auto",
+            "l2": "inputs larger than L2: every bank's KV exceeds the 129 MB L2 and each is read once per step"}
+
+
+# ------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="ouro", choices=W.WORKLOADS)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--split-tokens", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU time for cpu_baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if rank == 0:
+            print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl")
+    r = run_gpu(args, rank, world)
+    case = r["case"]
+    nlp = len(r["banks"])
+    step_bytes = attn_bytes(case) * nlp + append_bytes(case) * nlp + noise_bytes(case)
+    ms_step = r["ms_total"] / args.steps
+    ms_max = ms_step
+    e2e_ms_step = r["e2e_ms"] / args.steps
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms_step, e2e_ms_step], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max, e2e_ms_step = float(t[0]), float(t[1])
+    value = world * step_bytes / (ms_max * 1e-3) / 1e9
+    e2e_value = world * step_bytes / (e2e_ms_step * 1e-3) / 1e9
+
+    attn_launch_ms = statistics.mean(r["attn_ms"])
+    a_bytes = attn_bytes(case)
+    peak, peak_kind = hbm_peak()
+    achieved = a_bytes / (attn_launch_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(os.path.join(ROOT, "paged_kv_looped_gb300", "csrc", "attn.cu"))
+
+    cpu = None
+    if rank == 0 and args.cpu_budget > 0:
+        v, desc, _ = oracle_sample(case, args.cpu_budget)
+        cpu = {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 Q/K/V, random page allocation)",
+        "config": config_dict(case, args),
+        "us_per_layer_plane": round(ms_max * 1e3 / nlp, 2),
+        "pct_of_peak_hbm": round(100 * value / world / peak, 2),
+        "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "kv_tokens_per_s": round(world * case.kv_tokens() * nlp / (ms_max * 1e-3), 1),
+        "roofline": {"bound": "hbm", "kernel": "rlt_paged_decode_attn (split-K partial + combine)",
+                     "achieved": round(achieved, 2), "peak": peak, "peak_kind": f"{peak_kind} (HBM copy)",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": a_bytes, "launch_us": round(attn_launch_ms * 1e3, 2)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,217 @@
+/*
+ * rlt.h - C ABI of the GB300 paged-KV decode path for looped transformers.
+ *
+ * One shared library (librlt.so, sm_103a) with plain pointers and sizes: no
+ * C++ or framework types cross this boundary.  All array arguments of the
+ * compute entry points are DEVICE pointers owned by the caller; the library
+ * allocates nothing and keeps no state besides a per-device error word.
+ * Every compute call is enqueued on the caller's stream (a cudaStream_t passed
+ * as void*; NULL = the legacy default stream), returns without waiting for the
+ * GPU, and makes no host/device synchronisation.  Arguments are checked on
+ * the host before any launch; a failed check returns a status and launches
+ * nothing.  Kernels never trap: a page id or slot that is out of range at run
+ * time is skipped and recorded in the device error word
+ * (rlt_get_device_error).
+ *
+ * Sources (page title, section):
+ *  [FFM]   "Faster fuzzy minds" (dibbla.space/posts/matrices/fast_subconscious)
+ *          - "When scheduler does the work": paged KV cache = a flat pool of
+ *            fixed-size slots addressed through page_table[request, position];
+ *            two sequences may point at the same physical slots.
+ *          - "LOTUS - the one place I opened the scheduler": store_kv scatters
+ *            each token's K/V to the physical slots it is handed (out_loc);
+ *            handing the same slots again overwrites in place.
+ *          - "Recurrent depth - a deep model in a trench coat": L weight layers
+ *            looped T times are T*L attention layers; iteration t of layer l
+ *            writes KV bank t*L + l; decode attention over the paged pool
+ *            treats it as an ordinary deep transformer.
+ *  [PR152] vllm-rlt PR #152, "[Huginn] Opt-in prefix caching with
+ *          position-keyed recurrent-state noise", Summary para 1 (per-plane
+ *          layer map of #147: prelude/coda layers on plane 0 only) and para 2
+ *          (latent noise = f(request seed, position, channel) via a stage-wise
+ *          SplitMix64-style hash, a 24-bit uniform and an inverse normal CDF
+ *          onto a normal with std = initializer_range truncated at +-3 sigma).
+ *
+ * KV pool layout (this library's convention; the pages leave it open):
+ *   k and v are separate bf16 arrays, each
+ *       [num_banks][num_pages][num_kv_heads][page_size][head_dim]
+ *   so that the page_size rows of one (bank, page, kv head) are one contiguous
+ *   page_size*head_dim*2-byte chunk.  Logical position p of request b is at
+ *   page page_table[b*max_pages + p/page_size], offset p % page_size, i.e.
+ *   slot = page*page_size + offset.
+ */
+#ifndef RLT_H
+#define RLT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#ifndef RLT_API
+#define RLT_API __attribute__((visibility("default")))
+#endif
+
+typedef enum rlt_status {
+    RLT_OK = 0,
+    RLT_ERR_INVALID_ARG = 1,          /* null pointer, negative size, misaligned buffer */
+    RLT_ERR_OUT_OF_RANGE = 2,         /* bank, page, slot or length outside the pool */
+    RLT_ERR_UNSUPPORTED = 3,          /* a shape this build has no kernel for */
+    RLT_ERR_WORKSPACE_TOO_SMALL = 4,  /* see rlt_paged_decode_workspace_size */
+    RLT_ERR_CUDA = 5                  /* the CUDA runtime reported an error */
+} rlt_status;
+
+/* Bits of the device error word (rlt_get_device_error). */
+#define RLT_DEVERR_BAD_PAGE 1u        /* a page-table entry outside [0, num_pages) was skipped */
+#define RLT_DEVERR_BAD_SLOT 2u        /* an append slot >= num_pages*page_size was skipped */
+#define RLT_DEVERR_TIMEOUT 4u         /* a copy wait gave up after its time limit */
+#define RLT_DEVERR_BAD_LEN 8u         /* a seq_len outside [0, min(max_pages*page_size,
+                                         max_seq_len rounded to the split grid)] was clamped */
+
+/* A paged KV pool (device memory owned by the caller). */
+typedef struct rlt_kv_pool {
+    void *k;                /* bf16 [num_banks][num_pages][num_kv_heads][page_size][head_dim] */
+    void *v;                /* same shape as k */
+    int64_t num_pages;      /* physical pages per bank */
+    int32_t num_banks;      /* one bank per (layer, plane) the model holds */
+    int32_t num_kv_heads;
+    int32_t page_size;      /* tokens per page, >= 1 */
+    int32_t head_dim;       /* 64 or 128 */
+} rlt_kv_pool;
+
+/* Human-readable name of a status code (static string, never NULL). */
+RLT_API const char *rlt_status_string(rlt_status status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+RLT_API int32_t rlt_version(void);
+
+/*
+ * (layer, plane) -> bank map, HOST function ([FFM] "Recurrent depth";
+ * [PR152] Summary para 1).  recurrent[l] != 0 marks a looped layer.  Plane 0
+ * holds every layer; plane t >= 1 holds only the looped layers.  Banks are
+ * numbered plane by plane, layers in order within a plane, so a fully looped
+ * stack gets bank t*num_layers + l.  Writes map_out[l*num_planes + t] (bank,
+ * or -1 where the plane does not hold the layer) and returns the number of
+ * banks, or -RLT_ERR_INVALID_ARG for a null pointer or a size < 1.
+ */
+RLT_API int32_t rlt_bank_map(const uint8_t *recurrent, int32_t num_layers, int32_t num_planes,
+                     int32_t *map_out);
+
+/*
+ * KV append = store_kv ([FFM] "LOTUS"): for i < n_tokens with out_loc[i] >= 0,
+ * write k_new[i] and v_new[i] (bf16 [n_tokens][num_kv_heads][head_dim], device)
+ * to slot out_loc[i] (int64, device) of the given bank.  Negative slots mean
+ * "no token" and are skipped.  Slots within one call must be distinct (two
+ * writers to one slot race); writing slots of an earlier call again overwrites
+ * them in place.  A slot >= num_pages*page_size is skipped and sets
+ * RLT_DEVERR_BAD_SLOT.  k_new, v_new and the pool must be 16-byte aligned.
+ */
+RLT_API rlt_status rlt_kv_append(const rlt_kv_pool *pool, int32_t bank, const void *k_new,
+                         const void *v_new, const int64_t *out_loc, int32_t n_tokens,
+                         void *stream);
+
+/*
+ * Bytes of device workspace rlt_paged_decode_attn needs for these sizes
+ * (split-K partial outputs and log-sum-exps).  split_tokens as passed to
+ * rlt_paged_decode_attn (0 = the library's choice).  Returns 0 for invalid
+ * sizes.
+ */
+RLT_API size_t rlt_paged_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t max_seq_len,
+                                       int32_t split_tokens);
+
+/*
+ * Paged GQA decode attention ([FFM] "When scheduler does the work",
+ * "Recurrent depth").  For every request b < batch and query head h:
+ *     s_j = scale * <q[b][h], K_j>,  out[b][h] = sum_j softmax(s)_j V_j,
+ * over the seq_lens[b] cached tokens j of request b (the token appended this
+ * step included), K_j/V_j read from kv head h / (num_q_heads/num_kv_heads)
+ * at page page_table[b*max_pages + j/page_size], offset j % page_size, of
+ * bank `bank`.
+ *   q          bf16 [batch][num_q_heads][head_dim], device
+ *   page_table int32 [batch][max_pages], device; entries past a request's
+ *              last page are never read
+ *   seq_lens   int32 [batch], device, each in [0, max_seq_len]
+ *   max_seq_len host upper bound of seq_lens (sizes the split-K grid)
+ *   scale      softmax scale; <= 0 means 1/sqrt(head_dim)
+ *   out        bf16 [batch][num_q_heads][head_dim], device
+ *   lse_out    fp32 [batch][num_q_heads] natural-log sum of exp(s_j), or NULL
+ *   workspace  device scratch of >= rlt_paged_decode_workspace_size() bytes,
+ *              16-byte aligned; its contents need no initialisation and are
+ *              garbage afterwards.  Calls that overlap on the GPU must not
+ *              share one workspace.
+ *   split_tokens tokens per split-K chunk, a multiple of 16 up to 2048;
+ *              0 = the library's choice for the current device
+ * A request with seq_lens[b] == 0 gets out = 0 and lse = -inf.  Supported:
+ * head_dim 64 or 128; num_q_heads/num_kv_heads in {1, 2, 4, 8}; page_size a
+ * multiple of 16 up to 256.  Page-table entries outside [0, num_pages) are
+ * skipped (their tokens count as absent) and set RLT_DEVERR_BAD_PAGE.
+ * q, out, the pool and workspace must be 16-byte aligned.
+ */
+RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, const void *q,
+                                 int32_t num_q_heads, const int32_t *page_table,
+                                 int32_t max_pages, const int32_t *seq_lens, int32_t batch,
+                                 int32_t max_seq_len, float scale, void *out, float *lse_out,
+                                 void *workspace, size_t workspace_bytes,
+                                 int32_t split_tokens, void *stream);
+
+/*
+ * Position-keyed latent-state noise ([PR152] Summary para 2).  For each row r
+ * (a token) and channel c < channels:
+ *     key  = stage(stage(stage(0, seeds[r]), positions[r]), c),
+ *            stage(h, x) = mix64((h ^ x) + 0x9E3779B97F4A7C15),
+ *            mix64 = the SplitMix64 output function (mod 2^64 arithmetic);
+ *     h24  = key >> 40;  u = (h24 + 1/2) / 2^24;
+ *     out[r][c] = initializer_range * sqrt(2) * erfinv((2u - 1) * erf(3/sqrt(2)))
+ * i.e. the inverse CDF of N(0, initializer_range^2) truncated at +-3 sigma.
+ * The value depends only on (seed, position, channel), never on the batch.
+ *   out fp32 [n_rows][channels], seeds uint64 [n_rows], positions int64
+ *   [n_rows] (absolute token positions), all device.
+ */
+RLT_API rlt_status rlt_latent_noise_init(float *out, const uint64_t *seeds, const int64_t *positions,
+                                 int64_t n_rows, int32_t channels, float initializer_range,
+                                 void *stream);
+
+/* The 24-bit uniforms h24 of rlt_latent_noise_init, as uint32 [n_rows][channels]
+ * (device); for bit-exact checks of the hash. */
+RLT_API rlt_status rlt_noise_hash24(uint32_t *out, const uint64_t *seeds, const int64_t *positions,
+                            int64_t n_rows, int32_t channels, void *stream);
+
+/*
+ * Page-table gather ([FFM] "When scheduler does the work"): copy the K and V
+ * rows of the first seq_lens[b] logical positions of every request, in
+ * logical order, into k_out / v_out (bf16 [batch][max_len][num_kv_heads]
+ * [head_dim], device).  Rows at positions >= seq_lens[b] are not written.
+ * For bit-exact checks of the slot mapping.  seq_lens[b] must be <= max_len.
+ */
+RLT_API rlt_status rlt_paged_gather(const rlt_kv_pool *pool, int32_t bank, const int32_t *page_table,
+                            int32_t max_pages, const int32_t *seq_lens, int32_t batch,
+                            int32_t max_len, void *k_out, void *v_out, void *stream);
+
+/*
+ * HOST validation of a decode batch before it is handed to the GPU (all
+ * arrays are host copies): every page-table entry a request uses lies in
+ * [0, num_pages); seq_lens[b] in [0, max_pages*page_size]; every
+ * new_slots[b] >= 0 lies in the pool, on the page holding position
+ * seq_lens[b]-1 of request b, and no two requests share it; no page holding
+ * a new slot appears in another request's page table (shared prefix pages
+ * are read-only).  new_slots may be NULL.  Returns RLT_OK or the first
+ * violation as RLT_ERR_OUT_OF_RANGE / RLT_ERR_INVALID_ARG.
+ */
+RLT_API rlt_status rlt_validate_batch(const int32_t *page_table, int32_t max_pages,
+                              const int32_t *seq_lens, int32_t batch, const int64_t *new_slots,
+                              int64_t num_pages, int32_t page_size);
+
+/*
+ * Read and clear the device error word (RLT_DEVERR_* bits) of the current
+ * device.  Synchronises the device.
+ */
+RLT_API rlt_status rlt_get_device_error(uint32_t *error_bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RLT_H */

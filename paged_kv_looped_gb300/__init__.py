@@ -1,0 +1,268 @@
+"""Python binding of librlt, the sm_103a paged-KV decode path for looped transformers.
+
+Argument marshalling only: every step of the path runs in the CUDA kernels of
+``librlt.so`` behind the C ABI declared in ``include/rlt.h``.  PyTorch
+supplies device memory and streams.  There is no CPU fallback: if the library
+has not been built, every call raises.
+
+Functions keep the C names:
+
+* ``rlt_bank_map``          (layer, plane) -> KV bank map (host).
+* ``rlt_kv_append``         store_kv: scatter this step's K/V rows to their slots.
+* ``rlt_paged_decode_attn`` split-K paged GQA decode attention (+ combine).
+* ``rlt_latent_noise_init`` position-keyed truncated-normal latent noise.
+* ``rlt_noise_hash24``      the 24-bit uniforms behind that noise.
+* ``rlt_paged_gather``      page-table gather into dense rows (for checks).
+* ``rlt_validate_batch``    host validation of page tables and append slots.
+* ``rlt_get_device_error``  read and clear the kernels' error bits.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = [
+    "RltError", "KVPool", "library_path", "load", "rlt_bank_map", "rlt_kv_append",
+    "rlt_paged_decode_workspace_size", "rlt_paged_decode_attn", "rlt_latent_noise_init",
+    "rlt_noise_hash24", "rlt_paged_gather", "rlt_validate_batch", "rlt_get_device_error",
+    "rlt_version", "DEVERR_BAD_PAGE", "DEVERR_BAD_SLOT", "DEVERR_TIMEOUT", "DEVERR_BAD_LEN",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "librlt.so")
+
+STATUS = {0: "RLT_OK", 1: "RLT_ERR_INVALID_ARG", 2: "RLT_ERR_OUT_OF_RANGE", 3: "RLT_ERR_UNSUPPORTED",
+          4: "RLT_ERR_WORKSPACE_TOO_SMALL", 5: "RLT_ERR_CUDA"}
+DEVERR_BAD_PAGE, DEVERR_BAD_SLOT, DEVERR_TIMEOUT, DEVERR_BAD_LEN = 1, 2, 4, 8
+
+
+class RltError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+class rlt_kv_pool(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_pages", ctypes.c_int64),
+                ("num_banks", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load librlt.so; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it with paged_kv_looped_gb300.build.build() "
+                           "(nvcc, sm_103a); this package has no CPU fallback")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    pool_p = ctypes.POINTER(rlt_kv_pool)
+    sigs = {
+        "rlt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "rlt_version": (i32, []),
+        "rlt_bank_map": (i32, [P, i32, i32, P]),
+        "rlt_kv_append": (ctypes.c_int, [pool_p, i32, P, P, P, i32, P]),
+        "rlt_paged_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
+        "rlt_paged_decode_attn": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, P, i32, i32, f32, P, P, P,
+                                                 sz, i32, P]),
+        "rlt_latent_noise_init": (ctypes.c_int, [P, P, P, i64, i32, f32, P]),
+        "rlt_noise_hash24": (ctypes.c_int, [P, P, P, i64, i32, P]),
+        "rlt_paged_gather": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, i32, P, P, P]),
+        "rlt_validate_batch": (ctypes.c_int, [P, i32, P, i32, P, i64, i32]),
+        "rlt_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise RltError(status, where)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t, dtype, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+class KVPool:
+    """A paged KV pool: bf16 CUDA tensors k, v of shape [banks][pages][Hkv][page_size][D]."""
+
+    def __init__(self, k, v):
+        import torch
+        if k.shape != v.shape or k.dim() != 5:
+            raise ValueError("k and v must both be [banks][pages][kv_heads][page_size][head_dim]")
+        _dev(k, torch.bfloat16, "k")
+        _dev(v, torch.bfloat16, "v")
+        self.k, self.v = k, v
+        nb, P, Hkv, ps, D = k.shape
+        self.num_banks, self.num_pages, self.num_kv_heads, self.page_size, self.head_dim = nb, P, Hkv, ps, D
+        self.struct = rlt_kv_pool(k.data_ptr(), v.data_ptr(), P, nb, Hkv, ps, D)
+
+    @classmethod
+    def empty(cls, num_banks, num_pages, num_kv_heads, page_size, head_dim, device="cuda"):
+        import torch
+        shape = (num_banks, num_pages, num_kv_heads, page_size, head_dim)
+        return cls(torch.empty(shape, dtype=torch.bfloat16, device=device),
+                   torch.empty(shape, dtype=torch.bfloat16, device=device))
+
+
+# ---------------------------------------------------------------- host calls
+
+def rlt_version() -> int:
+    return int(load().rlt_version())
+
+
+def rlt_bank_map(recurrent, num_planes: int):
+    """(map int32 [num_layers][num_planes], num_banks); -1 where a plane does not hold a layer."""
+    rec, rp = _host(recurrent, np.uint8)
+    out = np.empty((rec.size, num_planes), np.int32)
+    n = load().rlt_bank_map(rp, rec.size, num_planes, out.ctypes.data_as(ctypes.c_void_p))
+    if n < 0:
+        raise RltError(-n, "rlt_bank_map")
+    return out, int(n)
+
+
+def rlt_validate_batch(page_table, seq_lens, new_slots, num_pages: int, page_size: int) -> int:
+    """Host check of a decode batch; returns the status code (0 = valid)."""
+    pt, ptp = _host(page_table, np.int32)
+    sl, slp = _host(seq_lens, np.int32)
+    ns, nsp = (None, None) if new_slots is None else _host(new_slots, np.int64)
+    return int(load().rlt_validate_batch(ptp, pt.shape[1] if pt.ndim == 2 else 0, slp, sl.size, nsp,
+                                         num_pages, page_size))
+
+
+def rlt_get_device_error() -> int:
+    """Read and clear the device error bits of the current device (synchronises it)."""
+    v = ctypes.c_uint32(0)
+    _check(load().rlt_get_device_error(ctypes.byref(v)), "rlt_get_device_error")
+    return int(v.value)
+
+
+# ------------------------------------------------------------- device calls
+
+def rlt_kv_append(pool: KVPool, bank: int, k_new, v_new, out_loc, stream=None):
+    """store_kv: k_new/v_new bf16 [N][Hkv][D], out_loc int64 [N] (negative = skip)."""
+    import torch
+    n = int(out_loc.numel())
+    if k_new.shape != (n, pool.num_kv_heads, pool.head_dim) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [N][num_kv_heads][head_dim] with N = out_loc.numel()")
+    _check(load().rlt_kv_append(ctypes.byref(pool.struct), bank, _dev(k_new, torch.bfloat16, "k_new"),
+                                _dev(v_new, torch.bfloat16, "v_new"), _dev(out_loc, torch.int64, "out_loc"),
+                                n, _stream(stream)), "rlt_kv_append")
+
+
+def rlt_paged_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                                    split_tokens=0) -> int:
+    return int(load().rlt_paged_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                      max_seq_len, split_tokens))
+
+
+def rlt_paged_decode_attn(pool: KVPool, bank: int, q, page_table, seq_lens, max_seq_len: int,
+                          out=None, lse_out=None, workspace=None, scale: float = 0.0,
+                          split_tokens: int = 0, stream=None):
+    """Paged decode attention of one bank. q bf16 [B][Hq][D]; page_table int32 [B][max_pages];
+    seq_lens int32 [B].  Returns out (bf16 [B][Hq][D])."""
+    import torch
+    B, Hq, D = q.shape
+    if D != pool.head_dim:
+        raise ValueError("q head_dim does not match the pool")
+    if out is None:
+        out = torch.empty_like(q)
+    ws_need = rlt_paged_decode_workspace_size(B, Hq, pool.num_kv_heads, D, max_seq_len, split_tokens)
+    if workspace is None and ws_need > 0:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else ctypes.c_void_p(0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    lse_ptr = _dev(lse_out, torch.float32, "lse_out") if lse_out is not None else ctypes.c_void_p(0)
+    if page_table.dim() != 2 or page_table.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("page_table must be [B][max_pages] and seq_lens [B]")
+    _check(load().rlt_paged_decode_attn(
+        ctypes.byref(pool.struct), bank, _dev(q, torch.bfloat16, "q"), Hq,
+        _dev(page_table, torch.int32, "page_table"), page_table.shape[1],
+        _dev(seq_lens, torch.int32, "seq_lens"), B, int(max_seq_len), float(scale),
+        _dev(out, torch.bfloat16, "out"), lse_ptr, ws_ptr, ws_bytes, int(split_tokens),
+        _stream(stream)), "rlt_paged_decode_attn")
+    return out
+
+
+def rlt_latent_noise_init(seeds, positions, channels: int, initializer_range: float, out=None,
+                          stream=None):
+    """fp32 [rows][channels] truncated-normal noise keyed by (seed, position, channel)."""
+    import torch
+    n = int(seeds.numel())
+    if positions.numel() != n:
+        raise ValueError("seeds and positions must have one entry per row")
+    if out is None:
+        out = torch.empty((n, channels), dtype=torch.float32, device=seeds.device)
+    _check(load().rlt_latent_noise_init(_dev(out, torch.float32, "out"), _dev(seeds, torch.uint64, "seeds")
+                                        if seeds.dtype == torch.uint64 else _dev(seeds, torch.int64, "seeds"),
+                                        _dev(positions, torch.int64, "positions"), n, channels,
+                                        float(initializer_range), _stream(stream)),
+           "rlt_latent_noise_init")
+    return out
+
+
+def rlt_noise_hash24(seeds, positions, channels: int, out=None, stream=None):
+    """uint32-valued (stored as int32) [rows][channels] 24-bit uniforms of the noise."""
+    import torch
+    n = int(seeds.numel())
+    if out is None:
+        out = torch.empty((n, channels), dtype=torch.int32, device=seeds.device)
+    _check(load().rlt_noise_hash24(_dev(out, torch.int32, "out"), _dev(seeds, seeds.dtype, "seeds"),
+                                   _dev(positions, torch.int64, "positions"), n, channels,
+                                   _stream(stream)), "rlt_noise_hash24")
+    return out
+
+
+def rlt_paged_gather(pool: KVPool, bank: int, page_table, seq_lens, max_len: int, k_out=None,
+                     v_out=None, stream=None):
+    """Dense bf16 [B][max_len][Hkv][D] copies of each request's cached K and V rows."""
+    import torch
+    B = int(seq_lens.numel())
+    shape = (B, max_len, pool.num_kv_heads, pool.head_dim)
+    if k_out is None:
+        k_out = torch.zeros(shape, dtype=torch.bfloat16, device=pool.k.device)
+    if v_out is None:
+        v_out = torch.zeros(shape, dtype=torch.bfloat16, device=pool.k.device)
+    _check(load().rlt_paged_gather(ctypes.byref(pool.struct), bank, _dev(page_table, torch.int32, "page_table"),
+                                   page_table.shape[1], _dev(seq_lens, torch.int32, "seq_lens"), B,
+                                   int(max_len), _dev(k_out, torch.bfloat16, "k_out"),
+                                   _dev(v_out, torch.bfloat16, "v_out"), _stream(stream)),
+           "rlt_paged_gather")
+    return k_out, v_out

@@ -1,0 +1,352 @@
+// extern "C" entry points of librlt: host-side argument checks, launch
+// planning and dispatch to the kernels.  Nothing here allocates device memory.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+#include <unordered_set>
+
+#include "rlt.h"
+#include "rlt_internal.h"
+
+namespace {
+
+// Per-device error word the kernels OR their RLT_DEVERR_* bits into.
+__device__ unsigned int g_device_error;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+unsigned int *g_err_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+
+bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
+// Device address of the error word and the SM count of the current device,
+// looked up once per device.
+rlt_status device_info(unsigned int **err, int *num_sms)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return RLT_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_err_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess)
+            return RLT_ERR_CUDA;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return RLT_ERR_CUDA;
+        g_num_sms[dev] = sms;
+        g_err_ptr[dev] = static_cast<unsigned int *>(p);
+    }
+    if (err != nullptr)
+        *err = g_err_ptr[dev];
+    if (num_sms != nullptr)
+        *num_sms = g_num_sms[dev];
+    return RLT_OK;
+}
+
+int current_sms()
+{
+    int sms = 0;
+    if (device_info(nullptr, &sms) != RLT_OK)
+        return 0;
+    return sms;
+}
+
+rlt_status check_pool(const rlt_kv_pool *pool, int32_t bank)
+{
+    if (pool == nullptr || pool->k == nullptr || pool->v == nullptr)
+        return RLT_ERR_INVALID_ARG;
+    if (pool->num_pages < 0 || pool->num_banks < 1 || pool->num_kv_heads < 1 ||
+        pool->page_size < 1 || pool->head_dim < 8 || pool->head_dim % 8 != 0)
+        return RLT_ERR_INVALID_ARG;
+    if (!aligned16(pool->k) || !aligned16(pool->v))
+        return RLT_ERR_INVALID_ARG;
+    if (bank < 0 || bank >= pool->num_banks)
+        return RLT_ERR_OUT_OF_RANGE;
+    return RLT_OK;
+}
+
+int64_t bank_elems(const rlt_kv_pool *pool)
+{
+    return pool->num_pages * pool->num_kv_heads * pool->page_size * (int64_t)pool->head_dim;
+}
+
+rlt_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RLT_OK : RLT_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+RLT_API const char *rlt_status_string(rlt_status status)
+{
+    switch (status) {
+    case RLT_OK: return "RLT_OK";
+    case RLT_ERR_INVALID_ARG: return "RLT_ERR_INVALID_ARG";
+    case RLT_ERR_OUT_OF_RANGE: return "RLT_ERR_OUT_OF_RANGE";
+    case RLT_ERR_UNSUPPORTED: return "RLT_ERR_UNSUPPORTED";
+    case RLT_ERR_WORKSPACE_TOO_SMALL: return "RLT_ERR_WORKSPACE_TOO_SMALL";
+    case RLT_ERR_CUDA: return "RLT_ERR_CUDA";
+    }
+    return "RLT_ERR_UNKNOWN";
+}
+
+RLT_API int32_t rlt_version(void) { return 100; }
+
+RLT_API int32_t rlt_bank_map(const uint8_t *recurrent, int32_t num_layers, int32_t num_planes,
+                             int32_t *map_out)
+{
+    if (recurrent == nullptr || map_out == nullptr || num_layers < 1 || num_planes < 1)
+        return -RLT_ERR_INVALID_ARG;
+    int32_t next = 0;
+    for (int32_t t = 0; t < num_planes; ++t)
+        for (int32_t l = 0; l < num_layers; ++l)
+            map_out[l * num_planes + t] = (t == 0 || recurrent[l] != 0) ? next++ : -1;
+    return next;
+}
+
+RLT_API rlt_status rlt_kv_append(const rlt_kv_pool *pool, int32_t bank, const void *k_new,
+                                 const void *v_new, const int64_t *out_loc, int32_t n_tokens,
+                                 void *stream)
+{
+    rlt_status st = check_pool(pool, bank);
+    if (st != RLT_OK)
+        return st;
+    if (n_tokens < 0)
+        return RLT_ERR_INVALID_ARG;
+    if (n_tokens == 0)
+        return RLT_OK;
+    if (k_new == nullptr || v_new == nullptr || out_loc == nullptr)
+        return RLT_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || reinterpret_cast<uintptr_t>(out_loc) % 8 != 0)
+        return RLT_ERR_INVALID_ARG;
+    unsigned int *err = nullptr;
+    if ((st = device_info(&err, nullptr)) != RLT_OK)
+        return st;
+    const int64_t off = bank * bank_elems(pool);
+    return from_cuda(rlt::launch_append(
+        static_cast<uint16_t *>(pool->k) + off, static_cast<uint16_t *>(pool->v) + off,
+        static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new), out_loc,
+        n_tokens, pool->num_kv_heads, pool->page_size, pool->head_dim, pool->num_pages, err,
+        static_cast<cudaStream_t>(stream)));
+}
+
+RLT_API size_t rlt_paged_decode_workspace_size(int32_t batch, int32_t num_q_heads,
+                                               int32_t num_kv_heads, int32_t head_dim,
+                                               int32_t max_seq_len, int32_t split_tokens)
+{
+    if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || max_seq_len < 0 ||
+        split_tokens < 0)
+        return 0;
+    return rlt::plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                            split_tokens, current_sms())
+        .workspace_bytes;
+}
+
+RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, const void *q,
+                                         int32_t num_q_heads, const int32_t *page_table,
+                                         int32_t max_pages, const int32_t *seq_lens,
+                                         int32_t batch, int32_t max_seq_len, float scale,
+                                         void *out, float *lse_out, void *workspace,
+                                         size_t workspace_bytes, int32_t split_tokens,
+                                         void *stream)
+{
+    rlt_status st = check_pool(pool, bank);
+    if (st != RLT_OK)
+        return st;
+    if (batch < 0 || max_seq_len < 0 || max_pages < 0 || num_q_heads < 1 || split_tokens < 0 ||
+        split_tokens % rlt::kTileTokens != 0 || split_tokens > 128 * rlt::kTileTokens)
+        return RLT_ERR_INVALID_ARG;
+    if (num_q_heads % pool->num_kv_heads != 0)
+        return RLT_ERR_INVALID_ARG;
+    const int group = num_q_heads / pool->num_kv_heads;
+    if (!rlt::decode_supported(pool->head_dim, group) || pool->page_size % rlt::kTileTokens != 0)
+        return RLT_ERR_UNSUPPORTED;
+    if (batch > 65535 || pool->num_kv_heads > 65535)
+        return RLT_ERR_UNSUPPORTED;
+    if (batch == 0)
+        return RLT_OK;
+    if (q == nullptr || page_table == nullptr || seq_lens == nullptr || out == nullptr ||
+        max_pages < 1)
+        return RLT_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || (workspace != nullptr && !aligned16(workspace)))
+        return RLT_ERR_INVALID_ARG;
+    if (!std::isfinite(scale))
+        return RLT_ERR_INVALID_ARG;
+
+    unsigned int *err = nullptr;
+    int sms = 0;
+    if ((st = device_info(&err, &sms)) != RLT_OK)
+        return st;
+    const rlt::DecodePlan plan = rlt::plan_decode(batch, num_q_heads, pool->num_kv_heads,
+                                                  pool->head_dim, max_seq_len, split_tokens, sms);
+    if (plan.workspace_bytes > 0 && (workspace == nullptr || workspace_bytes < plan.workspace_bytes))
+        return RLT_ERR_WORKSPACE_TOO_SMALL;
+
+    rlt::DecodeParams p{};
+    const int64_t off = bank * bank_elems(pool);
+    p.k_bank = static_cast<const uint16_t *>(pool->k) + off;
+    p.v_bank = static_cast<const uint16_t *>(pool->v) + off;
+    p.q = static_cast<const uint16_t *>(q);
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.out = static_cast<uint16_t *>(out);
+    p.lse_out = lse_out;
+    p.lse_part = static_cast<float *>(workspace);
+    p.o_part = workspace != nullptr
+                   ? reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.lse_part_bytes)
+                   : nullptr;
+    p.err = err;
+    p.num_pages = pool->num_pages;
+    p.num_kv_heads = pool->num_kv_heads;
+    p.num_q_heads = num_q_heads;
+    p.page_size = pool->page_size;
+    p.max_pages = max_pages;
+    p.batch = batch;
+    p.tiles_per_split = plan.tiles_per_split;
+    p.max_splits = plan.max_splits;
+    const double s = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)pool->head_dim);
+    p.qscale = (float)(s * 1.4426950408889634);   // log2(e): softmax in base 2
+    return from_cuda(rlt::launch_decode(p, pool->head_dim, group, static_cast<cudaStream_t>(stream)));
+}
+
+RLT_API rlt_status rlt_latent_noise_init(float *out, const uint64_t *seeds,
+                                         const int64_t *positions, int64_t n_rows,
+                                         int32_t channels, float initializer_range, void *stream)
+{
+    if (n_rows < 0 || channels < 1 || !std::isfinite(initializer_range))
+        return RLT_ERR_INVALID_ARG;
+    if (n_rows == 0)
+        return RLT_OK;
+    if (out == nullptr || seeds == nullptr || positions == nullptr)
+        return RLT_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(out) % 4 != 0 || reinterpret_cast<uintptr_t>(seeds) % 8 != 0 ||
+        reinterpret_cast<uintptr_t>(positions) % 8 != 0)
+        return RLT_ERR_INVALID_ARG;
+    return from_cuda(rlt::launch_noise(out, nullptr, seeds, positions, n_rows, channels,
+                                       initializer_range, static_cast<cudaStream_t>(stream)));
+}
+
+RLT_API rlt_status rlt_noise_hash24(uint32_t *out, const uint64_t *seeds, const int64_t *positions,
+                                    int64_t n_rows, int32_t channels, void *stream)
+{
+    if (n_rows < 0 || channels < 1)
+        return RLT_ERR_INVALID_ARG;
+    if (n_rows == 0)
+        return RLT_OK;
+    if (out == nullptr || seeds == nullptr || positions == nullptr)
+        return RLT_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(out) % 4 != 0 || reinterpret_cast<uintptr_t>(seeds) % 8 != 0 ||
+        reinterpret_cast<uintptr_t>(positions) % 8 != 0)
+        return RLT_ERR_INVALID_ARG;
+    return from_cuda(rlt::launch_noise(nullptr, out, seeds, positions, n_rows, channels, 0.f,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+RLT_API rlt_status rlt_paged_gather(const rlt_kv_pool *pool, int32_t bank,
+                                    const int32_t *page_table, int32_t max_pages,
+                                    const int32_t *seq_lens, int32_t batch, int32_t max_len,
+                                    void *k_out, void *v_out, void *stream)
+{
+    rlt_status st = check_pool(pool, bank);
+    if (st != RLT_OK)
+        return st;
+    if (batch < 0 || max_len < 0 || max_pages < 0)
+        return RLT_ERR_INVALID_ARG;
+    if (batch == 0 || max_len == 0)
+        return RLT_OK;
+    if (page_table == nullptr || seq_lens == nullptr || k_out == nullptr || v_out == nullptr ||
+        max_pages < 1)
+        return RLT_ERR_INVALID_ARG;
+    if (!aligned16(k_out) || !aligned16(v_out))
+        return RLT_ERR_INVALID_ARG;
+    unsigned int *err = nullptr;
+    if ((st = device_info(&err, nullptr)) != RLT_OK)
+        return st;
+    const int64_t off = bank * bank_elems(pool);
+    return from_cuda(rlt::launch_gather(
+        static_cast<const uint16_t *>(pool->k) + off, static_cast<const uint16_t *>(pool->v) + off,
+        page_table, max_pages, seq_lens, batch, max_len, static_cast<uint16_t *>(k_out),
+        static_cast<uint16_t *>(v_out), pool->num_kv_heads, pool->page_size, pool->head_dim,
+        pool->num_pages, err, static_cast<cudaStream_t>(stream)));
+}
+
+RLT_API rlt_status rlt_validate_batch(const int32_t *page_table, int32_t max_pages,
+                                      const int32_t *seq_lens, int32_t batch,
+                                      const int64_t *new_slots, int64_t num_pages,
+                                      int32_t page_size)
+{
+    if (batch < 0 || max_pages < 0 || num_pages < 0 || page_size < 1)
+        return RLT_ERR_INVALID_ARG;
+    if (batch == 0)
+        return RLT_OK;
+    if (page_table == nullptr || seq_lens == nullptr)
+        return RLT_ERR_INVALID_ARG;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t L = seq_lens[b];
+        if (L < 0 || L > (int64_t)max_pages * page_size)
+            return RLT_ERR_OUT_OF_RANGE;
+        const int64_t n = (L + page_size - 1) / page_size;
+        for (int64_t i = 0; i < n; ++i) {
+            const int64_t page = page_table[(int64_t)b * max_pages + i];
+            if (page < 0 || page >= num_pages)
+                return RLT_ERR_OUT_OF_RANGE;
+        }
+    }
+    if (new_slots == nullptr)
+        return RLT_OK;
+    std::unordered_set<int64_t> slots, write_pages;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t slot = new_slots[b];
+        if (slot < 0)
+            continue;
+        const int64_t L = seq_lens[b];
+        if (L < 1 || slot >= num_pages * page_size)
+            return RLT_ERR_OUT_OF_RANGE;
+        const int64_t last_page = page_table[(int64_t)b * max_pages + (L - 1) / page_size];
+        if (slot / page_size != last_page || slot % page_size != (L - 1) % page_size)
+            return RLT_ERR_OUT_OF_RANGE;
+        if (!slots.insert(slot).second)
+            return RLT_ERR_INVALID_ARG;            // two requests append to one slot
+        write_pages.insert(last_page);
+    }
+    // A page that receives a new token must belong to exactly one request.
+    std::unordered_set<int64_t> seen_in_request;
+    std::unordered_set<int64_t> owned;
+    for (int32_t b = 0; b < batch; ++b) {
+        seen_in_request.clear();
+        const int64_t n = ((int64_t)seq_lens[b] + page_size - 1) / page_size;
+        for (int64_t i = 0; i < n; ++i) {
+            const int64_t page = page_table[(int64_t)b * max_pages + i];
+            if (write_pages.count(page) == 0 || !seen_in_request.insert(page).second)
+                continue;
+            if (!owned.insert(page).second)
+                return RLT_ERR_INVALID_ARG;        // append into a shared (read-only) page
+        }
+    }
+    return RLT_OK;
+}
+
+RLT_API rlt_status rlt_get_device_error(uint32_t *error_bits)
+{
+    if (error_bits == nullptr)
+        return RLT_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess)
+        return RLT_ERR_CUDA;
+    unsigned int *err = nullptr;
+    rlt_status st = device_info(&err, nullptr);
+    if (st != RLT_OK)
+        return st;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return RLT_ERR_CUDA;
+    const unsigned int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+        return RLT_ERR_CUDA;
+    *error_bits = v;
+    return RLT_OK;
+}
+
+}  // extern "C"

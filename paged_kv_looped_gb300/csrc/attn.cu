@@ -1,0 +1,526 @@
+// Paged GQA decode attention for sm_103a: split-K partial kernel + LSE combine.
+//
+// What it computes ("Faster fuzzy minds", "When scheduler does the work" and
+// "Recurrent depth"): for every request b and query head h, softmax(q K^T *
+// scale) V over the seq_lens[b] cached tokens of b, gathered page by page
+// through the page table from one (layer, plane) bank of the pool.
+//
+// Design (HBM-bound: every K/V byte is read once and used by the G query heads
+// of its kv head):
+//  * One CTA per (split, kv head, request); a split is a run of 16-token tiles.
+//  * Pool layout [page][kv_head][offset][D] makes the 16 rows of a tile one
+//    contiguous chunk, so each tile is two `cp.async.bulk` copies (K and V) of
+//    16*D*2 bytes straight into shared memory, completing on an mbarrier.
+//  * The 4 warps of a CTA take tiles round-robin; each warp runs its own
+//    2-stage copy ring and its own online softmax, so no CTA-wide barrier is
+//    crossed until the final merge.
+//  * Inside a tile a half-warp holds 8 token rows, each lane D/16 dims:
+//    16-byte (D=128) shared loads without bank conflicts, scores reduced by a
+//    transpose butterfly (8 shuffles for 8 tokens), probabilities broadcast
+//    through shared memory for the P.V accumulation.
+//  * Splits write (o, log2-sum-exp) partials; the combine kernel merges them.
+//    Requests with one split write their output directly.
+#include <math_constants.h>
+
+#include "rlt_device.cuh"
+#include "rlt_internal.h"
+
+namespace rlt {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 2;                   // copy ring depth per warp
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D, int G>
+struct Cfg {
+    static constexpr int kDpl = D / 16;                          // dims per lane
+    static constexpr int kTileBytes = kTileTokens * D * 2;       // K (or V) rows of a tile
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kPipeBytes = kWarps * kStages * kStageBytes;
+    static constexpr int kMergeStride = D + 4;                   // floats per (warp, head)
+    static constexpr int kMergeBytes = kWarps * G * kMergeStride * 4;
+    static constexpr int kRegionBytes = kPipeBytes > kMergeBytes ? kPipeBytes : kMergeBytes;
+    static constexpr int kPBytes = kWarps * G * kTileTokens * 4;
+    static constexpr int kBarOffset = kRegionBytes + kPBytes;
+    static constexpr int kSmemBytes = kBarOffset + kWarps * kStages * 8;
+};
+
+// Length of request b as the kernels use it: seq_lens[b] clamped to what the
+// page table row and the split grid can hold (a clamp is recorded as an error).
+__device__ __forceinline__ int effective_len(const DecodeParams &p, int b, bool report)
+{
+    int L = p.seq_lens[b];
+    const int64_t cap_pages = (int64_t)p.max_pages * p.page_size;
+    const int64_t cap_grid = (int64_t)p.max_splits * p.tiles_per_split * kTileTokens;
+    const int cap = (int)(cap_pages < cap_grid ? cap_pages : cap_grid);
+    if (L < 0 || L > cap) {
+        if (report)
+            record_error(p.err, RLT_DEVERR_BAD_LEN);
+        L = L < 0 ? 0 : cap;
+    }
+    return L;
+}
+
+template <int DPL>
+__device__ __forceinline__ void load_frag(const unsigned char *src, float (&f)[DPL])
+{
+    if constexpr (DPL == 8) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(src);
+        f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+        f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z); f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
+    } else {
+        static_assert(DPL == 4, "head_dim 64 or 128");
+        const uint2 w = *reinterpret_cast<const uint2 *>(src);
+        f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+    }
+}
+
+template <int DPL>
+__device__ __forceinline__ void load_frag_global(const uint16_t *src, float (&f)[DPL])
+{
+    load_frag<DPL>(reinterpret_cast<const unsigned char *>(src), f);
+}
+
+// acc[h] += p[h][t] * V_t for the 8 rows t of this lane's half of a tile.  In
+// the last tile of a request, rows past its end are skipped: that pool memory
+// may hold anything, even NaN patterns, and 0 * NaN would poison the sum.
+template <int D, int G, bool kMasked>
+__device__ __forceinline__ void pv_tile(const unsigned char *vs, const float *pbuf, int half,
+                                        int j, int valid, float (&acc)[G][D / 16])
+{
+    constexpr int DPL = D / 16;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        if (kMasked && half * 8 + r >= valid)
+            continue;
+        float vf[DPL];
+        load_frag<DPL>(vs + ((half * 8 + r) * D + j * DPL) * 2, vf);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float pw = pbuf[h * kTileTokens + half * 8 + r];
+#pragma unroll
+            for (int d = 0; d < DPL; ++d)
+                acc[h][d] = fmaf(pw, vf[d], acc[h][d]);
+        }
+    }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads) decode_partial_kernel(const DecodeParams p)
+{
+    using C = Cfg<D, G>;
+    constexpr int DPL = C::kDpl;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int split = blockIdx.x;
+    const int g = blockIdx.y;
+    const int b = blockIdx.z;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int half = lane >> 4;                // which 8 rows of a tile
+    const int j = lane & 15;                   // which D/16 dims
+
+    const int L = effective_len(p, b, split == 0 && g == 0 && threadIdx.x == 0);
+    const int n_tiles = (L + kTileTokens - 1) / kTileTokens;
+    const int n_splits = (n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+
+    if (n_splits == 0) {                        // empty request: out = 0, lse = -inf
+        if (split == 0) {
+            for (int i = threadIdx.x; i < G * D / 2; i += kThreads) {
+                const int h = i / (D / 2), d2 = i % (D / 2);
+                reinterpret_cast<uint32_t *>(
+                    p.out + ((int64_t)b * p.num_q_heads + g * G + h) * D)[d2] = 0u;
+            }
+            if (p.lse_out != nullptr && threadIdx.x < G)
+                p.lse_out[(int64_t)b * p.num_q_heads + g * G + threadIdx.x] = -CUDART_INF_F;
+        }
+        return;
+    }
+    if (split >= n_splits)
+        return;
+
+    const int tile_begin = split * p.tiles_per_split;
+    const int tile_end = min(tile_begin + p.tiles_per_split, n_tiles);
+    const int my_first = tile_begin + warp;
+    const int my_count = my_first < tile_end ? (tile_end - my_first + kWarps - 1) / kWarps : 0;
+
+    unsigned char *pipe = smem + warp * kStages * C::kStageBytes;
+    float *pbuf = reinterpret_cast<float *>(smem + C::kRegionBytes) + warp * G * kTileTokens;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOffset) + warp * kStages;
+
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s)
+            mbar_init(&bars[s], 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+
+    // Page and in-page offset of this warp's i-th tile live in lane i.
+    int my_page = -1, my_off = 0;
+    if (lane < my_count) {
+        const int tok = (my_first + lane * kWarps) * kTileTokens;
+        const int page = p.page_table[(int64_t)b * p.max_pages + tok / p.page_size];
+        if (page >= 0 && (int64_t)page < p.num_pages)
+            my_page = page;
+        else
+            record_error(p.err, RLT_DEVERR_BAD_PAGE);
+        my_off = tok % p.page_size;
+    }
+
+    auto issue = [&](int i) {
+        const int page = __shfl_sync(kFullMask, my_page, i);
+        const int off = __shfl_sync(kFullMask, my_off, i);
+        if (lane == 0 && page >= 0) {
+            uint64_t *bar = &bars[i % kStages];
+            unsigned char *dst = pipe + (i % kStages) * C::kStageBytes;
+            const int64_t row = ((int64_t)page * p.num_kv_heads + g) * p.page_size + off;
+            mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+            bulk_load(dst, p.k_bank + row * D, C::kTileBytes, bar);
+            bulk_load(dst + C::kTileBytes, p.v_bank + row * D, C::kTileBytes, bar);
+        }
+    };
+
+    // Query heads g*G .. g*G+G-1, this lane's dims, pre-scaled into log2 units.
+    float q[G][DPL];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        load_frag_global<DPL>(p.q + ((int64_t)b * p.num_q_heads + g * G + h) * D + j * DPL, q[h]);
+#pragma unroll
+        for (int d = 0; d < DPL; ++d)
+            q[h][d] *= p.qscale;
+    }
+
+    float m[G], l[G], acc[G][DPL];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m[h] = -CUDART_INF_F;
+        l[h] = 0.f;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d)
+            acc[h][d] = 0.f;
+    }
+
+    const int n_pre = my_count < kStages ? my_count : kStages;
+    for (int i = 0; i < n_pre; ++i)
+        issue(i);
+    int issued = n_pre;
+    uint32_t phase = 0;                        // bit s: parity of stage s's next phase
+    int failed_at = -1;
+
+    for (int i = 0; i < my_count; ++i) {
+        const int s = i % kStages;
+        const int page = __shfl_sync(kFullMask, my_page, i);
+        if (page >= 0) {
+            const bool arrived = __all_sync(kFullMask, mbar_wait(&bars[s], (phase >> s) & 1u));
+            if (!arrived) {
+                failed_at = i;
+                break;
+            }
+            phase ^= 1u << s;
+
+            const int valid = min(kTileTokens, L - (my_first + i * kWarps) * kTileTokens);
+            const unsigned char *ks = pipe + s * C::kStageBytes;
+            const unsigned char *vs = ks + C::kTileBytes;
+
+            // Partial dot products of this lane's dims for its half's 8 rows.
+            float sc[G][8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                float kf[DPL];
+                load_frag<DPL>(ks + ((half * 8 + r) * D + j * DPL) * 2, kf);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float a = 0.f;
+#pragma unroll
+                    for (int d = 0; d < DPL; ++d)
+                        a = fmaf(q[h][d], kf[d], a);
+                    sc[h][r] = a;
+                }
+            }
+            // Transpose butterfly over the 16 lanes of the half: afterwards lane j
+            // holds the full score of row j>>1 (lanes j and j^1 agree).
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const bool up = j & 8;
+                    const float send = up ? sc[h][k] : sc[h][k + 4];
+                    const float keep = up ? sc[h][k + 4] : sc[h][k];
+                    sc[h][k] = keep + __shfl_xor_sync(kFullMask, send, 8);
+                }
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const bool up = j & 4;
+                    const float send = up ? sc[h][k] : sc[h][k + 2];
+                    const float keep = up ? sc[h][k + 2] : sc[h][k];
+                    sc[h][k] = keep + __shfl_xor_sync(kFullMask, send, 4);
+                }
+                {
+                    const bool up = j & 2;
+                    const float send = up ? sc[h][0] : sc[h][1];
+                    const float keep = up ? sc[h][1] : sc[h][0];
+                    sc[h][0] = keep + __shfl_xor_sync(kFullMask, send, 2);
+                }
+                sc[h][0] += __shfl_xor_sync(kFullMask, sc[h][0], 1);
+            }
+
+            // Online softmax update (log2 domain), one running max per head.
+            const int t = half * 8 + (j >> 1);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float s_t = t < valid ? sc[h][0] : -CUDART_INF_F;
+                const float m_new = fmaxf(m[h], warp_max_xor(s_t, 2));
+                const float alpha = exp2f(m[h] - m_new);
+                const float pr = exp2f(s_t - m_new);
+                l[h] = l[h] * alpha + ((j & 1) ? 0.f : pr);
+#pragma unroll
+                for (int d = 0; d < DPL; ++d)
+                    acc[h][d] *= alpha;
+                m[h] = m_new;
+                if ((j & 1) == 0)
+                    pbuf[h * kTileTokens + t] = pr;
+            }
+            __syncwarp();
+
+            // acc += p_t * V_t over this half's rows.
+            if (valid == kTileTokens)
+                pv_tile<D, G, false>(vs, pbuf, half, j, valid, acc);
+            else
+                pv_tile<D, G, true>(vs, pbuf, half, j, valid, acc);
+        }
+        __syncwarp();
+        fence_proxy_async();                   // our reads of stage s before its next refill
+        if (issued < my_count && issued == i + kStages) {
+            issue(issued);
+            ++issued;
+        }
+    }
+
+    if (failed_at >= 0) {
+        // A copy never arrived: record it, then wait (bounded) for this warp's
+        // copies still in flight before the shared memory is given up.
+        if (lane == 0)
+            record_error(p.err, RLT_DEVERR_TIMEOUT);
+        for (int k = failed_at; k < issued; ++k) {
+            const int s = k % kStages;
+            if (__shfl_sync(kFullMask, my_page, k) >= 0) {
+                mbar_wait(&bars[s], (phase >> s) & 1u);
+                phase ^= 1u << s;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            m[h] = -CUDART_INF_F;
+            l[h] = 0.f;
+        }
+    }
+
+    // Fold the two halves (same dims, different rows) and the per-lane sums.
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int d = 0; d < DPL; ++d)
+            acc[h][d] += __shfl_xor_sync(kFullMask, acc[h][d], 16);
+        l[h] = warp_sum_xor(l[h], 1);
+    }
+
+    // Merge the 4 warps through shared memory (aliases the copy rings).
+    __syncthreads();
+    float *mg = reinterpret_cast<float *>(smem);
+    if (half == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int d = 0; d < DPL; ++d)
+                mg[(warp * G + h) * C::kMergeStride + j * DPL + d] = acc[h][d];
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            mg[(warp * G + h) * C::kMergeStride + D] = m[h];
+            mg[(warp * G + h) * C::kMergeStride + D + 1] = l[h];
+        }
+    }
+    __syncthreads();
+
+    for (int item = threadIdx.x; item < G * D / 4; item += kThreads) {
+        const int h = item / (D / 4);
+        const int d0 = (item % (D / 4)) * 4;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            M = fmaxf(M, mg[(w * G + h) * C::kMergeStride + D]);
+        float ls = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+        if (M != -CUDART_INF_F) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float *row = mg + (w * G + h) * C::kMergeStride;
+                const float sc = exp2f(row[D] - M);
+                ls = fmaf(row[D + 1], sc, ls);
+                o0 = fmaf(row[d0 + 0], sc, o0);
+                o1 = fmaf(row[d0 + 1], sc, o1);
+                o2 = fmaf(row[d0 + 2], sc, o2);
+                o3 = fmaf(row[d0 + 3], sc, o3);
+            }
+        }
+        const float inv = ls > 0.f ? 1.f / ls : 0.f;
+        const float lse2 = ls > 0.f ? M + log2f(ls) : -CUDART_INF_F;
+        const int64_t bh = (int64_t)b * p.num_q_heads + g * G + h;
+        if (n_splits == 1) {
+            uint2 w;
+            w.x = pack_bf16x2(o0 * inv, o1 * inv);
+            w.y = pack_bf16x2(o2 * inv, o3 * inv);
+            *reinterpret_cast<uint2 *>(p.out + bh * D + d0) = w;
+            if (d0 == 0 && p.lse_out != nullptr)
+                p.lse_out[bh] = lse2 * kLn2;
+        } else {
+            *reinterpret_cast<float4 *>(p.o_part + (bh * p.max_splits + split) * D + d0) =
+                make_float4(o0 * inv, o1 * inv, o2 * inv, o3 * inv);
+            if (d0 == 0)
+                p.lse_part[bh * p.max_splits + split] = lse2;
+        }
+    }
+}
+
+// One warp per (request, query head): merge that request's split partials.
+template <int D>
+__global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams p)
+{
+    constexpr int DPL = D / 32;
+    const int64_t bh = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (bh >= (int64_t)p.batch * p.num_q_heads)
+        return;
+    const int b = (int)(bh / p.num_q_heads);
+    const int L = effective_len(p, b, false);
+    const int n_tiles = (L + kTileTokens - 1) / kTileTokens;
+    const int n = (n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    if (n <= 1)
+        return;                                  // written by the partial kernel
+
+    const float *lp = p.lse_part + bh * p.max_splits;
+    float M = -CUDART_INF_F;
+    for (int s = lane; s < n; s += 32)
+        M = fmaxf(M, lp[s]);
+    M = warp_max_xor(M, 1);
+
+    float acc[DPL];
+#pragma unroll
+    for (int d = 0; d < DPL; ++d)
+        acc[d] = 0.f;
+    float ls = 0.f;
+    if (M != -CUDART_INF_F) {
+        const float *op = p.o_part + bh * p.max_splits * D + lane * DPL;
+        for (int s = 0; s < n; ++s) {
+            const float w = exp2f(lp[s] - M);
+            ls += w;
+            if constexpr (DPL == 4) {
+                const float4 o = *reinterpret_cast<const float4 *>(op + (int64_t)s * D);
+                acc[0] = fmaf(w, o.x, acc[0]);
+                acc[1] = fmaf(w, o.y, acc[1]);
+                acc[2] = fmaf(w, o.z, acc[2]);
+                acc[3] = fmaf(w, o.w, acc[3]);
+            } else {
+                const float2 o = *reinterpret_cast<const float2 *>(op + (int64_t)s * D);
+                acc[0] = fmaf(w, o.x, acc[0]);
+                acc[1] = fmaf(w, o.y, acc[1]);
+            }
+        }
+    }
+    const float inv = ls > 0.f ? 1.f / ls : 0.f;
+    uint16_t *o = p.out + bh * D + lane * DPL;
+    if constexpr (DPL == 4) {
+        uint2 w;
+        w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2 *>(o) = w;
+    } else {
+        *reinterpret_cast<uint32_t *>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+    if (lane == 0 && p.lse_out != nullptr)
+        p.lse_out[bh] = ls > 0.f ? (M + log2f(ls)) * kLn2 : -CUDART_INF_F;
+}
+
+template <int D, int G>
+cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream)
+{
+    using C = Cfg<D, G>;
+    static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
+    auto kernel = decode_partial_kernel<D, G>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
+    const dim3 grid(p.max_splits, p.num_kv_heads, p.batch);
+    kernel<<<grid, kThreads, C::kSmemBytes, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || p.max_splits <= 1)
+        return e;
+    const int64_t warps = (int64_t)p.batch * p.num_q_heads;
+    const unsigned blocks = (unsigned)((warps + 7) / 8);
+    decode_combine_kernel<D><<<blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_supported(int head_dim, int group)
+{
+    return (head_dim == 64 || head_dim == 128) &&
+           (group == 1 || group == 2 || group == 4 || group == 8);
+}
+
+DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t max_seq_len, int32_t split_tokens, int num_sms)
+{
+    DecodePlan plan{};
+    const int64_t max_tiles = max_seq_len > 0 ? (max_seq_len + kTileTokens - 1) / kTileTokens : 1;
+    int tiles;
+    if (split_tokens > 0) {
+        tiles = (split_tokens + kTileTokens - 1) / kTileTokens;
+    } else {
+        // Largest split (fewest partials) that still gives every SM several
+        // waves of CTAs at 3 resident CTAs per SM.
+        const int64_t target = (int64_t)(num_sms > 0 ? num_sms : 148) * 3 * 8;
+        tiles = 128;
+        while (tiles > 8 &&
+               (int64_t)batch * num_kv_heads * ((max_tiles + tiles - 1) / tiles) < target)
+            tiles /= 2;
+    }
+    if (tiles > 128)
+        tiles = 128;                             // one page-table entry per lane per warp
+    if (tiles < 1)
+        tiles = 1;
+    plan.tiles_per_split = tiles;
+    plan.max_splits = (int32_t)((max_tiles + tiles - 1) / tiles);
+    if (plan.max_splits > 1) {
+        const size_t rows = (size_t)batch * num_q_heads * plan.max_splits;
+        plan.lse_part_bytes = (rows * sizeof(float) + 255) / 256 * 256;
+        plan.workspace_bytes = plan.lse_part_bytes + rows * head_dim * sizeof(float);
+    }
+    return plan;
+}
+
+cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, cudaStream_t stream)
+{
+    if (head_dim == 128) {
+        switch (group) {
+        case 1: return launch_typed<128, 1>(p, stream);
+        case 2: return launch_typed<128, 2>(p, stream);
+        case 4: return launch_typed<128, 4>(p, stream);
+        case 8: return launch_typed<128, 8>(p, stream);
+        }
+    } else if (head_dim == 64) {
+        switch (group) {
+        case 1: return launch_typed<64, 1>(p, stream);
+        case 2: return launch_typed<64, 2>(p, stream);
+        case 4: return launch_typed<64, 4>(p, stream);
+        case 8: return launch_typed<64, 8>(p, stream);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace rlt

@@ -1,0 +1,140 @@
+// Device helpers shared by the sm_103a kernels: bf16 unpacking, mbarrier and
+// bulk-copy (TMA, non-tensor) wrappers in inline PTX, bounded waits and the
+// device error word.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rlt.h"
+
+namespace rlt {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// A copy wait gives up after this long (nanoseconds of %globaltimer) and
+// records RLT_DEVERR_TIMEOUT instead of spinning forever.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ void record_error(unsigned int *err, unsigned int bits)
+{
+    if (err != nullptr)
+        atomicOr(err, bits);
+}
+
+// ---------------------------------------------------------------- bf16 bits
+// A bf16 value is the top half of an fp32 with the same bits.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// fp32 -> bf16 bits, round to nearest even (inputs here are finite).
+__device__ __forceinline__ uint32_t bf16_bits(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7f800000u) == 0x7f800000u)          // inf / nan: keep, quiet nan
+        return (u >> 16) | ((u & 0x007fffffu) ? 0x40u : 0u);
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return u >> 16;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    return bf16_bits(lo) | (bf16_bits(hi) << 16);
+}
+
+// ------------------------------------------------------------ shared memory
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// Make initialised barriers visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void mbar_init_fence()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for the phase with the given parity to complete; false after the time limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1; it != 0; ++it) {       // at most 2^32 - 1 tries
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 255u) == 0u && global_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+    return false;
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) writes to the same buffers.
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// One contiguous global -> shared bulk copy that completes `bytes` of the
+// barrier's transaction count.  dst and src 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// ------------------------------------------------------------- warp helpers
+__device__ __forceinline__ float warp_max_xor(float v, int from)
+{
+    for (int o = from; o < 32; o <<= 1)
+        v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum_xor(float v, int from)
+{
+    for (int o = from; o < 32; o <<= 1)
+        v += __shfl_xor_sync(kFullMask, v, o);
+    return v;
+}
+
+}  // namespace rlt

@@ -1,0 +1,65 @@
+// Host-side interface between the C-ABI entry points (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace rlt {
+
+// Tokens per attention tile: one bulk copy of K and one of V per tile.
+constexpr int kTileTokens = 16;
+
+struct DecodeParams {
+    const uint16_t *k_bank;      // bank base of the K pool: [num_pages][Hkv][ps][D]
+    const uint16_t *v_bank;
+    const uint16_t *q;           // [B][Hq][D]
+    const int32_t *page_table;   // [B][max_pages]
+    const int32_t *seq_lens;     // [B]
+    uint16_t *out;               // [B][Hq][D]
+    float *lse_out;              // [B][Hq] or null
+    float *lse_part;             // [B][Hq][max_splits], log2 units
+    float *o_part;               // [B][Hq][max_splits][D]
+    unsigned int *err;
+    int64_t num_pages;
+    int32_t num_kv_heads;
+    int32_t num_q_heads;
+    int32_t page_size;
+    int32_t max_pages;
+    int32_t batch;
+    int32_t tiles_per_split;
+    int32_t max_splits;
+    float qscale;                // softmax scale * log2(e)
+};
+
+// Split-K plan for one decode call.
+struct DecodePlan {
+    int32_t tiles_per_split;
+    int32_t max_splits;
+    size_t workspace_bytes;
+    size_t lse_part_bytes;       // offset of o_part inside the workspace
+};
+
+DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t max_seq_len, int32_t split_tokens, int num_sms);
+
+bool decode_supported(int head_dim, int group);
+cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, cudaStream_t stream);
+
+cudaError_t launch_append(uint16_t *k_bank, uint16_t *v_bank, const uint16_t *k_new,
+                          const uint16_t *v_new, const int64_t *out_loc, int32_t n_tokens,
+                          int32_t num_kv_heads, int32_t page_size, int32_t head_dim,
+                          int64_t num_pages, unsigned int *err, cudaStream_t stream);
+
+cudaError_t launch_gather(const uint16_t *k_bank, const uint16_t *v_bank,
+                          const int32_t *page_table, int32_t max_pages, const int32_t *seq_lens,
+                          int32_t batch, int32_t max_len, uint16_t *k_out, uint16_t *v_out,
+                          int32_t num_kv_heads, int32_t page_size, int32_t head_dim,
+                          int64_t num_pages, unsigned int *err, cudaStream_t stream);
+
+cudaError_t launch_noise(float *out, uint32_t *hash_out, const uint64_t *seeds,
+                         const int64_t *positions, int64_t n_rows, int32_t channels,
+                         float initializer_range, cudaStream_t stream);
+
+}  // namespace rlt

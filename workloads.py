@@ -98,8 +98,17 @@ class PagedCase:
 def bf16_normal(rng: np.random.Generator, shape) -> np.ndarray:
     """N(0,1) samples rounded to bf16, returned as their uint16 bit patterns."""
     f = rng.standard_normal(size=shape, dtype=np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16        # round to nearest even
+    return _round_bits(f)
+
+
+def _round_bits(f: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns, round to nearest even, in place on f's memory."""
+    u = f.view(np.uint32)
+    r = u >> 16
+    r &= 1
+    r += 0x7FFF
+    u += r                                           # finite inputs: no carry out of bit 31
+    u >>= 16
     return u.astype(np.uint16)
 
 
@@ -110,9 +119,7 @@ def bf16_bits_to_float(bits: np.ndarray) -> np.ndarray:
 
 def float_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 to bf16 (nearest even), as bit patterns (for building test cases)."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return u.astype(np.uint16)
+    return _round_bits(np.array(x, dtype=np.float32, copy=True, order="C"))
 
 
 @dataclasses.dataclass
@@ -282,3 +289,26 @@ def noise_keys(rows: int, channels: int, seed: int = 0, initializer_range: float
     seeds = rng.integers(0, 2**64, size=rows, dtype=np.uint64)
     pos = rng.integers(0, max_position, size=rows).astype(np.int64)
     return NoiseSpec(seeds, pos, channels, initializer_range)
+
+
+def subcase(case: PagedCase, rows) -> PagedCase:
+    """The requests ``rows`` of ``case`` alone, on a compact pool holding only their pages.
+
+    Pages shared between the chosen requests stay shared.  Used to time or check
+    the CPU oracle on a bounded sample of a large workload.
+    """
+    rows = np.asarray(rows, np.int64)
+    pt = case.page_table[rows]
+    sl = case.seq_lens[rows]
+    used = np.unique(np.concatenate([pt[i, : -(-int(sl[i]) // case.page_size)] for i in range(len(rows))]))
+    remap = {int(p): i for i, p in enumerate(used)}
+    pt2 = np.full_like(pt, -1)
+    for i in range(len(rows)):
+        n = -(-int(sl[i]) // case.page_size)
+        pt2[i, :n] = [remap[int(p)] for p in pt[i, :n]]
+    return PagedCase(name=f"{case.name}[{len(rows)} rows]", num_layers=case.num_layers,
+                     num_planes=case.num_planes, recurrent=case.recurrent, batch=len(rows),
+                     num_q_heads=case.num_q_heads, num_kv_heads=case.num_kv_heads,
+                     head_dim=case.head_dim, page_size=case.page_size, num_pages=int(used.size),
+                     seq_lens=sl.copy(), page_table=pt2,
+                     new_slots=_new_slots(sl, pt2, case.page_size), noise=None, seed=case.seed)
