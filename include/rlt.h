@@ -157,6 +157,36 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
                                  void *workspace, size_t workspace_bytes,
                                  int32_t split_tokens, void *stream);
 
+/* Size of the scratch array rlt_paged_decode_attn_noalloc uses (64 MiB). */
+#define RLT_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * rlt_paged_decode_attn without a workspace argument: the same computation,
+ * arguments and results as rlt_paged_decode_attn, but the split-K partials go
+ * to a fixed 64 MiB array inside the library, so the call allocates nothing.
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory at the point of the call, such as
+ * plugins whose host framework owns every device allocation, or decode loops
+ * that must not risk the device-wide synchronisation a cudaMalloc can cause.
+ *   - Each device that loads the library holds the array until the process
+ *     exits.  The first call on a device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; nothing in it needs to start at zero.  Calls that overlap on the
+ *     GPU (other streams, other host threads) race on it: serialise them.
+ *   - A shape whose partials need more than RLT_NOALLOC_SCRATCH_BYTES
+ *     (rlt_paged_decode_workspace_size) returns RLT_ERR_WORKSPACE_TOO_SMALL
+ *     and launches nothing; a larger split_tokens needs less.
+ */
+RLT_API rlt_status rlt_paged_decode_attn_noalloc(const rlt_kv_pool *pool, int32_t bank,
+                                                 const void *q, int32_t num_q_heads,
+                                                 const int32_t *page_table, int32_t max_pages,
+                                                 const int32_t *seq_lens, int32_t batch,
+                                                 int32_t max_seq_len, float scale, void *out,
+                                                 float *lse_out, int32_t split_tokens,
+                                                 void *stream);
+
 /*
  * Position-keyed latent-state noise ([PR152] Summary para 2).  For each row r
  * (a token) and channel c < channels:

@@ -25,7 +25,8 @@ import numpy as np
 
 __all__ = [
     "RltError", "KVPool", "library_path", "load", "rlt_bank_map", "rlt_kv_append",
-    "rlt_paged_decode_workspace_size", "rlt_paged_decode_attn", "rlt_latent_noise_init",
+    "rlt_paged_decode_workspace_size", "rlt_paged_decode_attn", "rlt_paged_decode_attn_noalloc",
+    "rlt_latent_noise_init",
     "rlt_noise_hash24", "rlt_paged_gather", "rlt_validate_batch", "rlt_get_device_error",
     "rlt_version", "DEVERR_BAD_PAGE", "DEVERR_BAD_SLOT", "DEVERR_TIMEOUT", "DEVERR_BAD_LEN",
 ]
@@ -79,6 +80,8 @@ def load():
         "rlt_latent_noise_init": (ctypes.c_int, [P, P, P, i64, i32, f32, P]),
         "rlt_noise_hash24": (ctypes.c_int, [P, P, P, i64, i32, P]),
         "rlt_paged_gather": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, i32, P, P, P]),
+        "rlt_paged_decode_attn_noalloc": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, P, i32, i32, f32, P, P,
+                                                         i32, P]),
         "rlt_validate_batch": (ctypes.c_int, [P, i32, P, i32, P, i64, i32]),
         "rlt_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     }
@@ -219,6 +222,35 @@ def rlt_paged_decode_attn(pool: KVPool, bank: int, q, page_table, seq_lens, max_
         _dev(out, torch.bfloat16, "out"), lse_ptr, ws_ptr, ws_bytes, int(split_tokens),
         _stream(stream)), "rlt_paged_decode_attn")
     return out
+
+
+def rlt_paged_decode_attn_noalloc(pool: KVPool, bank: int, q, page_table, seq_lens, max_seq_len: int,
+                                  out=None, lse_out=None, scale: float = 0.0, split_tokens: int = 0,
+                                  stream=None):
+    """rlt_paged_decode_attn with the split-K partials in the library's fixed scratch array.
+
+    For callers that cannot allocate device memory at the point of the call (a host
+    framework that owns all device allocations, or a decode loop that must not
+    risk a synchronising cudaMalloc).  Allocates nothing when ``out`` is given.
+    Calls on one device share the scratch array: calls that overlap on the GPU race.
+    """
+    import torch
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    lse_ptr = _dev(lse_out, torch.float32, "lse_out") if lse_out is not None else ctypes.c_void_p(0)
+    if page_table.dim() != 2 or page_table.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("page_table must be [B][max_pages] and seq_lens [B]")
+    _check(load().rlt_paged_decode_attn_noalloc(
+        ctypes.byref(pool.struct), bank, _dev(q, torch.bfloat16, "q"), Hq,
+        _dev(page_table, torch.int32, "page_table"), page_table.shape[1],
+        _dev(seq_lens, torch.int32, "seq_lens"), B, int(max_seq_len), float(scale),
+        _dev(out, torch.bfloat16, "out"), lse_ptr, int(split_tokens), _stream(stream)),
+        "rlt_paged_decode_attn_noalloc")
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 def rlt_latent_noise_init(seeds, positions, channels: int, initializer_range: float, out=None,
