@@ -175,6 +175,10 @@ def run_gpu(args, rank, world):
     lp = layer_planes(case)
     bmap, nbanks = rlt.rlt_bank_map(case.recurrent, case.num_planes)
     assert nbanks == len(lp)
+    if args.banks:
+        lp = lp[: args.banks]
+        nbanks = len(lp)
+        bmap = np.where(bmap < nbanks, bmap, -1)
     assert rlt.rlt_validate_batch(case.page_table, case.seq_lens, case.new_slots, case.num_pages,
                                   case.page_size) == 0
 
@@ -356,6 +360,7 @@ def config_dict(case, args):
             "batch": case.batch, "kv_tokens_per_layer_plane": case.kv_tokens(),
             "unique_kv_tokens_per_layer_plane": case.unique_tokens(),
             "split_tokens": args.split_tokens or "auto",
+            "banks_run": args.banks or "all",
             "l2": "inputs larger than L2: every bank's KV exceeds the 129 MB L2 and each is read once per step"}
 
 
@@ -369,6 +374,8 @@ def main():
     ap.add_argument("--workload", default="ouro", choices=W.WORKLOADS)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--split-tokens", type=int, default=0)
+    ap.add_argument("--banks", type=int, default=0,
+                    help="run only the first N layer-plane banks (small-footprint case for profilers); 0 = all")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU time for cpu_baseline")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
