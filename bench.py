@@ -364,6 +364,25 @@ def config_dict(case, args):
             "l2": "inputs larger than L2: every bank's KV exceeds the 129 MB L2 and each is read once per step"}
 
 
+# ------------------------------------------------------------ replicas
+
+def max_over_ranks(times_ms):
+    """Each timing's maximum over all ranks of the default process group (any backend)."""
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return [float(t) for t in times_ms]
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x) for x in times_ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_gbs(step_bytes_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job GB/s: every rank's bytes over the slowest rank's step time (weak scaling)."""
+    return world * step_bytes_per_rank / (ms_max * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------ main
 
 def main():
@@ -395,17 +414,9 @@ def main():
     case = r["case"]
     nlp = len(r["banks"])
     step_bytes = attn_bytes(case) * nlp + append_bytes(case) * nlp + noise_bytes(case)
-    ms_step = r["ms_total"] / args.steps
-    ms_max = ms_step
-    e2e_ms_step = r["e2e_ms"] / args.steps
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-        t = torch.tensor([ms_step, e2e_ms_step], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max, e2e_ms_step = float(t[0]), float(t[1])
-    value = world * step_bytes / (ms_max * 1e-3) / 1e9
-    e2e_value = world * step_bytes / (e2e_ms_step * 1e-3) / 1e9
+    ms_max, e2e_ms_step = max_over_ranks([r["ms_total"] / args.steps, r["e2e_ms"] / args.steps])
+    value = job_gbs(step_bytes, world, ms_max)
+    e2e_value = job_gbs(step_bytes, world, e2e_ms_step)
 
     attn_launch_ms = statistics.mean(r["attn_ms"])
     a_bytes = attn_bytes(case)

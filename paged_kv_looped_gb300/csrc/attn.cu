@@ -22,6 +22,8 @@
 //    Requests with one split write their output directly.
 #include <math_constants.h>
 
+#include <atomic>
+
 #include "rlt_device.cuh"
 #include "rlt_internal.h"
 
@@ -449,10 +451,19 @@ cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream)
     using C = Cfg<D, G>;
     static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
     auto kernel = decode_partial_kernel<D, G>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+    // The shared-memory opt-in is per function and device: set it once per device.
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit == 0 || (configured.load(std::memory_order_acquire) & bit) == 0) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess)
+            return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
     const dim3 grid(p.max_splits, p.num_kv_heads, p.batch);
     kernel<<<grid, kThreads, C::kSmemBytes, stream>>>(p);
     e = cudaGetLastError();
