@@ -157,6 +157,65 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
                                  void *workspace, size_t workspace_bytes,
                                  int32_t split_tokens, void *stream);
 
+/*
+ * Shared-prefix plan, HOST function ([FFM] "When scheduler does the work":
+ * a radix tree makes requests with a common prompt prefix point at the same
+ * physical pages).  From host copies of a decode batch's page tables it finds
+ * the 128-token tiles that several requests map to identical pages, walking a
+ * trie of tiles from position 0, and groups them into segments: runs of tiles
+ * shared by one fixed set of requests.  Along each request's path the
+ * segments' partial slots are numbered from 0.
+ *   chunk_tiles     tiles per CTA of the tensor-core prefix kernel (1..32)
+ *   segments        int32 [max_segments][6]: first tile, number of tiles,
+ *                   first partial slot, first member entry, member count,
+ *                   a member whose page-table row holds the segment's pages
+ *   members         int32 [max_member_entries]: request ids by segment
+ *   request_prefix  int32 [batch][2]: tokens of request b covered by its
+ *                   segments (a multiple of 128), partial slots they use
+ *   sizes           int32 [5]: segments, member entries, most chunks of one
+ *                   segment, most partial slots of one request, most members
+ *                   of one segment (filled even when the capacities are short)
+ * Returns RLT_ERR_OUT_OF_RANGE when max_segments or max_member_entries is too
+ * small (sizes[] says what is needed), RLT_ERR_UNSUPPORTED when page_size
+ * neither divides nor is a multiple of 128.
+ */
+RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t max_pages,
+                                   const int32_t *seq_lens, int32_t batch, int32_t page_size,
+                                   int32_t chunk_tiles, int32_t *segments, int32_t max_segments,
+                                   int32_t *members, int32_t max_member_entries,
+                                   int32_t *request_prefix, int32_t *sizes);
+
+/* Device workspace bytes of rlt_paged_decode_attn_prefix (sizes[3] of the plan
+ * as max_prefix_slots). */
+RLT_API size_t rlt_paged_decode_prefix_workspace_size(int32_t batch, int32_t num_q_heads,
+                                                      int32_t num_kv_heads, int32_t head_dim,
+                                                      int32_t max_seq_len, int32_t max_prefix_slots,
+                                                      int32_t split_tokens);
+
+/*
+ * Paged decode attention with shared prefixes read once ("cascade"): the same
+ * result as rlt_paged_decode_attn, up to fp32 rounding order.  The plan's
+ * arrays (segments, members, request_prefix: DEVICE copies of
+ * rlt_plan_prefix's output) name the tiles several requests share; each is
+ * read from HBM once per kv head and applied to every member's queries by a
+ * tcgen05 tensor-core kernel (S = Q K^T, O = P V with the members' query rows
+ * as M = 128), the rest of each request goes through the split-K kernel, and
+ * a log-sum-exp combine merges the partials.  num_segments, max_members,
+ * max_chunks, max_prefix_slots are sizes[0], [4], [2], [3] of the plan and
+ * chunk_tiles the value it was built with.  Other arguments as
+ * rlt_paged_decode_attn; the workspace (rlt_paged_decode_prefix_workspace_size
+ * bytes) is required.  num_segments == 0 runs rlt_paged_decode_attn.
+ * Supported: head_dim 128, num_q_heads/num_kv_heads in {1, 2, 4, 8}, page_size
+ * a multiple of 16 dividing or divisible by 128.
+ */
+RLT_API rlt_status rlt_paged_decode_attn_prefix(
+    const rlt_kv_pool *pool, int32_t bank, const void *q, int32_t num_q_heads,
+    const int32_t *page_table, int32_t max_pages, const int32_t *seq_lens, int32_t batch,
+    int32_t max_seq_len, const int32_t *segments, const int32_t *members,
+    const int32_t *request_prefix, int32_t num_segments, int32_t max_members, int32_t max_chunks,
+    int32_t max_prefix_slots, int32_t chunk_tiles, float scale, void *out, float *lse_out,
+    void *workspace, size_t workspace_bytes, int32_t split_tokens, void *stream);
+
 /* Size of the scratch array rlt_paged_decode_attn_noalloc uses (64 MiB). */
 #define RLT_NOALLOC_SCRATCH_BYTES (64u << 20)
 

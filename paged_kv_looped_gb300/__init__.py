@@ -28,7 +28,8 @@ __all__ = [
     "rlt_paged_decode_workspace_size", "rlt_paged_decode_attn", "rlt_paged_decode_attn_noalloc",
     "rlt_latent_noise_init",
     "rlt_noise_hash24", "rlt_paged_gather", "rlt_validate_batch", "rlt_get_device_error",
-    "rlt_version", "DEVERR_BAD_PAGE", "DEVERR_BAD_SLOT", "DEVERR_TIMEOUT", "DEVERR_BAD_LEN",
+    "rlt_version", "PrefixPlan", "rlt_plan_prefix", "rlt_paged_decode_attn_prefix",
+    "rlt_paged_decode_prefix_workspace_size", "DEVERR_BAD_PAGE", "DEVERR_BAD_SLOT", "DEVERR_TIMEOUT", "DEVERR_BAD_LEN",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -83,6 +84,10 @@ def load():
         "rlt_paged_decode_attn_noalloc": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, P, i32, i32, f32, P, P,
                                                          i32, P]),
         "rlt_validate_batch": (ctypes.c_int, [P, i32, P, i32, P, i64, i32]),
+        "rlt_plan_prefix": (ctypes.c_int, [P, i32, P, i32, i32, i32, P, i32, P, i32, P, P]),
+        "rlt_paged_decode_prefix_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, i32]),
+        "rlt_paged_decode_attn_prefix": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, P, i32, i32, P, P, P, i32,
+                                                        i32, i32, i32, i32, f32, P, P, P, sz, i32, P]),
         "rlt_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     }
     for name, (res, args) in sigs.items():
@@ -298,3 +303,89 @@ def rlt_paged_gather(pool: KVPool, bank: int, page_table, seq_lens, max_len: int
                                    _dev(v_out, torch.bfloat16, "v_out"), _stream(stream)),
            "rlt_paged_gather")
     return k_out, v_out
+
+
+# ------------------------------------------------------------ shared prefixes
+
+SEG_FIELDS = 6
+
+
+class PrefixPlan:
+    """Host result of rlt_plan_prefix plus (after ``.to(device)``) its device copies."""
+
+    def __init__(self, segments, members, request_prefix, sizes, chunk_tiles):
+        self.segments = segments            # int32 [n][6]
+        self.members = members              # int32 [entries]
+        self.request_prefix = request_prefix  # int32 [B][2]
+        self.num_segments, self.member_entries, self.max_chunks, self.max_prefix_slots, \
+            self.max_members = (int(x) for x in sizes)
+        self.chunk_tiles = chunk_tiles
+        self.dev = None
+
+    def to(self, device):
+        import torch
+        def t(a):
+            a = np.ascontiguousarray(a, np.int32).reshape(-1)
+            return torch.from_numpy(a if a.size else np.zeros(1, np.int32)).to(device)
+        self.dev = (t(self.segments), t(self.members), t(self.request_prefix))
+        return self
+
+
+def rlt_plan_prefix(page_table, seq_lens, page_size: int, chunk_tiles: int = 4) -> PrefixPlan:
+    """Find the 128-token tiles several requests share (host arrays in, host plan out)."""
+    pt, ptp = _host(page_table, np.int32)
+    sl, slp = _host(seq_lens, np.int32)
+    B = sl.size
+    req = np.zeros((B, 2), np.int32)
+    sizes = np.zeros(5, np.int32)
+    lib = load()
+    null = ctypes.c_void_p(0)
+    st = lib.rlt_plan_prefix(ptp, pt.shape[1], slp, B, page_size, chunk_tiles, null, 0, null, 0,
+                             req.ctypes.data_as(ctypes.c_void_p), sizes.ctypes.data_as(ctypes.c_void_p))
+    if st not in (0, 2):
+        raise RltError(st, "rlt_plan_prefix")
+    seg = np.zeros((max(int(sizes[0]), 1), SEG_FIELDS), np.int32)
+    mem = np.zeros(max(int(sizes[1]), 1), np.int32)
+    if st == 2:
+        _check(lib.rlt_plan_prefix(ptp, pt.shape[1], slp, B, page_size, chunk_tiles,
+                                   seg.ctypes.data_as(ctypes.c_void_p), seg.shape[0],
+                                   mem.ctypes.data_as(ctypes.c_void_p), mem.size,
+                                   req.ctypes.data_as(ctypes.c_void_p), sizes.ctypes.data_as(ctypes.c_void_p)),
+               "rlt_plan_prefix")
+    n = int(sizes[0])
+    return PrefixPlan(seg[:n], mem[: int(sizes[1])], req, sizes, chunk_tiles)
+
+
+def rlt_paged_decode_prefix_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                                           max_prefix_slots, split_tokens=0) -> int:
+    return int(load().rlt_paged_decode_prefix_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                             max_seq_len, max_prefix_slots, split_tokens))
+
+
+def rlt_paged_decode_attn_prefix(pool: KVPool, bank: int, q, page_table, seq_lens, max_seq_len: int,
+                                 plan: PrefixPlan, out=None, lse_out=None, workspace=None, scale: float = 0.0,
+                                 split_tokens: int = 0, stream=None):
+    """Paged decode attention reading shared-prefix tiles once (plan from rlt_plan_prefix, .to(device))."""
+    import torch
+    B, Hq, D = q.shape
+    if plan.dev is None:
+        plan.to(q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    need = rlt_paged_decode_prefix_workspace_size(B, Hq, pool.num_kv_heads, D, max_seq_len,
+                                                  plan.max_prefix_slots, split_tokens)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    lse_ptr = _dev(lse_out, torch.float32, "lse_out") if lse_out is not None else ctypes.c_void_p(0)
+    seg, mem, req = plan.dev
+    _check(load().rlt_paged_decode_attn_prefix(
+        ctypes.byref(pool.struct), bank, _dev(q, torch.bfloat16, "q"), Hq,
+        _dev(page_table, torch.int32, "page_table"), page_table.shape[1],
+        _dev(seq_lens, torch.int32, "seq_lens"), B, int(max_seq_len),
+        _dev(seg, torch.int32, "segments"), _dev(mem, torch.int32, "members"),
+        _dev(req, torch.int32, "request_prefix"), plan.num_segments, max(plan.max_members, 1),
+        plan.max_chunks, plan.max_prefix_slots, plan.chunk_tiles, float(scale),
+        _dev(out, torch.bfloat16, "out"), lse_ptr, ctypes.c_void_p(workspace.data_ptr()),
+        workspace.numel() * workspace.element_size(), int(split_tokens), _stream(stream)),
+        "rlt_paged_decode_attn_prefix")
+    return out

@@ -207,9 +207,115 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
     p.batch = batch;
     p.tiles_per_split = plan.tiles_per_split;
     p.max_splits = plan.max_splits;
+    p.part_stride = plan.max_splits;
     const double s = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)pool->head_dim);
     p.qscale = (float)(s * 1.4426950408889634);   // log2(e): softmax in base 2
     return from_cuda(rlt::launch_decode(p, pool->head_dim, group, static_cast<cudaStream_t>(stream)));
+}
+
+RLT_API size_t rlt_paged_decode_prefix_workspace_size(int32_t batch, int32_t num_q_heads,
+                                                      int32_t num_kv_heads, int32_t head_dim,
+                                                      int32_t max_seq_len, int32_t max_prefix_slots,
+                                                      int32_t split_tokens)
+{
+    if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || max_seq_len < 0 ||
+        max_prefix_slots < 0 || split_tokens < 0)
+        return 0;
+    const rlt::DecodePlan plan = rlt::plan_decode(batch, num_q_heads, num_kv_heads, head_dim,
+                                                  max_seq_len, split_tokens, current_sms());
+    const size_t rows = (size_t)batch * num_q_heads * (size_t)(max_prefix_slots + plan.max_splits);
+    return (rows * sizeof(float) + 255) / 256 * 256 + rows * head_dim * sizeof(float);
+}
+
+RLT_API rlt_status rlt_paged_decode_attn_prefix(
+    const rlt_kv_pool *pool, int32_t bank, const void *q, int32_t num_q_heads,
+    const int32_t *page_table, int32_t max_pages, const int32_t *seq_lens, int32_t batch,
+    int32_t max_seq_len, const int32_t *segments, const int32_t *members,
+    const int32_t *request_prefix, int32_t num_segments, int32_t max_members, int32_t max_chunks,
+    int32_t max_prefix_slots, int32_t chunk_tiles, float scale, void *out, float *lse_out,
+    void *workspace, size_t workspace_bytes, int32_t split_tokens, void *stream)
+{
+    if (num_segments == 0)      // nothing shared: the plain kernel computes the same thing
+        return rlt_paged_decode_attn(pool, bank, q, num_q_heads, page_table, max_pages, seq_lens,
+                                     batch, max_seq_len, scale, out, lse_out, workspace,
+                                     workspace_bytes, split_tokens, stream);
+    rlt_status st = check_pool(pool, bank);
+    if (st != RLT_OK)
+        return st;
+    if (batch < 0 || max_seq_len < 0 || max_pages < 1 || num_q_heads < 1 || split_tokens < 0 ||
+        split_tokens % rlt::kTileTokens != 0 || split_tokens > 128 * rlt::kTileTokens ||
+        num_segments < 0 || max_members < 1 || max_chunks < 0 || max_prefix_slots < 0 ||
+        chunk_tiles < 1 || num_q_heads % pool->num_kv_heads != 0)
+        return RLT_ERR_INVALID_ARG;
+    const int group = num_q_heads / pool->num_kv_heads;
+    if (!rlt::decode_supported(pool->head_dim, group) || pool->page_size % rlt::kTileTokens != 0 ||
+        !rlt::prefix_supported(pool->head_dim, group, pool->page_size) || batch > 65535 ||
+        pool->num_kv_heads > 65535)
+        return RLT_ERR_UNSUPPORTED;
+    if (q == nullptr || page_table == nullptr || seq_lens == nullptr || out == nullptr ||
+        segments == nullptr || members == nullptr || request_prefix == nullptr || workspace == nullptr)
+        return RLT_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || !std::isfinite(scale))
+        return RLT_ERR_INVALID_ARG;
+    const int64_t bank_rows = pool->num_pages * pool->num_kv_heads * (int64_t)pool->page_size;
+    if (bank_rows >= (int64_t(1) << 31))
+        return RLT_ERR_UNSUPPORTED;
+
+    unsigned int *err = nullptr;
+    int sms = 0;
+    if ((st = device_info(&err, &sms)) != RLT_OK)
+        return st;
+    const rlt::DecodePlan plan = rlt::plan_decode(batch, num_q_heads, pool->num_kv_heads,
+                                                  pool->head_dim, max_seq_len, split_tokens, sms);
+    const int32_t stride = max_prefix_slots + plan.max_splits;
+    const size_t rows = (size_t)batch * num_q_heads * stride;
+    const size_t lse_bytes = (rows * sizeof(float) + 255) / 256 * 256;
+    if (workspace_bytes < lse_bytes + rows * pool->head_dim * sizeof(float))
+        return RLT_ERR_WORKSPACE_TOO_SMALL;
+
+    rlt::DecodeParams p{};
+    const int64_t off = bank * bank_elems(pool);
+    p.k_bank = static_cast<const uint16_t *>(pool->k) + off;
+    p.v_bank = static_cast<const uint16_t *>(pool->v) + off;
+    p.q = static_cast<const uint16_t *>(q);
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.out = static_cast<uint16_t *>(out);
+    p.lse_out = lse_out;
+    p.lse_part = static_cast<float *>(workspace);
+    p.o_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + lse_bytes);
+    p.err = err;
+    p.num_pages = pool->num_pages;
+    p.num_kv_heads = pool->num_kv_heads;
+    p.num_q_heads = num_q_heads;
+    p.page_size = pool->page_size;
+    p.max_pages = max_pages;
+    p.batch = batch;
+    p.tiles_per_split = plan.tiles_per_split;
+    p.max_splits = plan.max_splits;
+    const double s = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)pool->head_dim);
+    p.qscale = (float)(s * 1.4426950408889634);
+    p.request_prefix = request_prefix;
+    p.prefix_slots = max_prefix_slots;
+    p.part_stride = stride;
+
+    rlt::PrefixParams pp{};
+    pp.segments = segments;
+    pp.members = members;
+    pp.num_segments = num_segments;
+    pp.chunk_tiles = chunk_tiles;
+    const int per_block = 128 / group;
+    pp.member_blocks = (max_members + per_block - 1) / per_block;
+    if ((int64_t)num_segments * pp.member_blocks > 65535)
+        return RLT_ERR_UNSUPPORTED;
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = rlt::launch_prefix(p, pp, max_chunks, p.k_bank, p.v_bank, bank_rows, cs);
+    if (e == cudaSuccess)
+        e = rlt::launch_decode(p, pool->head_dim, group, cs);
+    if (e == cudaSuccess)
+        e = rlt::launch_combine(p, pool->head_dim, cs);
+    return from_cuda(e);
 }
 
 RLT_API rlt_status rlt_latent_noise_init(float *out, const uint64_t *seeds,

@@ -125,10 +125,17 @@ __global__ void __launch_bounds__(kThreads) decode_partial_kernel(const DecodePa
     const int j = lane & 15;                   // which D/16 dims
 
     const int L = effective_len(p, b, split == 0 && g == 0 && threadIdx.x == 0);
-    const int n_tiles = (L + kTileTokens - 1) / kTileTokens;
+    // In shared-prefix mode the first tok0 tokens were covered by the prefix kernel,
+    // which wrote n_pre partials; this kernel covers [tok0, L).
+    int tok0 = 0, n_pre = 0;
+    if (p.request_prefix != nullptr) {
+        tok0 = min(max(p.request_prefix[2 * b], 0), L);
+        n_pre = p.request_prefix[2 * b + 1];
+    }
+    const int n_tiles = (L - tok0 + kTileTokens - 1) / kTileTokens;
     const int n_splits = (n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
 
-    if (n_splits == 0) {                        // empty request: out = 0, lse = -inf
+    if (n_splits == 0 && n_pre == 0) {          // empty request: out = 0, lse = -inf
         if (split == 0) {
             for (int i = threadIdx.x; i < G * D / 2; i += kThreads) {
                 const int h = i / (D / 2), d2 = i % (D / 2);
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) decode_partial_kernel(const DecodePa
 
     const int tile_begin = split * p.tiles_per_split;
     const int tile_end = min(tile_begin + p.tiles_per_split, n_tiles);
-    const int my_first = tile_begin + warp;
+    const int my_first = tile_begin + warp;      // tile index counted from tok0
     const int my_count = my_first < tile_end ? (tile_end - my_first + kWarps - 1) / kWarps : 0;
 
     unsigned char *pipe = smem + warp * kStages * C::kStageBytes;
@@ -162,7 +169,7 @@ __global__ void __launch_bounds__(kThreads) decode_partial_kernel(const DecodePa
     // Page and in-page offset of this warp's i-th tile live in lane i.
     int my_page = -1, my_off = 0;
     if (lane < my_count) {
-        const int tok = (my_first + lane * kWarps) * kTileTokens;
+        const int tok = tok0 + (my_first + lane * kWarps) * kTileTokens;
         const int page = p.page_table[(int64_t)b * p.max_pages + tok / p.page_size];
         if (page >= 0 && (int64_t)page < p.num_pages)
             my_page = page;
@@ -204,10 +211,10 @@ __global__ void __launch_bounds__(kThreads) decode_partial_kernel(const DecodePa
             acc[h][d] = 0.f;
     }
 
-    const int n_pre = my_count < kStages ? my_count : kStages;
-    for (int i = 0; i < n_pre; ++i)
+    const int n_prologue = my_count < kStages ? my_count : kStages;
+    for (int i = 0; i < n_prologue; ++i)
         issue(i);
-    int issued = n_pre;
+    int issued = n_prologue;
     uint32_t phase = 0;                        // bit s: parity of stage s's next phase
     int failed_at = -1;
 
@@ -222,7 +229,7 @@ __global__ void __launch_bounds__(kThreads) decode_partial_kernel(const DecodePa
             }
             phase ^= 1u << s;
 
-            const int valid = min(kTileTokens, L - (my_first + i * kWarps) * kTileTokens);
+            const int valid = min(kTileTokens, L - tok0 - (my_first + i * kWarps) * kTileTokens);
             const unsigned char *ks = pipe + s * C::kStageBytes;
             const unsigned char *vs = ks + C::kTileBytes;
 
@@ -370,7 +377,7 @@ __global__ void __launch_bounds__(kThreads) decode_partial_kernel(const DecodePa
         const float inv = ls > 0.f ? 1.f / ls : 0.f;
         const float lse2 = ls > 0.f ? M + log2f(ls) : -CUDART_INF_F;
         const int64_t bh = (int64_t)b * p.num_q_heads + g * G + h;
-        if (n_splits == 1) {
+        if (n_splits == 1 && n_pre == 0) {
             uint2 w;
             w.x = pack_bf16x2(o0 * inv, o1 * inv);
             w.y = pack_bf16x2(o2 * inv, o3 * inv);
@@ -378,15 +385,17 @@ __global__ void __launch_bounds__(kThreads) decode_partial_kernel(const DecodePa
             if (d0 == 0 && p.lse_out != nullptr)
                 p.lse_out[bh] = lse2 * kLn2;
         } else {
-            *reinterpret_cast<float4 *>(p.o_part + (bh * p.max_splits + split) * D + d0) =
+            const int64_t slot = bh * p.part_stride + p.prefix_slots + split;
+            *reinterpret_cast<float4 *>(p.o_part + slot * D + d0) =
                 make_float4(o0 * inv, o1 * inv, o2 * inv, o3 * inv);
             if (d0 == 0)
-                p.lse_part[bh * p.max_splits + split] = lse2;
+                p.lse_part[slot] = lse2;
         }
     }
 }
 
-// One warp per (request, query head): merge that request's split partials.
+// One warp per (request, query head): merge that request's partials -- its
+// shared-prefix slots [0, n_pre) and split-K slots [prefix_slots, prefix_slots + n).
 template <int D>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams p)
 {
@@ -397,15 +406,24 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
         return;
     const int b = (int)(bh / p.num_q_heads);
     const int L = effective_len(p, b, false);
-    const int n_tiles = (L + kTileTokens - 1) / kTileTokens;
+    int tok0 = 0, n_pre = 0;
+    if (p.request_prefix != nullptr) {
+        tok0 = min(max(p.request_prefix[2 * b], 0), L);
+        n_pre = p.request_prefix[2 * b + 1];
+    }
+    const int n_tiles = (L - tok0 + kTileTokens - 1) / kTileTokens;
     const int n = (n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
-    if (n <= 1)
+    if (n_pre == 0 && n <= 1)
         return;                                  // written by the partial kernel
+    const int total = n_pre + n;
 
-    const float *lp = p.lse_part + bh * p.max_splits;
+    // slot of the s-th partial of this (b, h)
+    auto slot_of = [&](int s) -> int64_t {
+        return bh * p.part_stride + (s < n_pre ? s : p.prefix_slots + (s - n_pre));
+    };
     float M = -CUDART_INF_F;
-    for (int s = lane; s < n; s += 32)
-        M = fmaxf(M, lp[s]);
+    for (int s = lane; s < total; s += 32)
+        M = fmaxf(M, p.lse_part[slot_of(s)]);
     M = warp_max_xor(M, 1);
 
     float acc[DPL];
@@ -414,18 +432,19 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
         acc[d] = 0.f;
     float ls = 0.f;
     if (M != -CUDART_INF_F) {
-        const float *op = p.o_part + bh * p.max_splits * D + lane * DPL;
-        for (int s = 0; s < n; ++s) {
-            const float w = exp2f(lp[s] - M);
+        for (int s = 0; s < total; ++s) {
+            const int64_t slot = slot_of(s);
+            const float w = exp2f(p.lse_part[slot] - M);
             ls += w;
+            const float *op = p.o_part + slot * D + lane * DPL;
             if constexpr (DPL == 4) {
-                const float4 o = *reinterpret_cast<const float4 *>(op + (int64_t)s * D);
+                const float4 o = *reinterpret_cast<const float4 *>(op);
                 acc[0] = fmaf(w, o.x, acc[0]);
                 acc[1] = fmaf(w, o.y, acc[1]);
                 acc[2] = fmaf(w, o.z, acc[2]);
                 acc[3] = fmaf(w, o.w, acc[3]);
             } else {
-                const float2 o = *reinterpret_cast<const float2 *>(op + (int64_t)s * D);
+                const float2 o = *reinterpret_cast<const float2 *>(op);
                 acc[0] = fmaf(w, o.x, acc[0]);
                 acc[1] = fmaf(w, o.y, acc[1]);
             }
@@ -443,6 +462,15 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
     }
     if (lane == 0 && p.lse_out != nullptr)
         p.lse_out[bh] = ls > 0.f ? (M + log2f(ls)) * kLn2 : -CUDART_INF_F;
+}
+
+template <int D>
+cudaError_t launch_combine_typed(const DecodeParams &p, cudaStream_t stream)
+{
+    const int64_t warps = (int64_t)p.batch * p.num_q_heads;
+    const unsigned blocks = (unsigned)((warps + 7) / 8);
+    decode_combine_kernel<D><<<blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
 }
 
 template <int D, int G>
@@ -467,12 +495,10 @@ cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream)
     const dim3 grid(p.max_splits, p.num_kv_heads, p.batch);
     kernel<<<grid, kThreads, C::kSmemBytes, stream>>>(p);
     e = cudaGetLastError();
-    if (e != cudaSuccess || p.max_splits <= 1)
+    // plain decode merges here; shared-prefix mode merges after the prefix kernel
+    if (e != cudaSuccess || p.max_splits <= 1 || p.request_prefix != nullptr)
         return e;
-    const int64_t warps = (int64_t)p.batch * p.num_q_heads;
-    const unsigned blocks = (unsigned)((warps + 7) / 8);
-    decode_combine_kernel<D><<<blocks, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_combine_typed<D>(p, stream);
 }
 
 }  // namespace
@@ -512,6 +538,15 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
         plan.workspace_bytes = plan.lse_part_bytes + rows * head_dim * sizeof(float);
     }
     return plan;
+}
+
+cudaError_t launch_combine(const DecodeParams &p, int head_dim, cudaStream_t stream)
+{
+    if (head_dim == 128)
+        return launch_combine_typed<128>(p, stream);
+    if (head_dim == 64)
+        return launch_combine_typed<64>(p, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, cudaStream_t stream)

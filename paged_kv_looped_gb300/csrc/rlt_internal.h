@@ -31,7 +31,32 @@ struct DecodeParams {
     int32_t tiles_per_split;
     int32_t max_splits;
     float qscale;                // softmax scale * log2(e)
+    // Shared-prefix (cascade) mode; all zero / null for plain decode.
+    const int32_t *request_prefix;  // [B][2]: tokens covered by shared segments, their partial slots
+    int32_t prefix_slots;        // partial slots reserved per (b, h) ahead of the split-K slots
+    int32_t part_stride;         // partial slots per (b, h): prefix_slots + max_splits
 };
+
+// Tokens per tensor-core tile of the shared-prefix kernel.
+constexpr int kPrefixTile = 128;
+
+// Fields of one segment of a prefix plan (rlt_plan_prefix).
+enum PrefixSegField { kSegFirstTile = 0, kSegNumTiles, kSegSlotBase, kSegMemberBegin,
+                      kSegMemberCount, kSegPageRow, kSegFields };
+
+struct PrefixParams {
+    const int32_t *segments;     // [num_segments][kSegFields]
+    const int32_t *members;      // request ids, grouped by segment
+    int32_t num_segments;
+    int32_t chunk_tiles;         // 128-token tiles per CTA
+    int32_t member_blocks;       // CTAs per segment along the members
+};
+
+bool prefix_supported(int head_dim, int group, int page_size);
+size_t prefix_smem_bytes(int chunk_tiles, int page_size);
+cudaError_t launch_prefix(const DecodeParams &p, const PrefixParams &pp, int max_chunks,
+                          const void *k_bank, const void *v_bank, int64_t bank_rows,
+                          cudaStream_t stream);
 
 // Split-K plan for one decode call.
 struct DecodePlan {
@@ -46,6 +71,7 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
 
 bool decode_supported(int head_dim, int group);
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, cudaStream_t stream);
+cudaError_t launch_combine(const DecodeParams &p, int head_dim, cudaStream_t stream);
 
 cudaError_t launch_append(uint16_t *k_bank, uint16_t *v_bank, const uint16_t *k_new,
                           const uint16_t *v_new, const int64_t *out_loc, int32_t n_tokens,

@@ -1,0 +1,121 @@
+"""Host planner of the shared-prefix (cascade) attention, checked by brute force.
+
+"Faster fuzzy minds" ("When scheduler does the work"): with a radix prefix
+cache, requests sharing a prompt prefix point at the same physical pages.
+rlt_plan_prefix must find, for every request, exactly the leading 128-token
+tiles it shares page-for-page with at least one other request, group them into
+segments of one member set, and number each request's partial slots 0..n-1.
+The brute-force reference compares every pair of requests tile by tile.
+"""
+import numpy as np
+import pytest
+
+import paged_kv_looped_gb300 as rlt
+import workloads as W
+
+TILE = 128
+
+
+def tile_key(pt, b, t, ps):
+    tok = t * TILE
+    if ps <= TILE:
+        return tuple(pt[b, (tok + j * ps) // ps] for j in range(TILE // ps))
+    return (pt[b, tok // ps], tok % ps)
+
+
+def common_tiles(pt, sl, ps, b, c):
+    n = min(int(sl[b]) // TILE, int(sl[c]) // TILE)
+    t = 0
+    while t < n and tile_key(pt, b, t, ps) == tile_key(pt, c, t, ps):
+        t += 1
+    return t
+
+
+def check_plan(case, chunk_tiles=4):
+    pt, sl, ps = case.page_table, case.seq_lens, case.page_size
+    plan = rlt.rlt_plan_prefix(pt, sl, ps, chunk_tiles)
+    B = case.batch
+    cp = np.zeros((B, B), int)
+    for b in range(B):
+        for c in range(B):
+            if b != c:
+                cp[b, c] = common_tiles(pt, sl, ps, b, c)
+    # each request's covered prefix = its longest shared run with any other request
+    for b in range(B):
+        assert plan.request_prefix[b, 0] == TILE * (cp[b].max() if B > 1 else 0), b
+    # segments: members share the segment's tiles page for page, and nobody else does
+    seg_of_tile = {}
+    for s in range(plan.num_segments):
+        first, n, base, mb, mc, row = plan.segments[s]
+        mem = plan.members[mb: mb + mc]
+        assert mc >= 2 and row in mem and list(mem) == sorted(mem)
+        for t in range(first, first + n):
+            want = {row} | {c for c in range(B) if c != row and cp[row, c] >= t + 1}
+            assert set(mem) == want, (s, t)
+            for b in mem:
+                assert tile_key(pt, b, t, ps) == tile_key(pt, row, t, ps)
+                seg_of_tile.setdefault(b, []).append((t, s))
+    # along each request's path: tiles 0..n-1 in order, partial slots contiguous from 0
+    for b in range(B):
+        tiles = sorted(seg_of_tile.get(b, []))
+        assert [t for t, _ in tiles] == list(range(plan.request_prefix[b, 0] // TILE))
+        slots = []
+        for s in dict.fromkeys(s for _, s in tiles):
+            first, n, base = plan.segments[s][:3]
+            slots += list(range(base, base + -(-n // chunk_tiles)))
+        assert slots == list(range(len(slots))) and len(slots) == plan.request_prefix[b, 1]
+    assert plan.max_prefix_slots == (plan.request_prefix[:, 1].max() if B else 0)
+    return plan
+
+
+@pytest.mark.parametrize("name", ["huginn", "longctx", "ouro", "tiny"])
+def test_plan_of_workloads(name):
+    plan = check_plan(W.config(name))
+    if name in ("huginn", "longctx"):
+        assert plan.num_segments > 0
+    else:
+        assert plan.num_segments == 0              # nothing shared
+
+
+@pytest.mark.parametrize("chunk_tiles", [1, 3, 32])
+def test_plan_chunking(chunk_tiles):
+    check_plan(W.config("huginn"), chunk_tiles)
+
+
+def test_plan_of_two_trees_and_loners():
+    # requests 0-3 share one 700-token prompt, 4-6 another, 7 and 8 share nothing
+    rng = np.random.default_rng(3)
+    ps = 16
+    lens = [900, 1300, 751, 2000, 1500, 1600, 1501, 999, 3000]
+    P = 2000
+    perm = iter(rng.permutation(P))
+    max_pages = -(-max(lens) // ps)
+    pt = np.full((len(lens), max_pages), -1, np.int32)
+    a = [next(perm) for _ in range(700 // ps)]
+    bprefix = [next(perm) for _ in range(1400 // ps)]
+    for r, L in enumerate(lens):
+        n = -(-L // ps)
+        shared = a if r < 4 else bprefix if r < 7 else []
+        k = min(len(shared), n - 1)
+        pt[r, :k] = shared[:k]
+        pt[r, k:n] = [next(perm) for _ in range(n - k)]
+    case = W.PagedCase(name="trees", num_layers=1, num_planes=1, recurrent=np.zeros(1, np.uint8), batch=len(lens),
+                       num_q_heads=8, num_kv_heads=8, head_dim=128, page_size=ps, num_pages=P,
+                       seq_lens=np.array(lens, np.int32), page_table=pt, new_slots=np.zeros(len(lens), np.int64))
+    plan = check_plan(case)
+    assert plan.request_prefix[7, 0] == 0 and plan.request_prefix[8, 0] == 0
+    assert plan.request_prefix[0, 0] == 640                 # 700 tokens -> 5 whole tiles
+    assert plan.request_prefix[4, 0] == 1280
+
+
+@pytest.mark.parametrize("ps", [32, 64, 128, 256])
+def test_plan_page_sizes(ps):
+    case = W.custom(B=5, Hq=8, Hkv=8, D=128, ps=ps, seq_lens=[3000, 2600, 4100, 1700, 2222], shared_frac=0.8,
+                    seed=ps)
+    check_plan(case)
+
+
+def test_plan_rejects_page_size_not_aligned_to_tiles():
+    case = W.custom(B=2, Hq=2, Hkv=2, D=128, ps=48, seq_lens=[300, 300], shared_frac=0.5)
+    with pytest.raises(rlt.RltError):
+        rlt.rlt_plan_prefix(case.page_table, case.seq_lens, 48)
