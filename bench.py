@@ -199,7 +199,21 @@ def run_gpu(args, rank, world):
     loc, pt, sl = loc_h.to(dev), pt_h.to(dev), sl_h.to(dev)
     out = torch.empty((nbanks, B, Hq, D), dtype=torch.bfloat16, device=dev)
     out_h = torch.empty_like(out, device="cpu").pin_memory()
-    ws_bytes = rlt.rlt_paged_decode_workspace_size(B, Hq, Hkv, D, case.max_seq_len, args.split_tokens)
+    # shared-prefix plan (the scheduler's radix tree, recovered from the page tables)
+    plan = None
+    if args.cascade != "off":
+        plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, args.chunk_tiles)
+        if plan.num_segments == 0 and args.cascade == "auto":
+            plan = None
+        else:
+            plan.to(dev)
+    if plan is not None:
+        ws_bytes = rlt.rlt_paged_decode_prefix_workspace_size(B, Hq, Hkv, D, case.max_seq_len,
+                                                              plan.max_prefix_slots, args.split_tokens)
+        plan_h = [torch.from_numpy(np.ascontiguousarray(a, np.int32).reshape(-1)).pin_memory()
+                  for a in (plan.segments, plan.members, plan.request_prefix)]
+    else:
+        ws_bytes = rlt.rlt_paged_decode_workspace_size(B, Hq, Hkv, D, case.max_seq_len, args.split_tokens)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     nz = case.noise
     if nz is not None:
@@ -222,8 +236,12 @@ def run_gpu(args, rank, world):
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-            rlt.rlt_paged_decode_attn(pool, bank, q[i], pt, sl, case.max_seq_len, out=out[i], workspace=ws,
-                                      split_tokens=args.split_tokens, stream=stream)
+            if plan is not None:
+                rlt.rlt_paged_decode_attn_prefix(pool, bank, q[i], pt, sl, case.max_seq_len, plan, out=out[i],
+                                                 workspace=ws, split_tokens=args.split_tokens, stream=stream)
+            else:
+                rlt.rlt_paged_decode_attn(pool, bank, q[i], pt, sl, case.max_seq_len, out=out[i], workspace=ws,
+                                          split_tokens=args.split_tokens, stream=stream)
             if time_attn:
                 e1.record(stream)
                 ev_attn.append((e0, e1))
@@ -260,6 +278,11 @@ def run_gpu(args, rank, world):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
+        if plan is not None:        # the host plans the step from its page tables, then ships the plan
+            p2 = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, args.chunk_tiles)
+            for host, arr, devt in zip(plan_h, (p2.segments, p2.members, p2.request_prefix), plan.dev):
+                host.numpy()[:] = np.ascontiguousarray(arr, np.int32).reshape(-1)
+                devt.copy_(host, non_blocking=True)
         q.copy_(q_h, non_blocking=True)
         kn.copy_(kn_h, non_blocking=True)
         vn.copy_(vn_h, non_blocking=True)
@@ -281,9 +304,14 @@ def run_gpu(args, rank, world):
     if nz is not None:
         h2d += seeds_h.numel() * 8 + pos_h.numel() * 8
         d2h += noise_h.numel() * 4
+    if plan is not None:
+        h2d += sum(t.numel() * 4 for t in plan_h)
+        per_lp = 4                   # append, prefix (tensor cores), split-K, combine
+    else:
+        per_lp = 3 if ws_bytes > 0 else 2
     combine = ws_bytes > 0
-    launches = args.steps * (len(banks) * (3 if combine else 2) + (1 if nz is not None else 0))
-    return dict(case=case, banks=banks, ms_total=ms_total, attn_ms=attn_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+    launches = args.steps * (len(banks) * per_lp + (1 if nz is not None else 0))
+    return dict(case=case, banks=banks, cascade=plan is not None, ms_total=ms_total, attn_ms=attn_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                 clocks=clocks.summary(), launches=launches, combine=combine, ws_bytes=ws_bytes)
 
 
@@ -360,6 +388,7 @@ def config_dict(case, args):
             "batch": case.batch, "kv_tokens_per_layer_plane": case.kv_tokens(),
             "unique_kv_tokens_per_layer_plane": case.unique_tokens(),
             "split_tokens": args.split_tokens or "auto",
+            "cascade": args.cascade, "chunk_tiles": args.chunk_tiles,
             "banks_run": args.banks or "all",
             "l2": "inputs larger than L2: every bank's KV exceeds the 129 MB L2 and each is read once per step"}
 
@@ -393,6 +422,9 @@ def main():
     ap.add_argument("--workload", default="ouro", choices=W.WORKLOADS)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--split-tokens", type=int, default=0)
+    ap.add_argument("--cascade", default="auto", choices=["auto", "on", "off"],
+                    help="read shared-prefix tiles once (tensor-core cascade) when the page tables share them")
+    ap.add_argument("--chunk-tiles", type=int, default=4, help="128-token tiles per CTA of the cascade kernel")
     ap.add_argument("--banks", type=int, default=0,
                     help="run only the first N layer-plane banks (small-footprint case for profilers); 0 = all")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU time for cpu_baseline")
@@ -440,7 +472,9 @@ def main():
         "pct_of_peak_hbm": round(100 * value / world / peak, 2),
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "kv_tokens_per_s": round(world * case.kv_tokens() * nlp / (ms_max * 1e-3), 1),
-        "roofline": {"bound": "hbm", "kernel": "rlt_paged_decode_attn (split-K partial + combine)",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("rlt_paged_decode_attn_prefix (tcgen05 shared-prefix + split-K + combine)"
+                                if r["cascade"] else "rlt_paged_decode_attn (split-K partial + combine)"),
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": f"{peak_kind} (HBM copy)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": a_bytes, "launch_us": round(attn_launch_ms * 1e3, 2)},

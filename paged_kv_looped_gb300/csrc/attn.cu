@@ -394,16 +394,20 @@ __global__ void __launch_bounds__(kThreads) decode_partial_kernel(const DecodePa
     }
 }
 
-// One warp per (request, query head): merge that request's partials -- its
-// shared-prefix slots [0, n_pre) and split-K slots [prefix_slots, prefix_slots + n).
+// Merge the partials of one (request, query head): its shared-prefix slots
+// [0, n_pre) and split-K slots [prefix_slots, prefix_slots + n).  Four warps per
+// pair take every fourth slot (lanes over the D dims, loads of two slots in
+// flight), then fold their (max, sum, vector) through shared memory.
+constexpr int kCombineWarps = 4;
+
 template <int D>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeParams p)
 {
     constexpr int DPL = D / 32;
-    const int64_t bh = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (bh >= (int64_t)p.batch * p.num_q_heads)
-        return;
+    __shared__ float red_m[kCombineWarps], red_l[kCombineWarps];
+    __shared__ __align__(16) float red_o[kCombineWarps][D];
+    const int64_t bh = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = (int)(bh / p.num_q_heads);
     const int L = effective_len(p, b, false);
     int tok0 = 0, n_pre = 0;
@@ -416,39 +420,72 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
     if (n_pre == 0 && n <= 1)
         return;                                  // written by the partial kernel
     const int total = n_pre + n;
-
-    // slot of the s-th partial of this (b, h)
     auto slot_of = [&](int s) -> int64_t {
         return bh * p.part_stride + (s < n_pre ? s : p.prefix_slots + (s - n_pre));
     };
+
     float M = -CUDART_INF_F;
-    for (int s = lane; s < total; s += 32)
+    for (int s = threadIdx.x; s < total; s += kCombineWarps * 32)
         M = fmaxf(M, p.lse_part[slot_of(s)]);
     M = warp_max_xor(M, 1);
+    if (lane == 0)
+        red_m[warp] = M;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w)
+        M = fmaxf(M, red_m[w]);
 
     float acc[DPL];
 #pragma unroll
     for (int d = 0; d < DPL; ++d)
         acc[d] = 0.f;
     float ls = 0.f;
-    if (M != -CUDART_INF_F) {
-        for (int s = 0; s < total; ++s) {
-            const int64_t slot = slot_of(s);
-            const float w = exp2f(p.lse_part[slot] - M);
-            ls += w;
-            const float *op = p.o_part + slot * D + lane * DPL;
-            if constexpr (DPL == 4) {
-                const float4 o = *reinterpret_cast<const float4 *>(op);
-                acc[0] = fmaf(w, o.x, acc[0]);
-                acc[1] = fmaf(w, o.y, acc[1]);
-                acc[2] = fmaf(w, o.z, acc[2]);
-                acc[3] = fmaf(w, o.w, acc[3]);
-            } else {
-                const float2 o = *reinterpret_cast<const float2 *>(op);
-                acc[0] = fmaf(w, o.x, acc[0]);
-                acc[1] = fmaf(w, o.y, acc[1]);
-            }
+    auto add = [&](int64_t slot, float lse) {
+        const float w = exp2f(lse - M);
+        ls += w;
+        const float *op = p.o_part + slot * D + lane * DPL;
+        if constexpr (DPL == 4) {
+            const float4 o = *reinterpret_cast<const float4 *>(op);
+            acc[0] = fmaf(w, o.x, acc[0]);
+            acc[1] = fmaf(w, o.y, acc[1]);
+            acc[2] = fmaf(w, o.z, acc[2]);
+            acc[3] = fmaf(w, o.w, acc[3]);
+        } else {
+            const float2 o = *reinterpret_cast<const float2 *>(op);
+            acc[0] = fmaf(w, o.x, acc[0]);
+            acc[1] = fmaf(w, o.y, acc[1]);
         }
+    };
+    if (M != -CUDART_INF_F) {
+        int s = warp;
+        for (; s + kCombineWarps < total; s += 2 * kCombineWarps) {
+            const int64_t s0 = slot_of(s), s1 = slot_of(s + kCombineWarps);
+            const float l0 = p.lse_part[s0], l1 = p.lse_part[s1];
+            add(s0, l0);
+            add(s1, l1);
+        }
+        if (s < total)
+            add(slot_of(s), p.lse_part[slot_of(s)]);
+    }
+    if (lane == 0)
+        red_l[warp] = ls;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d)
+        red_o[warp][lane * DPL + d] = acc[d];
+    __syncthreads();
+    if (warp != 0)
+        return;
+    ls = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w)
+        ls += red_l[w];
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) {
+        float a = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCombineWarps; ++w)
+            a += red_o[w][lane * DPL + d];
+        acc[d] = a;
     }
     const float inv = ls > 0.f ? 1.f / ls : 0.f;
     uint16_t *o = p.out + bh * D + lane * DPL;
@@ -467,9 +504,8 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
 template <int D>
 cudaError_t launch_combine_typed(const DecodeParams &p, cudaStream_t stream)
 {
-    const int64_t warps = (int64_t)p.batch * p.num_q_heads;
-    const unsigned blocks = (unsigned)((warps + 7) / 8);
-    decode_combine_kernel<D><<<blocks, 256, 0, stream>>>(p);
+    const int64_t pairs = (int64_t)p.batch * p.num_q_heads;
+    decode_combine_kernel<D><<<(unsigned)pairs, kCombineWarps * 32, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

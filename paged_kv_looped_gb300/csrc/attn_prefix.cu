@@ -30,19 +30,34 @@
 namespace rlt {
 namespace {
 
-constexpr int kPThreads = 128;              // 4 warps, one TMEM lane quadrant each
-constexpr int kPStages = 2;                 // K/V tile ring depth
-constexpr int kHalf = 128 * 128;            // one 64-element column block of a 128-row tile
-constexpr int kTileBytesP = 2 * kHalf;      // K (or V) tile: 128 tokens x 128 dims, bf16
-constexpr int kStageBytesP = 2 * kTileBytesP;
+// Roles: warps 0-3 own query rows 0..127 (softmax, rescale, output; warp w may
+// only touch TMEM lanes 32w..32w+31), warp 4 issues the MMAs, warp 5 issues the
+// TMA copies.  Work goes in 64-token sub-tiles (half a planner tile).
+constexpr int kSoftWarps = 4;
+constexpr int kPThreads = (kSoftWarps + 2) * 32;
+constexpr int kMmaWarp = kSoftWarps, kLoadWarp = kSoftWarps + 1;
+constexpr int kSub = 64;                    // tokens per sub-tile
+constexpr int kStagesP = 4;                 // K/V sub-tile ring depth
+constexpr int kHalfQ = 128 * 128;           // one 64-element column block of the 128 Q rows
+constexpr int kHalfKV = kSub * 128;         // one 64-dim column block of a sub-tile (64 rows x 128 B)
+constexpr int kKVBytes = 2 * kHalfKV;       // K (or V) of one sub-tile
+constexpr int kStageBytesP = 2 * kKVBytes;  // K + V
+constexpr int kPBytes = 128 * kSub * 2;     // P of one sub-tile: 128 rows x 64 tokens, bf16
 constexpr int kMaxChunkTiles = 32;
-constexpr int kMaxBoxes = 8;                // 128-token tile = up to 8 page boxes (page_size 16)
-constexpr int kQOff = 0, kPOff = kTileBytesP, kStageOff = 2 * kTileBytesP;
-constexpr int kRowsOff = kStageOff + kPStages * kStageBytesP;
-constexpr int kMemOff = kRowsOff + kMaxChunkTiles * kMaxBoxes * 4;
-constexpr int kBarOff = kMemOff + kPThreads * 4;
-constexpr int kSmemP = kBarOff + 64 + 1024;  // + alignment slack for the 1024-byte base
-constexpr uint32_t kTmemCols = 256;          // S in columns [0,128), O in [128,256)
+constexpr int kMaxBoxes = 2 * kMaxChunkTiles * 4;   // sub-tiles x boxes (page_size 16: 4 per sub-tile)
+constexpr int kQOff = 0;
+constexpr int kPOff = kQOff + 2 * kHalfQ;
+constexpr int kStageOff = kPOff + 2 * kPBytes;
+constexpr int kRowsOff = kStageOff + kStagesP * kStageBytesP;
+constexpr int kMemOff = kRowsOff + kMaxBoxes * 4;
+constexpr int kBarOff = kMemOff + 128 * 4;
+constexpr int kNumBars = 2 * kStagesP + 6;  // full[4], free[4], s_full[2], p_full[2], o_full[2]
+constexpr int kSmemP = kBarOff + kNumBars * 8 + 16 + 1024;
+constexpr uint32_t kTmemCols = 256;         // S[2] x 64 cols, O x 128 cols
+constexpr uint32_t kColS = 0, kColO = 128;
+// O accumulates in TMEM against a per-row reference max that moves only when
+// the row's running max exceeds it by more than this (log2 units): p <= 2^8.
+constexpr float kRescaleThreshold = 8.f;
 
 __global__ void __launch_bounds__(kPThreads, 1)
     decode_prefix_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -53,12 +68,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
     unsigned char *base =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     unsigned char *qs = base + kQOff;
-    unsigned char *ps = base + kPOff;
+    unsigned char *pbuf = base + kPOff;
     unsigned char *stages = base + kStageOff;
     int32_t *box_rows = reinterpret_cast<int32_t *>(base + kRowsOff);
     int32_t *mem = reinterpret_cast<int32_t *>(base + kMemOff);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(base + kBarOff);   // full[2], s_done, o_done
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 4);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + kBarOff);
+    uint64_t *full = bars, *stage_free = bars + kStagesP;
+    uint64_t *s_full = bars + 2 * kStagesP, *p_full = s_full + 2, *o_full = s_full + 4;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
 
     const int G = p.num_q_heads / p.num_kv_heads;
     const int chunk = blockIdx.x, g = blockIdx.y;
@@ -71,7 +89,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (t0 >= num_tiles)
         return;
     const int nt = min(pp.chunk_tiles, num_tiles - t0);
-    const int per_block = kPThreads / G;
+    const int per_block = 128 / G;
     const int m0 = mb * per_block;
     const int n_mem = min(per_block, sd[kSegMemberCount] - m0);
     if (n_mem <= 0)
@@ -79,15 +97,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int R = n_mem * G;                    // live query rows of this CTA
     const int page_row = sd[kSegPageRow];
     const int first_tile = sd[kSegFirstTile] + t0;
+    const int nsub = 2 * nt;                    // 64-token sub-tiles
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int BR = p.page_size < kPrefixTile ? p.page_size : kPrefixTile;   // rows per TMA box
-    const int boxes = kPrefixTile / BR;
+    const int BR = p.page_size < kSub ? p.page_size : kSub;    // rows per TMA box
+    const int boxes = kSub / BR;                                // boxes per sub-tile
 
     for (int i = tid; i < n_mem; i += kPThreads)
         mem[i] = pp.members[sd[kSegMemberBegin] + m0 + i];
-    for (int i = tid; i < nt * boxes; i += kPThreads) {
-        const int64_t tok = (int64_t)(first_tile + i / boxes) * kPrefixTile + (i % boxes) * BR;
+    for (int i = tid; i < nsub * boxes; i += kPThreads) {
+        const int64_t tok = (int64_t)first_tile * kPrefixTile + (int64_t)(i / boxes) * kSub + (i % boxes) * BR;
         const int64_t idx = tok / p.page_size;
         int64_t page = idx < p.max_pages ? p.page_table[(int64_t)page_row * p.max_pages + idx] : -1;
         if (page < 0 || page >= p.num_pages) {
@@ -97,8 +116,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
         box_rows[i] = (int32_t)((page * p.num_kv_heads + g) * p.page_size + tok % p.page_size);
     }
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i)
-            mbar_init(&bars[i], 1);
+        for (int i = 0; i < kStagesP; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&stage_free[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], (R + 31) / 32);   // one arrive per softmax warp with live rows
+            mbar_init(&o_full[i], 1);
+        }
+        *abort_flag = 0;
         mbar_init_fence();
     }
     if (warp == 0)
@@ -111,193 +138,202 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int b = mem[r / G], h = r % G;
         const uint4 v = *reinterpret_cast<const uint4 *>(
             p.q + ((int64_t)b * p.num_q_heads + g * G + h) * 128 + c16 * 8);
-        *reinterpret_cast<uint4 *>(qs + (c16 >> 3) * kHalf + tc::sw128_offset(r, (c16 & 7) * 8)) = v;
+        *reinterpret_cast<uint4 *>(qs + (c16 >> 3) * kHalfQ + tc::sw128_offset(r, (c16 & 7) * 8)) = v;
     }
     fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
+    bool ok = true;
 
-    // Warp 0 loads tile i into stage i % 2: lane j copies box j/4, column block (j/2)&1,
-    // of K (j even) or V (j odd); lane 0 arms the barrier first.
-    auto load_tile = [&](int i) {
-        uint64_t *full = &bars[i % kPStages];
-        unsigned char *st = stages + (i % kPStages) * kStageBytesP;
-        if (lane == 0)
-            mbar_arrive_expect_tx(full, kStageBytesP);
-        __syncwarp();
-        if (lane < 4 * boxes) {
-            const int box = lane >> 2, half = (lane >> 1) & 1, is_v = lane & 1;
-            tc::tma_load_2d(st + is_v * kTileBytesP + half * kHalf + box * BR * 128,
-                            is_v ? &vmap : &kmap, half * 64, box_rows[i * boxes + box], full);
-        }
-    };
-    int issued = 0;
-    if (warp == 0) {
+    if (warp == kLoadWarp) {
+        // ---------------------------------------------------------- TMA producer
+        // Lane j copies box j/4, column block (j/2)&1, of K (j even) or V (j odd).
         if (lane == 0) {
             tc::prefetch_tmap(&kmap);
             tc::prefetch_tmap(&vmap);
         }
-        for (; issued < kPStages && issued < nt; ++issued)
-            load_tile(issued);
-    }
-
-    const uint32_t id_s = tc::instr_desc_bf16(128, 128, false);
-    const uint32_t id_o = tc::instr_desc_bf16(128, 128, true);
-    const uint32_t qa = smem_u32(qs), pa = smem_u32(ps);
-    const int row = warp * 32 + lane;
-    const bool warp_live = warp * 32 < R;
-    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
-
-    float acc[128];
-#pragma unroll
-    for (int j = 0; j < 128; ++j)
-        acc[j] = 0.f;
-    float m_run = -CUDART_INF_F, l_run = 0.f;
-    uint32_t ph_full = 0, ph_s = 0, ph_o = 0;
-    bool ok = true, pending_s = false, pending_o = false;
-    int consumed = 0;
-
-    for (int i = 0; i < nt; ++i) {
-        const int s = i % kPStages;
-        const uint32_t ka = smem_u32(stages + s * kStageBytesP);
-        const uint32_t va = ka + kTileBytesP;
-        if (tid == 0) {
-            ok = mbar_wait(&bars[s], (ph_full >> s) & 1u);
-            if (ok) {
-                ph_full ^= 1u << s;
-                tc::fence_after_sync();
+        int j = 0;
+        for (; j < nsub && ok; ++j) {
+            const int st = j % kStagesP;
+            if (j >= kStagesP)
+                ok = mbar_wait_or_abort(&stage_free[st], ((j / kStagesP) - 1) & 1u, abort_flag);
+            if (!ok)
+                break;
+            unsigned char *kst = stages + st * kStageBytesP;
+            if (lane == 0)
+                mbar_arrive_expect_tx(&full[st], kStageBytesP);
+            __syncwarp();
+            if (lane < 4 * boxes) {
+                const int box = lane >> 2, half = (lane >> 1) & 1, is_v = lane & 1;
+                tc::tma_load_2d(kst + is_v * kKVBytes + half * kHalfKV + box * BR * 128,
+                                is_v ? &vmap : &kmap, half * 64, box_rows[j * boxes + box], &full[st]);
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            // copies of the last (up to 4) sub-tiles may still be landing: wait for them (bounded)
+            if (lane == 0)
+                for (int k = max(0, j - kStagesP); k < j; ++k)
+                    mbar_wait(&full[k % kStagesP], (k / kStagesP) & 1u);
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------- MMA issuer
+        const uint32_t id_s = tc::instr_desc_bf16(128, kSub, false);
+        const uint32_t id_o = tc::instr_desc_bf16(128, 128, true);
+        const uint32_t qa = smem_u32(qs), pa = smem_u32(pbuf), sa = smem_u32(stages);
+        auto issue_s = [&](int j) -> bool {   // S_j = Q K_j^T into S[j % 2]
+            const int st = j % kStagesP;
+            if (!mbar_wait_or_abort(&full[st], (j / kStagesP) & 1u, abort_flag))
+                return false;
+            tc::fence_after_sync();
+            if (lane == 0) {
+                const uint32_t ka = sa + st * kStageBytesP;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_bf16(tmem, tc::smem_desc(qa + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
-                                 tc::smem_desc(ka + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024), id_s,
+                    tc::mma_bf16(tmem + kColS + (j & 1) * kSub,
+                                 tc::smem_desc(qa + (kk >> 2) * kHalfQ + (kk & 3) * 32, 16, 1024),
+                                 tc::smem_desc(ka + (kk >> 2) * kHalfKV + (kk & 3) * 32, 16, 1024), id_s,
                                  kk > 0);
-                tc::mma_commit(&bars[2]);
+                tc::mma_commit(&s_full[j & 1]);
             }
+            __syncwarp();
+            return true;
+        };
+        ok = issue_s(0);
+        if (ok && nsub > 1)
+            ok = issue_s(1);
+        for (int j = 0; j < nsub && ok; ++j) {
+            // P_j written, S[j%2] read and O rescaled where needed by the softmax warps
+            ok = mbar_wait_or_abort(&p_full[j & 1], (j >> 1) & 1u, abort_flag);
+            if (!ok)
+                break;
+            tc::fence_after_sync();
+            if (lane == 0) {
+                const uint32_t va = sa + (j % kStagesP) * kStageBytesP + kKVBytes;
+                const uint32_t pj = pa + (j & 1) * kPBytes;
+#pragma unroll
+                for (int kk = 0; kk < kSub / 16; ++kk)
+                    tc::mma_bf16(tmem + kColO, tc::smem_desc(pj + kk * 32, 16, 1024),
+                                 tc::smem_desc(va + kk * 2048, kHalfKV, 1024), id_o, (j > 0) || (kk > 0));
+                tc::mma_commit(&o_full[j & 1]);
+                tc::mma_commit(&stage_free[j % kStagesP]);
+            }
+            __syncwarp();
+            if (j + 2 < nsub)
+                ok = issue_s(j + 2);
         }
-        ok = __syncthreads_and(ok) != 0;
-        if (!ok)
-            break;
-        ++consumed;
-        pending_s = true;
-        ok = mbar_wait(&bars[2], ph_s);
-        if (ok) {
-            ph_s ^= 1u;
-            pending_s = false;
+        if (!ok) {
+            *abort_flag = 1;
+            // let issued MMAs finish before the CTA gives up its shared memory (bounded)
+            if (lane == 0)
+                mbar_wait(&stage_free[0], 0);    // returns at once or after the time limit
         }
-        if (!__syncthreads_and(ok)) {
-            ok = false;
-            break;
-        }
-        tc::fence_after_sync();
+    } else if (warp * 32 < R) {
+        // ------------------------------------------- softmax warps with live rows
+        const int row = warp * 32 + lane;
+        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        float m_ref = -CUDART_INF_F, l_run = 0.f;
 
-        // Softmax of this thread's query row over the tile's 128 tokens (log2 domain).
-        float m_new = m_run, alpha = 1.f;
-        if (warp_live) {
+        for (int j = 0; j < nsub && ok; ++j) {
+            ok = mbar_wait_or_abort(&s_full[j & 1], (j >> 1) & 1u, abort_flag);
+            if (!ok)
+                break;
+            tc::fence_after_sync();
+            float v[64];
+            tc::tmem_ld64(t_lane + kColS + (j & 1) * kSub, v);
             float mx = -CUDART_INF_F;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float v[32];
-                tc::tmem_ld32(t_row + c * 32, v);
+            for (int i = 0; i < 64; ++i)
+                mx = fmaxf(mx, v[i]);
+            mx *= p.qscale;
+            const bool up = mx > m_ref + kRescaleThreshold;
+            const float m_next = up ? mx : m_ref;   // rows >= R hold garbage and are never stored
+            const float scale_o = exp2f(m_ref - m_next);   // 1 if the reference stays, 0 at first
+            if (__any_sync(kFullMask, up) && j > 0) {
+                // rescale this row's O (PV of sub-tile j-1 must have landed)
+                ok = mbar_wait_or_abort(&o_full[(j - 1) & 1], ((j - 1) >> 1) & 1u, abort_flag);
+                if (!__all_sync(kFullMask, ok)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    mx = fmaxf(mx, v[j]);
+                for (int c = 0; c < 4; ++c) {
+                    float o[32];
+                    tc::tmem_ld32(t_lane + kColO + c * 32, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o[i] *= scale_o;
+                    tc::tmem_st32(t_lane + kColO + c * 32, o);
+                }
             }
-            m_new = fmaxf(m_run, mx * p.qscale);
-            alpha = exp2f(m_run - m_new);
+            l_run *= scale_o;
+            m_ref = m_next;
             float lsum = 0.f;
+            uint32_t w[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float v[32];
-                tc::tmem_ld32(t_row + c * 32, v);
-                uint32_t w[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float p0 = exp2f(fmaf(v[2 * j], p.qscale, -m_new));
-                    const float p1 = exp2f(fmaf(v[2 * j + 1], p.qscale, -m_new));
-                    lsum += p0 + p1;
-                    w[j] = pack_bf16x2(p0, p1);
-                }
-                if (row < R) {
-#pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8)
-                        *reinterpret_cast<uint4 *>(ps + (c >> 1) * kHalf +
-                                                   tc::sw128_offset(row, (c & 1) * 32 + q8 * 8)) =
-                            make_uint4(w[4 * q8], w[4 * q8 + 1], w[4 * q8 + 2], w[4 * q8 + 3]);
+            for (int i = 0; i < 32; ++i) {
+                const float p0 = fast_exp2(fmaf(v[2 * i], p.qscale, -m_ref));
+                const float p1 = fast_exp2(fmaf(v[2 * i + 1], p.qscale, -m_ref));
+                lsum += p0 + p1;
+                w[i] = cvt_bf16x2(p0, p1);
+            }
+            l_run += lsum;
+            if (j >= 2) {   // P[j%2] was read by the PV of sub-tile j-2
+                ok = mbar_wait_or_abort(&o_full[j & 1], ((j - 2) >> 1) & 1u, abort_flag);
+                if (!__all_sync(kFullMask, ok)) {
+                    ok = false;
+                    break;
                 }
             }
-            l_run = l_run * alpha + lsum;
-        }
-        fence_proxy_async();                    // P (generic writes) -> MMA (async proxy)
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            tc::fence_after_sync();
+            if (row < R) {
+                unsigned char *pj = pbuf + (j & 1) * kPBytes;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16(tmem + 128, tc::smem_desc(pa + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
-                             tc::smem_desc(va + kk * 2048, kHalf, 1024), id_o, kk > 0);
-            tc::mma_commit(&bars[3]);
+                for (int c8 = 0; c8 < 8; ++c8)
+                    *reinterpret_cast<uint4 *>(pj + tc::sw128_offset(row, c8 * 8)) =
+                        make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
+            }
+            fence_proxy_async();                // P (generic writes) -> MMA (async proxy)
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&p_full[j & 1]);
         }
-        pending_o = true;
-        ok = mbar_wait(&bars[3], ph_o);
         if (ok) {
-            ph_o ^= 1u;
-            pending_o = false;
+            ok = mbar_wait_or_abort(&o_full[(nsub - 1) & 1], ((nsub - 1) >> 1) & 1u, abort_flag);
+            ok = __all_sync(kFullMask, ok);
         }
-        if (!__syncthreads_and(ok)) {
-            ok = false;
-            break;
-        }
-        tc::fence_after_sync();
-        if (warp_live) {
+        if (!ok)
+            *abort_flag = 1;
+        if (__all_sync(kFullMask, ok && *abort_flag == 0)) {   // warp-uniform: TMEM loads below
+            tc::fence_after_sync();
+            const int b = row < R ? mem[row / G] : 0, h = row % G;
+            const int64_t slot = ((int64_t)b * p.num_q_heads + g * G + h) * p.part_stride +
+                                 sd[kSegSlotBase] + chunk;
+            const float inv = 1.f / l_run;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                float v[32];
-                tc::tmem_ld32(t_row + 128 + c * 32, v);
+                float o[32];
+                tc::tmem_ld32(t_lane + kColO + c * 32, o);
+                if (row < R) {
+                    float4 *dst = reinterpret_cast<float4 *>(p.o_part + slot * 128 + c * 32);
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    acc[c * 32 + j] = fmaf(acc[c * 32 + j], alpha, v[j]);
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                             o[4 * i + 3] * inv);
+                }
             }
-        }
-        m_run = m_new;
-        // both MMAs reading stage s are complete: refill it
-        if (warp == 0 && issued < nt) {
-            load_tile(issued);
-            ++issued;
+            if (row < R)
+                p.lse_part[slot] = m_ref + log2f(l_run);
         }
     }
 
-    if (!ok) {
-        // A wait ran out: flag it, let this CTA's copies still in flight land
-        // (bounded), and skip the partial.
-        if (tid == 0) {
-            record_error(p.err, RLT_DEVERR_TIMEOUT);
-            for (int k = consumed; k < issued; ++k) {
-                const int s = k % kPStages;
-                mbar_wait(&bars[s], (ph_full >> s) & 1u);
-                ph_full ^= 1u << s;
-            }
-            if (pending_s)
-                mbar_wait(&bars[2], ph_s);      // MMAs still reading shared memory
-            if (pending_o)
-                mbar_wait(&bars[3], ph_o);
-        }
-    } else if (warp_live && row < R) {
-        const int b = mem[row / G], h = row % G;
-        const int64_t slot = ((int64_t)b * p.num_q_heads + g * G + h) * p.part_stride +
-                             pp.segments[seg * kSegFields + kSegSlotBase] + chunk;
-        const float inv = 1.f / l_run;
-        float4 *dst = reinterpret_cast<float4 *>(p.o_part + slot * 128);
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            dst[j] = make_float4(acc[4 * j] * inv, acc[4 * j + 1] * inv, acc[4 * j + 2] * inv,
-                                 acc[4 * j + 3] * inv);
-        p.lse_part[slot] = m_run + log2f(l_run);
-    }
     tc::fence_before_sync();
     __syncthreads();
+    if (tid == 0 && *abort_flag != 0)
+        record_error(p.err, RLT_DEVERR_TIMEOUT);
     if (warp == 0)
         tc::tmem_dealloc(tmem, kTmemCols);
 }
@@ -357,7 +393,7 @@ cudaError_t launch_prefix(const DecodeParams &p, const PrefixParams &pp, int max
         return cudaSuccess;
     if (pp.chunk_tiles < 1 || pp.chunk_tiles > kMaxChunkTiles || bank_rows >= (int64_t(1) << 31))
         return cudaErrorInvalidValue;
-    const int box_rows = p.page_size < kPrefixTile ? p.page_size : kPrefixTile;
+    const int box_rows = p.page_size < kSub ? p.page_size : kSub;
     CUtensorMap kmap, vmap;
     if (!make_map(&kmap, k_bank, bank_rows, box_rows) || !make_map(&vmap, v_bank, bank_rows, box_rows))
         return cudaErrorInvalidValue;

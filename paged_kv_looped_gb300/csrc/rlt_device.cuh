@@ -42,6 +42,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return bf16_bits(lo) | (bf16_bits(hi) << 16);
 }
 
+// Same rounding (nearest even) in one instruction: hi -> upper half, lo -> lower half.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 2^x on the special-function unit (flushes denormal results to zero).
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // ------------------------------------------------------------ shared memory
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -102,6 +118,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
             return false;
     }
     return false;
+}
+
+// As mbar_wait, but also gives up as soon as *abort turns non-zero (another
+// role of the CTA gave up first).
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity,
+                                                   const volatile int *abort)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1; it != 0; ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 63u) == 0u && (*abort != 0 || global_ns() - t0 > kWaitLimitNs))
+            return false;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Order this thread's earlier generic-proxy shared-memory accesses before
