@@ -162,6 +162,17 @@ def profiled_traffic(kernel_src: str):
 
 # ------------------------------------------------------------ GPU arm
 
+def auto_chunk_tiles(rlt, case, tails, num_sms):
+    """Tiles per CTA of the tensor-core kernel: the largest power of two (4..16) that
+    still leaves two CTAs per SM over all (segment, kv head) work."""
+    p1 = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, 1, tails)
+    units = int(sum(int(s[1]) for s in p1.segments)) * case.num_kv_heads
+    chunk = 16
+    while chunk > 4 and units / chunk < 2 * num_sms:
+        chunk //= 2
+    return chunk
+
+
 def run_gpu(args, rank, world):
     import torch
 
@@ -201,14 +212,19 @@ def run_gpu(args, rank, world):
     out_h = torch.empty_like(out, device="cpu").pin_memory()
     # shared-prefix plan (the scheduler's radix tree, recovered from the page tables)
     plan = None
+    G = case.num_q_heads // case.num_kv_heads
+    tails = args.tails == "on" or (args.tails == "auto" and G >= 8)
     if args.cascade != "off":
-        plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, args.chunk_tiles)
-        if plan.num_segments == 0 and args.cascade == "auto":
+        if args.chunk_tiles == 0:
+            args.chunk_tiles = auto_chunk_tiles(rlt, case, tails, torch.cuda.get_device_properties(dev).multi_processor_count)
+        plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, args.chunk_tiles, tails)
+        if plan.num_segments == 0 or (args.cascade == "auto" and not tails and
+                                      plan.max_rest_len == case.max_seq_len):
             plan = None
         else:
             plan.to(dev)
     if plan is not None:
-        ws_bytes = rlt.rlt_paged_decode_prefix_workspace_size(B, Hq, Hkv, D, case.max_seq_len,
+        ws_bytes = rlt.rlt_paged_decode_prefix_workspace_size(B, Hq, Hkv, D, plan.max_rest_len,
                                                               plan.max_prefix_slots, args.split_tokens)
         plan_h = [torch.from_numpy(np.ascontiguousarray(a, np.int32).reshape(-1)).pin_memory()
                   for a in (plan.segments, plan.members, plan.request_prefix)]
@@ -279,7 +295,7 @@ def run_gpu(args, rank, world):
     e0.record(stream)
     for _ in range(args.steps):
         if plan is not None:        # the host plans the step from its page tables, then ships the plan
-            p2 = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, args.chunk_tiles)
+            p2 = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, args.chunk_tiles, tails)
             for host, arr, devt in zip(plan_h, (p2.segments, p2.members, p2.request_prefix), plan.dev):
                 host.numpy()[:] = np.ascontiguousarray(arr, np.int32).reshape(-1)
                 devt.copy_(host, non_blocking=True)
@@ -306,7 +322,7 @@ def run_gpu(args, rank, world):
         d2h += noise_h.numel() * 4
     if plan is not None:
         h2d += sum(t.numel() * 4 for t in plan_h)
-        per_lp = 4                   # append, prefix (tensor cores), split-K, combine
+        per_lp = 4 if plan.max_rest_len > 0 else 3    # append, tensor-core segments, [split-K], combine
     else:
         per_lp = 3 if ws_bytes > 0 else 2
     combine = ws_bytes > 0
@@ -388,7 +404,7 @@ def config_dict(case, args):
             "batch": case.batch, "kv_tokens_per_layer_plane": case.kv_tokens(),
             "unique_kv_tokens_per_layer_plane": case.unique_tokens(),
             "split_tokens": args.split_tokens or "auto",
-            "cascade": args.cascade, "chunk_tiles": args.chunk_tiles,
+            "cascade": args.cascade, "chunk_tiles": args.chunk_tiles, "tails": args.tails,
             "banks_run": args.banks or "all",
             "l2": "inputs larger than L2: every bank's KV exceeds the 129 MB L2 and each is read once per step"}
 
@@ -424,7 +440,11 @@ def main():
     ap.add_argument("--split-tokens", type=int, default=0)
     ap.add_argument("--cascade", default="auto", choices=["auto", "on", "off"],
                     help="read shared-prefix tiles once (tensor-core cascade) when the page tables share them")
-    ap.add_argument("--chunk-tiles", type=int, default=4, help="128-token tiles per CTA of the cascade kernel")
+    ap.add_argument("--chunk-tiles", type=int, default=0,
+                    help="128-token tiles per CTA of the tensor-core kernel (0 = from the plan's size)")
+    ap.add_argument("--tails", default="auto", choices=["auto", "on", "off"],
+                    help="also send each request's unshared tokens through the tensor-core kernel "
+                         "(auto: when a kv head serves >= 8 query heads)")
     ap.add_argument("--banks", type=int, default=0,
                     help="run only the first N layer-plane banks (small-footprint case for profilers); 0 = all")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU time for cpu_baseline")

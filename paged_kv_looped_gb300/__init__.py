@@ -84,10 +84,10 @@ def load():
         "rlt_paged_decode_attn_noalloc": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, P, i32, i32, f32, P, P,
                                                          i32, P]),
         "rlt_validate_batch": (ctypes.c_int, [P, i32, P, i32, P, i64, i32]),
-        "rlt_plan_prefix": (ctypes.c_int, [P, i32, P, i32, i32, i32, P, i32, P, i32, P, P]),
+        "rlt_plan_prefix": (ctypes.c_int, [P, i32, P, i32, i32, i32, i32, P, i32, P, i32, P, P]),
         "rlt_paged_decode_prefix_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, i32]),
         "rlt_paged_decode_attn_prefix": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, P, i32, i32, P, P, P, i32,
-                                                        i32, i32, i32, i32, f32, P, P, P, sz, i32, P]),
+                                                        i32, i32, i32, i32, i32, f32, P, P, P, sz, i32, P]),
         "rlt_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     }
     for name, (res, args) in sigs.items():
@@ -307,7 +307,7 @@ def rlt_paged_gather(pool: KVPool, bank: int, page_table, seq_lens, max_len: int
 
 # ------------------------------------------------------------ shared prefixes
 
-SEG_FIELDS = 6
+SEG_FIELDS = 7
 
 
 class PrefixPlan:
@@ -318,7 +318,7 @@ class PrefixPlan:
         self.members = members              # int32 [entries]
         self.request_prefix = request_prefix  # int32 [B][2]
         self.num_segments, self.member_entries, self.max_chunks, self.max_prefix_slots, \
-            self.max_members = (int(x) for x in sizes)
+            self.max_members, self.max_rest_len = (int(x) for x in sizes)
         self.chunk_tiles = chunk_tiles
         self.dev = None
 
@@ -331,23 +331,26 @@ class PrefixPlan:
         return self
 
 
-def rlt_plan_prefix(page_table, seq_lens, page_size: int, chunk_tiles: int = 4) -> PrefixPlan:
-    """Find the 128-token tiles several requests share (host arrays in, host plan out)."""
+def rlt_plan_prefix(page_table, seq_lens, page_size: int, chunk_tiles: int = 4,
+                    private_tails: bool = False) -> PrefixPlan:
+    """Find the 128-token tiles several requests share (host arrays in, host plan out).
+    With ``private_tails`` every request's remaining tokens get a one-member segment too."""
     pt, ptp = _host(page_table, np.int32)
     sl, slp = _host(seq_lens, np.int32)
     B = sl.size
     req = np.zeros((B, 2), np.int32)
-    sizes = np.zeros(5, np.int32)
+    sizes = np.zeros(6, np.int32)
     lib = load()
     null = ctypes.c_void_p(0)
-    st = lib.rlt_plan_prefix(ptp, pt.shape[1], slp, B, page_size, chunk_tiles, null, 0, null, 0,
+    tails = 1 if private_tails else 0
+    st = lib.rlt_plan_prefix(ptp, pt.shape[1], slp, B, page_size, chunk_tiles, tails, null, 0, null, 0,
                              req.ctypes.data_as(ctypes.c_void_p), sizes.ctypes.data_as(ctypes.c_void_p))
     if st not in (0, 2):
         raise RltError(st, "rlt_plan_prefix")
     seg = np.zeros((max(int(sizes[0]), 1), SEG_FIELDS), np.int32)
     mem = np.zeros(max(int(sizes[1]), 1), np.int32)
     if st == 2:
-        _check(lib.rlt_plan_prefix(ptp, pt.shape[1], slp, B, page_size, chunk_tiles,
+        _check(lib.rlt_plan_prefix(ptp, pt.shape[1], slp, B, page_size, chunk_tiles, tails,
                                    seg.ctypes.data_as(ctypes.c_void_p), seg.shape[0],
                                    mem.ctypes.data_as(ctypes.c_void_p), mem.size,
                                    req.ctypes.data_as(ctypes.c_void_p), sizes.ctypes.data_as(ctypes.c_void_p)),
@@ -356,10 +359,10 @@ def rlt_plan_prefix(page_table, seq_lens, page_size: int, chunk_tiles: int = 4) 
     return PrefixPlan(seg[:n], mem[: int(sizes[1])], req, sizes, chunk_tiles)
 
 
-def rlt_paged_decode_prefix_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+def rlt_paged_decode_prefix_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_rest_len,
                                            max_prefix_slots, split_tokens=0) -> int:
     return int(load().rlt_paged_decode_prefix_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
-                                                             max_seq_len, max_prefix_slots, split_tokens))
+                                                             max_rest_len, max_prefix_slots, split_tokens))
 
 
 def rlt_paged_decode_attn_prefix(pool: KVPool, bank: int, q, page_table, seq_lens, max_seq_len: int,
@@ -372,7 +375,8 @@ def rlt_paged_decode_attn_prefix(pool: KVPool, bank: int, q, page_table, seq_len
         plan.to(q.device)
     if out is None:
         out = torch.empty_like(q)
-    need = rlt_paged_decode_prefix_workspace_size(B, Hq, pool.num_kv_heads, D, max_seq_len,
+    rest = plan.max_rest_len if plan.num_segments else int(max_seq_len)
+    need = rlt_paged_decode_prefix_workspace_size(B, Hq, pool.num_kv_heads, D, rest,
                                                   plan.max_prefix_slots, split_tokens)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -384,7 +388,7 @@ def rlt_paged_decode_attn_prefix(pool: KVPool, bank: int, q, page_table, seq_len
         _dev(seq_lens, torch.int32, "seq_lens"), B, int(max_seq_len),
         _dev(seg, torch.int32, "segments"), _dev(mem, torch.int32, "members"),
         _dev(req, torch.int32, "request_prefix"), plan.num_segments, max(plan.max_members, 1),
-        plan.max_chunks, plan.max_prefix_slots, plan.chunk_tiles, float(scale),
+        plan.max_chunks, plan.max_prefix_slots, plan.chunk_tiles, rest, float(scale),
         _dev(out, torch.bfloat16, "out"), lse_ptr, ctypes.c_void_p(workspace.data_ptr()),
         workspace.numel() * workspace.element_size(), int(split_tokens), _stream(stream)),
         "rlt_paged_decode_attn_prefix")

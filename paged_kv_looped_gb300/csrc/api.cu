@@ -215,14 +215,14 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
 
 RLT_API size_t rlt_paged_decode_prefix_workspace_size(int32_t batch, int32_t num_q_heads,
                                                       int32_t num_kv_heads, int32_t head_dim,
-                                                      int32_t max_seq_len, int32_t max_prefix_slots,
+                                                      int32_t max_rest_len, int32_t max_prefix_slots,
                                                       int32_t split_tokens)
 {
-    if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || max_seq_len < 0 ||
+    if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || max_rest_len < 0 ||
         max_prefix_slots < 0 || split_tokens < 0)
         return 0;
     const rlt::DecodePlan plan = rlt::plan_decode(batch, num_q_heads, num_kv_heads, head_dim,
-                                                  max_seq_len, split_tokens, current_sms());
+                                                  max_rest_len, split_tokens, current_sms());
     const size_t rows = (size_t)batch * num_q_heads * (size_t)(max_prefix_slots + plan.max_splits);
     return (rows * sizeof(float) + 255) / 256 * 256 + rows * head_dim * sizeof(float);
 }
@@ -232,8 +232,8 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     const int32_t *page_table, int32_t max_pages, const int32_t *seq_lens, int32_t batch,
     int32_t max_seq_len, const int32_t *segments, const int32_t *members,
     const int32_t *request_prefix, int32_t num_segments, int32_t max_members, int32_t max_chunks,
-    int32_t max_prefix_slots, int32_t chunk_tiles, float scale, void *out, float *lse_out,
-    void *workspace, size_t workspace_bytes, int32_t split_tokens, void *stream)
+    int32_t max_prefix_slots, int32_t chunk_tiles, int32_t max_rest_len, float scale, void *out,
+    float *lse_out, void *workspace, size_t workspace_bytes, int32_t split_tokens, void *stream)
 {
     if (num_segments == 0)      // nothing shared: the plain kernel computes the same thing
         return rlt_paged_decode_attn(pool, bank, q, num_q_heads, page_table, max_pages, seq_lens,
@@ -245,7 +245,8 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     if (batch < 0 || max_seq_len < 0 || max_pages < 1 || num_q_heads < 1 || split_tokens < 0 ||
         split_tokens % rlt::kTileTokens != 0 || split_tokens > 128 * rlt::kTileTokens ||
         num_segments < 0 || max_members < 1 || max_chunks < 0 || max_prefix_slots < 0 ||
-        chunk_tiles < 1 || num_q_heads % pool->num_kv_heads != 0)
+        chunk_tiles < 1 || max_rest_len < 0 || max_rest_len > max_seq_len ||
+        num_q_heads % pool->num_kv_heads != 0)
         return RLT_ERR_INVALID_ARG;
     const int group = num_q_heads / pool->num_kv_heads;
     if (!rlt::decode_supported(pool->head_dim, group) || pool->page_size % rlt::kTileTokens != 0 ||
@@ -265,8 +266,9 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     int sms = 0;
     if ((st = device_info(&err, &sms)) != RLT_OK)
         return st;
+    // the split-K grid covers only what the segments leave: at most max_rest_len tokens
     const rlt::DecodePlan plan = rlt::plan_decode(batch, num_q_heads, pool->num_kv_heads,
-                                                  pool->head_dim, max_seq_len, split_tokens, sms);
+                                                  pool->head_dim, max_rest_len, split_tokens, sms);
     const int32_t stride = max_prefix_slots + plan.max_splits;
     const size_t rows = (size_t)batch * num_q_heads * stride;
     const size_t lse_bytes = (rows * sizeof(float) + 255) / 256 * 256;
@@ -311,7 +313,7 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = rlt::launch_prefix(p, pp, max_chunks, p.k_bank, p.v_bank, bank_rows, cs);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && max_rest_len > 0)
         e = rlt::launch_decode(p, pool->head_dim, group, cs);
     if (e == cudaSuccess)
         e = rlt::launch_combine(p, pool->head_dim, cs);

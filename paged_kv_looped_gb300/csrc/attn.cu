@@ -49,20 +49,35 @@ struct Cfg {
     static constexpr int kSmemBytes = kBarOffset + kWarps * kStages * 8;
 };
 
-// Length of request b as the kernels use it: seq_lens[b] clamped to what the
-// page table row and the split grid can hold (a clamp is recorded as an error).
-__device__ __forceinline__ int effective_len(const DecodeParams &p, int b, bool report)
+// Tokens [tok0, L) of request b that the split-K kernels cover, and n_pre, the
+// partials the shared-prefix kernel wrote for it.  seq_lens[b] is clamped to
+// the page-table row and the split grid (a clamp is recorded as an error).
+struct Span {
+    int tok0, L, n_pre;
+};
+
+__device__ __forceinline__ Span request_span(const DecodeParams &p, int b, bool report)
 {
-    int L = p.seq_lens[b];
+    int len = p.seq_lens[b];
+    bool bad = false;
     const int64_t cap_pages = (int64_t)p.max_pages * p.page_size;
-    const int64_t cap_grid = (int64_t)p.max_splits * p.tiles_per_split * kTileTokens;
-    const int cap = (int)(cap_pages < cap_grid ? cap_pages : cap_grid);
-    if (L < 0 || L > cap) {
-        if (report)
-            record_error(p.err, RLT_DEVERR_BAD_LEN);
-        L = L < 0 ? 0 : cap;
+    if (len < 0 || len > cap_pages) {
+        len = len < 0 ? 0 : (int)cap_pages;
+        bad = true;
     }
-    return L;
+    Span sp{0, len, 0};
+    if (p.request_prefix != nullptr) {
+        sp.tok0 = min(max(p.request_prefix[2 * b], 0), len);
+        sp.n_pre = p.request_prefix[2 * b + 1];
+    }
+    const int64_t cap_grid = (int64_t)p.max_splits * p.tiles_per_split * kTileTokens;
+    if (sp.L - sp.tok0 > cap_grid) {
+        sp.L = (int)(sp.tok0 + cap_grid);
+        bad = true;
+    }
+    if (bad && report)
+        record_error(p.err, RLT_DEVERR_BAD_LEN);
+    return sp;
 }
 
 template <int DPL>
@@ -124,14 +139,10 @@ __global__ void __launch_bounds__(kThreads) decode_partial_kernel(const DecodePa
     const int half = lane >> 4;                // which 8 rows of a tile
     const int j = lane & 15;                   // which D/16 dims
 
-    const int L = effective_len(p, b, split == 0 && g == 0 && threadIdx.x == 0);
     // In shared-prefix mode the first tok0 tokens were covered by the prefix kernel,
     // which wrote n_pre partials; this kernel covers [tok0, L).
-    int tok0 = 0, n_pre = 0;
-    if (p.request_prefix != nullptr) {
-        tok0 = min(max(p.request_prefix[2 * b], 0), L);
-        n_pre = p.request_prefix[2 * b + 1];
-    }
+    const Span sp = request_span(p, b, split == 0 && g == 0 && threadIdx.x == 0);
+    const int L = sp.L, tok0 = sp.tok0, n_pre = sp.n_pre;
     const int n_tiles = (L - tok0 + kTileTokens - 1) / kTileTokens;
     const int n_splits = (n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
 
@@ -409,17 +420,22 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     const int64_t bh = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = (int)(bh / p.num_q_heads);
-    const int L = effective_len(p, b, false);
-    int tok0 = 0, n_pre = 0;
-    if (p.request_prefix != nullptr) {
-        tok0 = min(max(p.request_prefix[2 * b], 0), L);
-        n_pre = p.request_prefix[2 * b + 1];
-    }
-    const int n_tiles = (L - tok0 + kTileTokens - 1) / kTileTokens;
+    const Span sp = request_span(p, b, false);
+    const int n_pre = sp.n_pre;
+    const int n_tiles = (sp.L - sp.tok0 + kTileTokens - 1) / kTileTokens;
     const int n = (n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
-    if (n_pre == 0 && n <= 1)
+    if (n_pre == 0 && n == 1)
         return;                                  // written by the partial kernel
     const int total = n_pre + n;
+    if (total == 0) {                            // empty request: out = 0, lse = -inf
+        if (warp == 0) {
+            for (int d = lane; d < D / 2; d += 32)
+                reinterpret_cast<uint32_t *>(p.out + bh * D)[d] = 0u;
+            if (lane == 0 && p.lse_out != nullptr)
+                p.lse_out[bh] = -CUDART_INF_F;
+        }
+        return;
+    }
     auto slot_of = [&](int s) -> int64_t {
         return bh * p.part_stride + (s < n_pre ? s : p.prefix_slots + (s - n_pre));
     };

@@ -97,7 +97,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int R = n_mem * G;                    // live query rows of this CTA
     const int page_row = sd[kSegPageRow];
     const int first_tile = sd[kSegFirstTile] + t0;
-    const int nsub = 2 * nt;                    // 64-token sub-tiles
+    // tokens [tok_begin, tok_end) of this CTA; a private tail segment ends mid-tile
+    const int64_t tok_begin = (int64_t)first_tile * kPrefixTile;
+    const int64_t tok_end = min((int64_t)(first_tile + nt) * kPrefixTile, (int64_t)sd[kSegEndToken]);
+    if (tok_end <= tok_begin)
+        return;
+    const int nsub = (int)((tok_end - tok_begin + kSub - 1) / kSub);   // 64-token sub-tiles
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int BR = p.page_size < kSub ? p.page_size : kSub;    // rows per TMA box
@@ -106,7 +111,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
     for (int i = tid; i < n_mem; i += kPThreads)
         mem[i] = pp.members[sd[kSegMemberBegin] + m0 + i];
     for (int i = tid; i < nsub * boxes; i += kPThreads) {
-        const int64_t tok = (int64_t)first_tile * kPrefixTile + (int64_t)(i / boxes) * kSub + (i % boxes) * BR;
+        const int64_t tok = tok_begin + (int64_t)(i / boxes) * kSub + (i % boxes) * BR;
+        if (tok >= tok_end) {
+            box_rows[i] = -1;                    // past the request's last token: not loaded
+            continue;
+        }
         const int64_t idx = tok / p.page_size;
         int64_t page = idx < p.max_pages ? p.page_table[(int64_t)page_row * p.max_pages + idx] : -1;
         if (page < 0 || page >= p.num_pages) {
@@ -162,10 +171,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (!ok)
                 break;
             unsigned char *kst = stages + st * kStageBytesP;
+            const int64_t sub_begin = tok_begin + (int64_t)j * kSub;
+            const int nbox = (int)min((int64_t)boxes, (tok_end - sub_begin + BR - 1) / BR);
             if (lane == 0)
-                mbar_arrive_expect_tx(&full[st], kStageBytesP);
+                mbar_arrive_expect_tx(&full[st], (uint32_t)(nbox * BR * 128 * 4));
             __syncwarp();
-            if (lane < 4 * boxes) {
+            if (lane < 4 * nbox) {
                 const int box = lane >> 2, half = (lane >> 1) & 1, is_v = lane & 1;
                 tc::tma_load_2d(kst + is_v * kKVBytes + half * kHalfKV + box * BR * 128,
                                 is_v ? &vmap : &kmap, half * 64, box_rows[j * boxes + box], &full[st]);
@@ -243,6 +254,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tc::fence_after_sync();
             float v[64];
             tc::tmem_ld64(t_lane + kColS + (j & 1) * kSub, v);
+            const int valid = (int)min((int64_t)kSub, tok_end - (tok_begin + (int64_t)j * kSub));
+            if (valid < kSub) {
+                // ragged end of a private tail: mask the missing tokens, and zero their V
+                // rows, whose memory may hold anything (0 * NaN would poison O)
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    v[i] = i < valid ? v[i] : -CUDART_INF_F;
+                if (warp == 0) {
+                    unsigned char *vst = stages + (j % kStagesP) * kStageBytesP + kKVBytes;
+                    for (int c = lane; c < (kSub - valid) * 16; c += 32) {
+                        const int r = valid + c / 16, c16 = c % 16;
+                        *reinterpret_cast<uint4 *>(vst + (c16 >> 3) * kHalfKV + r * 128 + (c16 & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+            }
             float mx = -CUDART_INF_F;
 #pragma unroll
             for (int i = 0; i < 64; ++i)
@@ -421,9 +448,10 @@ cudaError_t launch_prefix(const DecodeParams &p, const PrefixParams &pp, int max
 extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t max_pages,
                                               const int32_t *seq_lens, int32_t batch,
                                               int32_t page_size, int32_t chunk_tiles,
-                                              int32_t *segments, int32_t max_segments,
-                                              int32_t *members, int32_t max_member_entries,
-                                              int32_t *request_prefix, int32_t *sizes)
+                                              int32_t private_tails, int32_t *segments,
+                                              int32_t max_segments, int32_t *members,
+                                              int32_t max_member_entries, int32_t *request_prefix,
+                                              int32_t *sizes)
 {
     using rlt::kPrefixTile;
     if (batch < 0 || max_pages < 0 || page_size < 1 || chunk_tiles < 1 ||
@@ -450,7 +478,7 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
         return (int)(L / kPrefixTile);
     };
 
-    struct Seg { int first, tiles, parent; std::vector<int> mem; };
+    struct Seg { int first, tiles, parent; std::vector<int> mem; int64_t end_token; };
     std::vector<Seg> segs;
     std::vector<int> deepest(batch, -1);       // segment holding each request's last shared tile
     struct Group { std::vector<int> mem; int seg; };
@@ -480,7 +508,7 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
                     segs[s].tiles++;
                 } else {
                     s = (int)segs.size();
-                    segs.push_back({t, 1, grp.seg, kv.second});
+                    segs.push_back({t, 1, grp.seg, kv.second, 0});
                 }
                 for (int b : kv.second)
                     deepest[b] = s;
@@ -490,6 +518,25 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
         level.swap(next);
     }
 
+    for (Seg &sg : segs)
+        sg.end_token = (int64_t)(sg.first + sg.tiles) * kPrefixTile;
+    std::vector<int64_t> covered(batch, 0);
+    for (int b = 0; b < batch; ++b)
+        if (deepest[b] >= 0)
+            covered[b] = segs[deepest[b]].end_token;
+    if (private_tails) {
+        // every request's own remaining tokens become a one-member segment
+        for (int b = 0; b < batch; ++b) {
+            const int64_t L = std::min<int64_t>(std::max(seq_lens[b], 0), (int64_t)max_pages * page_size);
+            if (L <= covered[b])
+                continue;
+            const int first = (int)(covered[b] / kPrefixTile);
+            const int tiles = (int)((L + kPrefixTile - 1) / kPrefixTile) - first;
+            segs.push_back({first, tiles, deepest[b], {b}, L});
+            deepest[b] = (int)segs.size() - 1;
+            covered[b] = L;
+        }
+    }
     const int nseg = (int)segs.size();
     std::vector<int> chunks(nseg), slot_base(nseg);
     int64_t member_entries = 0;
@@ -507,13 +554,17 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
     sizes[3] = 0;
     sizes[4] = max_members;
     int max_slots = 0;
+    int64_t max_rest = 0;
     for (int b = 0; b < batch; ++b) {
         const int s = deepest[b];
-        request_prefix[2 * b] = s < 0 ? 0 : (segs[s].first + segs[s].tiles) * kPrefixTile;
+        request_prefix[2 * b] = (int32_t)covered[b];
         request_prefix[2 * b + 1] = s < 0 ? 0 : slot_base[s] + chunks[s];
         max_slots = std::max(max_slots, request_prefix[2 * b + 1]);
+        const int64_t L = std::min<int64_t>(std::max(seq_lens[b], 0), (int64_t)max_pages * page_size);
+        max_rest = std::max(max_rest, L - covered[b]);
     }
     sizes[3] = max_slots;
+    sizes[5] = (int32_t)max_rest;
     if (nseg > max_segments || member_entries > max_member_entries)
         return RLT_ERR_OUT_OF_RANGE;               // sizes[] tells the caller what is needed
     int64_t m = 0;
@@ -525,6 +576,7 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
         row[rlt::kSegMemberBegin] = (int32_t)m;
         row[rlt::kSegMemberCount] = (int32_t)segs[s].mem.size();
         row[rlt::kSegPageRow] = segs[s].mem[0];
+        row[rlt::kSegEndToken] = (int32_t)segs[s].end_token;
         for (int b : segs[s].mem)
             members[m++] = b;
     }

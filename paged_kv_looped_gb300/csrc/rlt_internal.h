@@ -42,7 +42,7 @@ constexpr int kPrefixTile = 128;
 
 // Fields of one segment of a prefix plan (rlt_plan_prefix).
 enum PrefixSegField { kSegFirstTile = 0, kSegNumTiles, kSegSlotBase, kSegMemberBegin,
-                      kSegMemberCount, kSegPageRow, kSegFields };
+                      kSegMemberCount, kSegPageRow, kSegEndToken, kSegFields };
 
 struct PrefixParams {
     const int32_t *segments;     // [num_segments][kSegFields]

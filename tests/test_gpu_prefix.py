@@ -18,12 +18,13 @@ from helpers import attn_close, bf16_dev, bits_host, i32_dev
 pytestmark = pytest.mark.gpu
 
 
-def run_both(case, h, device, chunk_tiles=4, split_tokens=0):
+def run_both(case, h, device, chunk_tiles=4, split_tokens=0, private_tails=False):
     pool = rlt.KVPool(bf16_dev(h.k_pool, device)[None].contiguous(), bf16_dev(h.v_pool, device)[None].contiguous())
     q = bf16_dev(h.q, device)
     pt = i32_dev(case.page_table, device)
     sl = i32_dev(case.seq_lens, device)
-    plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, chunk_tiles).to(device)
+    plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, chunk_tiles,
+                               private_tails).to(device)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=device)
     out = rlt.rlt_paged_decode_attn_prefix(pool, 0, q, pt, sl, case.max_seq_len, plan, lse_out=lse,
                                            split_tokens=split_tokens)
@@ -129,3 +130,36 @@ def test_longctx_full_size_sampled(cuda_device):
     ref, ref_lse = oracle.decode_attn_rows(q_bits, bits_host(kd[0]), bits_host(vd[0]), case.page_table,
                                            case.seq_lens, rows)
     check(got[rows], ref, lse[rows], ref_lse)
+
+
+@pytest.mark.parametrize("G,ps,shared_frac", [(8, 64, 0.9), (8, 16, 0.0), (4, 16, 0.5), (2, 32, 0.8), (1, 128, 0.7)])
+def test_private_tails_on_tensor_cores(cuda_device, G, ps, shared_frac):
+    # every token through the tcgen05 kernel, ragged ends of all kinds (1, 63, 64, 65, 127, 129 ... tokens)
+    lens = [1, 63, 64, 65, 127, 128, 129, 1000, 3001, 4096, 2222, 777]
+    case = W.custom(B=len(lens), Hq=G * 2, Hkv=2, D=128, ps=ps, seq_lens=lens, shared_frac=shared_frac,
+                    seed=G + ps)
+    h = W.host_tensors(case)
+    plan, got, lse, _, _ = run_both(case, h, cuda_device, chunk_tiles=2, private_tails=True)
+    assert plan.max_rest_len == 0 and plan.num_segments >= len(lens)
+    ref, ref_lse = oracle.decode_attn(h.q, h.k_pool, h.v_pool, case.page_table, case.seq_lens)
+    check(got, ref, lse, ref_lse)
+
+
+def test_private_tails_with_empty_and_nan_padding(cuda_device):
+    # page memory past each request's end holds NaN: the masked tail must not leak it
+    lens = [0, 5, 70, 200, 0, 1300]
+    case = W.custom(B=len(lens), Hq=16, Hkv=2, D=128, ps=64, seq_lens=lens, seed=3)
+    h = W.host_tensors(case)
+    kp, vp = h.k_pool.copy(), h.v_pool.copy()
+    for b, L in enumerate(lens):
+        n = -(-L // 64)
+        if n:
+            last = case.page_table[b, n - 1]
+            kp[last, :, L - (n - 1) * 64:, :] = 0x7FC0          # bf16 quiet NaN
+            vp[last, :, L - (n - 1) * 64:, :] = 0x7FC0
+    h = W.HostTensors(kp, vp, h.q, h.k_new, h.v_new)
+    plan, got, lse, _, _ = run_both(case, h, cuda_device, private_tails=True)
+    ref, ref_lse = oracle.decode_attn(h.q, kp, vp, case.page_table, case.seq_lens)
+    assert np.all(got[0] == 0) and np.all(got[4] == 0)
+    assert np.all(np.isfinite(got))
+    check(got[[1, 2, 3, 5]], ref[[1, 2, 3, 5]], lse[[1, 2, 3, 5]], ref_lse[[1, 2, 3, 5]])

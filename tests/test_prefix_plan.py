@@ -34,6 +34,7 @@ def common_tiles(pt, sl, ps, b, c):
 def check_plan(case, chunk_tiles=4):
     pt, sl, ps = case.page_table, case.seq_lens, case.page_size
     plan = rlt.rlt_plan_prefix(pt, sl, ps, chunk_tiles)
+    assert plan.max_rest_len == max(int(sl[b]) - int(plan.request_prefix[b, 0]) for b in range(case.batch))
     B = case.batch
     cp = np.zeros((B, B), int)
     for b in range(B):
@@ -46,7 +47,8 @@ def check_plan(case, chunk_tiles=4):
     # segments: members share the segment's tiles page for page, and nobody else does
     seg_of_tile = {}
     for s in range(plan.num_segments):
-        first, n, base, mb, mc, row = plan.segments[s]
+        first, n, base, mb, mc, row, end = plan.segments[s]
+        assert end == (first + n) * TILE
         mem = plan.members[mb: mb + mc]
         assert mc >= 2 and row in mem and list(mem) == sorted(mem)
         for t in range(first, first + n):
@@ -119,3 +121,25 @@ def test_plan_rejects_page_size_not_aligned_to_tiles():
     case = W.custom(B=2, Hq=2, Hkv=2, D=128, ps=48, seq_lens=[300, 300], shared_frac=0.5)
     with pytest.raises(rlt.RltError):
         rlt.rlt_plan_prefix(case.page_table, case.seq_lens, 48)
+
+
+@pytest.mark.parametrize("name", ["huginn", "longctx", "gqa", "tiny"])
+def test_private_tails_cover_every_token(name):
+    case = W.config(name)
+    pt, sl, ps = case.page_table, case.seq_lens, case.page_size
+    shared = rlt.rlt_plan_prefix(pt, sl, ps, 4)
+    plan = rlt.rlt_plan_prefix(pt, sl, ps, 4, private_tails=True)
+    assert plan.max_rest_len == 0
+    assert np.array_equal(plan.request_prefix[:, 0], sl)
+    # the shared segments are unchanged; one tail per request follows them
+    n = shared.num_segments
+    assert np.array_equal(plan.segments[:n], shared.segments)
+    tails = plan.segments[n:]
+    assert len(tails) == sum(1 for b in range(case.batch) if sl[b] > shared.request_prefix[b, 0])
+    for first, ntiles, base, mb, mc, row, end in tails:
+        b = plan.members[mb]
+        assert mc == 1 and row == b and end == sl[b]
+        assert first * TILE == shared.request_prefix[b, 0]
+        assert (first + ntiles) * TILE >= end > (first + ntiles - 1) * TILE
+        assert base == shared.request_prefix[b, 1]
+        assert plan.request_prefix[b, 1] == base + -(-ntiles // 4)
