@@ -165,7 +165,7 @@ def profiled_traffic(kernel_src: str):
 def auto_chunk_tiles(rlt, case, tails, num_sms):
     """Tiles per CTA of the tensor-core kernel: the largest power of two (4..16) that
     still leaves two CTAs per SM over all (segment, kv head) work."""
-    p1 = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, 1, tails)
+    p1 = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, 1, tails, case.group)
     units = int(sum(int(s[1]) for s in p1.segments)) * case.num_kv_heads
     chunk = 16
     while chunk > 4 and units / chunk < 2 * num_sms:
@@ -217,7 +217,8 @@ def run_gpu(args, rank, world):
     if args.cascade != "off":
         if args.chunk_tiles == 0:
             args.chunk_tiles = auto_chunk_tiles(rlt, case, tails, torch.cuda.get_device_properties(dev).multi_processor_count)
-        plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, args.chunk_tiles, tails)
+        plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, args.chunk_tiles, tails,
+                                   case.group)
         if plan.num_segments == 0 or (args.cascade == "auto" and not tails and
                                       plan.max_rest_len == case.max_seq_len):
             plan = None
@@ -295,7 +296,8 @@ def run_gpu(args, rank, world):
     e0.record(stream)
     for _ in range(args.steps):
         if plan is not None:        # the host plans the step from its page tables, then ships the plan
-            p2 = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, args.chunk_tiles, tails)
+            p2 = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, args.chunk_tiles, tails,
+                                     case.group)
             for host, arr, devt in zip(plan_h, (p2.segments, p2.members, p2.request_prefix), plan.dev):
                 host.numpy()[:] = np.ascontiguousarray(arr, np.int32).reshape(-1)
                 devt.copy_(host, non_blocking=True)

@@ -166,31 +166,35 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
  * shared by one fixed set of requests.  Along each request's path the
  * segments' partial slots are numbered from 0.
  *   chunk_tiles     tiles per CTA of the tensor-core prefix kernel (1..32)
+ *   query_group     num_q_heads / num_kv_heads of the attention it plans for
+ *                   (a CTA holds 128 query rows, so 128 / query_group members)
  *   private_tails   non-zero: also give every request a one-member segment
  *                   for its remaining (unshared) tokens, so that the
  *                   tensor-core kernel covers all of them -- worth it when
  *                   num_q_heads/num_kv_heads >= 4 makes each request's own
  *                   query rows a dense enough contraction
- *   segments        int32 [max_segments][7]: first tile, number of tiles,
+ *   segments        int32 [max_segments][8]: first tile, number of tiles,
  *                   first partial slot, first member entry, member count,
  *                   a member whose page-table row holds the segment's pages,
- *                   end token (exclusive; a private tail may end mid-tile)
+ *                   end token (exclusive; a private tail may end mid-tile),
+ *                   first work unit (CTA) of the segment
  *   members         int32 [max_member_entries]: request ids by segment
  *   request_prefix  int32 [batch][2]: tokens of request b covered by its
  *                   segments (a multiple of 128 unless a private tail
  *                   covers all of it), partial slots they use
- *   sizes           int32 [6]: segments, member entries, most chunks of one
+ *   sizes           int32 [7]: segments, member entries, most chunks of one
  *                   segment, most partial slots of one request, most members
  *                   of one segment, most tokens of one request left to the
- *                   split-K kernel (filled even when the capacities are short)
+ *                   split-K kernel, work units (filled even when the
+ *                   capacities are short)
  * Returns RLT_ERR_OUT_OF_RANGE when max_segments or max_member_entries is too
  * small (sizes[] says what is needed), RLT_ERR_UNSUPPORTED when page_size
  * neither divides nor is a multiple of 128.
  */
 RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t max_pages,
                                    const int32_t *seq_lens, int32_t batch, int32_t page_size,
-                                   int32_t chunk_tiles, int32_t private_tails, int32_t *segments,
-                                   int32_t max_segments, int32_t *members,
+                                   int32_t chunk_tiles, int32_t query_group, int32_t private_tails,
+                                   int32_t *segments, int32_t max_segments, int32_t *members,
                                    int32_t max_member_entries, int32_t *request_prefix,
                                    int32_t *sizes);
 
@@ -209,10 +213,11 @@ RLT_API size_t rlt_paged_decode_prefix_workspace_size(int32_t batch, int32_t num
  * read from HBM once per kv head and applied to every member's queries by a
  * tcgen05 tensor-core kernel (S = Q K^T, O = P V with the members' query rows
  * as M = 128), the rest of each request goes through the split-K kernel, and
- * a log-sum-exp combine merges the partials.  num_segments, max_members,
- * max_chunks, max_prefix_slots, max_rest_len are sizes[0], [4], [2], [3], [5]
- * of the plan and chunk_tiles the value it was built with; max_rest_len == 0
- * (private tails) launches no split-K kernel.  Other arguments as
+ * a log-sum-exp combine merges the partials.  num_segments, work_units,
+ * max_prefix_slots, max_rest_len are sizes[0], [6], [3], [5] of the plan,
+ * which must have been built with this call's query group, and chunk_tiles
+ * the value it was built with; max_rest_len == 0 (private tails) launches no
+ * split-K kernel.  Other arguments as
  * rlt_paged_decode_attn; the workspace (rlt_paged_decode_prefix_workspace_size
  * bytes) is required.  num_segments == 0 runs rlt_paged_decode_attn.
  * Supported: head_dim 128, num_q_heads/num_kv_heads in {1, 2, 4, 8}, page_size
@@ -222,7 +227,7 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     const rlt_kv_pool *pool, int32_t bank, const void *q, int32_t num_q_heads,
     const int32_t *page_table, int32_t max_pages, const int32_t *seq_lens, int32_t batch,
     int32_t max_seq_len, const int32_t *segments, const int32_t *members,
-    const int32_t *request_prefix, int32_t num_segments, int32_t max_members, int32_t max_chunks,
+    const int32_t *request_prefix, int32_t num_segments, int32_t work_units,
     int32_t max_prefix_slots, int32_t chunk_tiles, int32_t max_rest_len, float scale, void *out,
     float *lse_out, void *workspace, size_t workspace_bytes, int32_t split_tokens, void *stream);
 

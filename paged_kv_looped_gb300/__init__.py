@@ -84,10 +84,10 @@ def load():
         "rlt_paged_decode_attn_noalloc": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, P, i32, i32, f32, P, P,
                                                          i32, P]),
         "rlt_validate_batch": (ctypes.c_int, [P, i32, P, i32, P, i64, i32]),
-        "rlt_plan_prefix": (ctypes.c_int, [P, i32, P, i32, i32, i32, i32, P, i32, P, i32, P, P]),
+        "rlt_plan_prefix": (ctypes.c_int, [P, i32, P, i32, i32, i32, i32, i32, P, i32, P, i32, P, P]),
         "rlt_paged_decode_prefix_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, i32]),
         "rlt_paged_decode_attn_prefix": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, P, i32, i32, P, P, P, i32,
-                                                        i32, i32, i32, i32, i32, f32, P, P, P, sz, i32, P]),
+                                                        i32, i32, i32, i32, f32, P, P, P, sz, i32, P]),
         "rlt_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     }
     for name, (res, args) in sigs.items():
@@ -307,19 +307,20 @@ def rlt_paged_gather(pool: KVPool, bank: int, page_table, seq_lens, max_len: int
 
 # ------------------------------------------------------------ shared prefixes
 
-SEG_FIELDS = 7
+SEG_FIELDS = 8
 
 
 class PrefixPlan:
     """Host result of rlt_plan_prefix plus (after ``.to(device)``) its device copies."""
 
-    def __init__(self, segments, members, request_prefix, sizes, chunk_tiles):
+    def __init__(self, segments, members, request_prefix, sizes, chunk_tiles, query_group):
         self.segments = segments            # int32 [n][6]
         self.members = members              # int32 [entries]
         self.request_prefix = request_prefix  # int32 [B][2]
         self.num_segments, self.member_entries, self.max_chunks, self.max_prefix_slots, \
-            self.max_members, self.max_rest_len = (int(x) for x in sizes)
+            self.max_members, self.max_rest_len, self.work_units = (int(x) for x in sizes)
         self.chunk_tiles = chunk_tiles
+        self.query_group = query_group
         self.dev = None
 
     def to(self, device):
@@ -332,31 +333,33 @@ class PrefixPlan:
 
 
 def rlt_plan_prefix(page_table, seq_lens, page_size: int, chunk_tiles: int = 4,
-                    private_tails: bool = False) -> PrefixPlan:
+                    private_tails: bool = False, query_group: int = 1) -> PrefixPlan:
     """Find the 128-token tiles several requests share (host arrays in, host plan out).
-    With ``private_tails`` every request's remaining tokens get a one-member segment too."""
+    With ``private_tails`` every request's remaining tokens get a one-member segment too.
+    ``query_group`` = num_q_heads / num_kv_heads of the attention the plan is for."""
     pt, ptp = _host(page_table, np.int32)
     sl, slp = _host(seq_lens, np.int32)
     B = sl.size
     req = np.zeros((B, 2), np.int32)
-    sizes = np.zeros(6, np.int32)
+    sizes = np.zeros(7, np.int32)
     lib = load()
     null = ctypes.c_void_p(0)
     tails = 1 if private_tails else 0
-    st = lib.rlt_plan_prefix(ptp, pt.shape[1], slp, B, page_size, chunk_tiles, tails, null, 0, null, 0,
+    st = lib.rlt_plan_prefix(ptp, pt.shape[1], slp, B, page_size, chunk_tiles, query_group, tails, null, 0,
+                             null, 0,
                              req.ctypes.data_as(ctypes.c_void_p), sizes.ctypes.data_as(ctypes.c_void_p))
     if st not in (0, 2):
         raise RltError(st, "rlt_plan_prefix")
     seg = np.zeros((max(int(sizes[0]), 1), SEG_FIELDS), np.int32)
     mem = np.zeros(max(int(sizes[1]), 1), np.int32)
     if st == 2:
-        _check(lib.rlt_plan_prefix(ptp, pt.shape[1], slp, B, page_size, chunk_tiles, tails,
+        _check(lib.rlt_plan_prefix(ptp, pt.shape[1], slp, B, page_size, chunk_tiles, query_group, tails,
                                    seg.ctypes.data_as(ctypes.c_void_p), seg.shape[0],
                                    mem.ctypes.data_as(ctypes.c_void_p), mem.size,
                                    req.ctypes.data_as(ctypes.c_void_p), sizes.ctypes.data_as(ctypes.c_void_p)),
                "rlt_plan_prefix")
     n = int(sizes[0])
-    return PrefixPlan(seg[:n], mem[: int(sizes[1])], req, sizes, chunk_tiles)
+    return PrefixPlan(seg[:n], mem[: int(sizes[1])], req, sizes, chunk_tiles, query_group)
 
 
 def rlt_paged_decode_prefix_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_rest_len,
@@ -371,6 +374,8 @@ def rlt_paged_decode_attn_prefix(pool: KVPool, bank: int, q, page_table, seq_len
     """Paged decode attention reading shared-prefix tiles once (plan from rlt_plan_prefix, .to(device))."""
     import torch
     B, Hq, D = q.shape
+    if plan.num_segments and plan.query_group != Hq // pool.num_kv_heads:
+        raise ValueError("the plan was built for another query group")
     if plan.dev is None:
         plan.to(q.device)
     if out is None:
@@ -387,8 +392,8 @@ def rlt_paged_decode_attn_prefix(pool: KVPool, bank: int, q, page_table, seq_len
         _dev(page_table, torch.int32, "page_table"), page_table.shape[1],
         _dev(seq_lens, torch.int32, "seq_lens"), B, int(max_seq_len),
         _dev(seg, torch.int32, "segments"), _dev(mem, torch.int32, "members"),
-        _dev(req, torch.int32, "request_prefix"), plan.num_segments, max(plan.max_members, 1),
-        plan.max_chunks, plan.max_prefix_slots, plan.chunk_tiles, rest, float(scale),
+        _dev(req, torch.int32, "request_prefix"), plan.num_segments, plan.work_units,
+        plan.max_prefix_slots, plan.chunk_tiles, rest, float(scale),
         _dev(out, torch.bfloat16, "out"), lse_ptr, ctypes.c_void_p(workspace.data_ptr()),
         workspace.numel() * workspace.element_size(), int(split_tokens), _stream(stream)),
         "rlt_paged_decode_attn_prefix")

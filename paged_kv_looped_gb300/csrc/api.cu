@@ -231,7 +231,7 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     const rlt_kv_pool *pool, int32_t bank, const void *q, int32_t num_q_heads,
     const int32_t *page_table, int32_t max_pages, const int32_t *seq_lens, int32_t batch,
     int32_t max_seq_len, const int32_t *segments, const int32_t *members,
-    const int32_t *request_prefix, int32_t num_segments, int32_t max_members, int32_t max_chunks,
+    const int32_t *request_prefix, int32_t num_segments, int32_t work_units,
     int32_t max_prefix_slots, int32_t chunk_tiles, int32_t max_rest_len, float scale, void *out,
     float *lse_out, void *workspace, size_t workspace_bytes, int32_t split_tokens, void *stream)
 {
@@ -244,7 +244,7 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
         return st;
     if (batch < 0 || max_seq_len < 0 || max_pages < 1 || num_q_heads < 1 || split_tokens < 0 ||
         split_tokens % rlt::kTileTokens != 0 || split_tokens > 128 * rlt::kTileTokens ||
-        num_segments < 0 || max_members < 1 || max_chunks < 0 || max_prefix_slots < 0 ||
+        num_segments < 0 || work_units < 0 || max_prefix_slots < 0 ||
         chunk_tiles < 1 || max_rest_len < 0 || max_rest_len > max_seq_len ||
         num_q_heads % pool->num_kv_heads != 0)
         return RLT_ERR_INVALID_ARG;
@@ -306,13 +306,10 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     pp.members = members;
     pp.num_segments = num_segments;
     pp.chunk_tiles = chunk_tiles;
-    const int per_block = 128 / group;
-    pp.member_blocks = (max_members + per_block - 1) / per_block;
-    if ((int64_t)num_segments * pp.member_blocks > 65535)
-        return RLT_ERR_UNSUPPORTED;
+    pp.work_units = work_units;
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    cudaError_t e = rlt::launch_prefix(p, pp, max_chunks, p.k_bank, p.v_bank, bank_rows, cs);
+    cudaError_t e = rlt::launch_prefix(p, pp, p.k_bank, p.v_bank, bank_rows, cs);
     if (e == cudaSuccess && max_rest_len > 0)
         e = rlt::launch_decode(p, pool->head_dim, group, cs);
     if (e == cudaSuccess)

@@ -34,30 +34,42 @@ namespace {
 // only touch TMEM lanes 32w..32w+31), warp 4 issues the MMAs, warp 5 issues the
 // TMA copies.  Work goes in 64-token sub-tiles (half a planner tile).
 constexpr int kSoftWarps = 4;
-constexpr int kPThreads = (kSoftWarps + 2) * 32;
-constexpr int kMmaWarp = kSoftWarps, kLoadWarp = kSoftWarps + 1;
+constexpr int kPThreads = (kSoftWarps + 3) * 32;
+// The MMA warp spins on its barriers: it shares a scheduler (warp id mod 4) with softmax warp 2,
+// which has live rows only for more than 64 query rows.
+constexpr int kLoadVWarp = kSoftWarps, kLoadKWarp = kSoftWarps + 1, kMmaWarp = kSoftWarps + 2;
 constexpr int kSub = 64;                    // tokens per sub-tile
 constexpr int kStagesP = 4;                 // K/V sub-tile ring depth
 constexpr int kHalfQ = 128 * 128;           // one 64-element column block of the 128 Q rows
 constexpr int kHalfKV = kSub * 128;         // one 64-dim column block of a sub-tile (64 rows x 128 B)
 constexpr int kKVBytes = 2 * kHalfKV;       // K (or V) of one sub-tile
-constexpr int kStageBytesP = 2 * kKVBytes;  // K + V
+constexpr int kStageBytesP = 2 * kKVBytes;  // one K slot + one V slot
 constexpr int kPBytes = 128 * kSub * 2;     // P of one sub-tile: 128 rows x 64 tokens, bf16
 constexpr int kMaxChunkTiles = 32;
 constexpr int kMaxBoxes = 2 * kMaxChunkTiles * 4;   // sub-tiles x boxes (page_size 16: 4 per sub-tile)
 constexpr int kQOff = 0;
+constexpr int kSBufs = 4;                   // S buffers in TMEM: S runs up to 4 sub-tiles ahead
+constexpr int kPBufs = 3;                   // P buffers in shared memory
 constexpr int kPOff = kQOff + 2 * kHalfQ;
-constexpr int kStageOff = kPOff + 2 * kPBytes;
+constexpr int kStageOff = kPOff + kPBufs * kPBytes;
 constexpr int kRowsOff = kStageOff + kStagesP * kStageBytesP;
 constexpr int kMemOff = kRowsOff + kMaxBoxes * 4;
 constexpr int kBarOff = kMemOff + 128 * 4;
-constexpr int kNumBars = 2 * kStagesP + 6;  // full[4], free[4], s_full[2], p_full[2], o_full[2]
+// K and V have rings of their own: a K slot is free once S has read it, a V slot once P.V has
+constexpr int kNumBars = 4 * kStagesP + 2 * kSBufs + kPBufs;   // K/V rings, s_full, p_full, o_full
 constexpr int kSmemP = kBarOff + kNumBars * 8 + 16 + 1024;
-constexpr uint32_t kTmemCols = 256;         // S[2] x 64 cols, O x 128 cols
-constexpr uint32_t kColS = 0, kColO = 128;
+constexpr uint32_t kTmemCols = 512;         // S[4] x 64 cols, O x 128 cols
+constexpr uint32_t kColS = 0, kColO = kSBufs * kSub;
 // O accumulates in TMEM against a per-row reference max that moves only when
 // the row's running max exceeds it by more than this (log2 units): p <= 2^8.
 constexpr float kRescaleThreshold = 8.f;
+
+constexpr int kQBarrier = 1;                // named barrier: Q staged (softmax warps + MMA warp)
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 __global__ void __launch_bounds__(kPThreads, 1)
     decode_prefix_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -73,23 +85,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
     int32_t *box_rows = reinterpret_cast<int32_t *>(base + kRowsOff);
     int32_t *mem = reinterpret_cast<int32_t *>(base + kMemOff);
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + kBarOff);
-    uint64_t *full = bars, *stage_free = bars + kStagesP;
-    uint64_t *s_full = bars + 2 * kStagesP, *p_full = s_full + 2, *o_full = s_full + 4;
+    uint64_t *full_k = bars, *free_k = bars + kStagesP, *full_v = bars + 2 * kStagesP,
+             *free_v = bars + 3 * kStagesP;
+    uint64_t *s_full = bars + 4 * kStagesP, *p_full = s_full + kSBufs, *o_full = p_full + kSBufs;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
 
+    // work unit -> (segment, chunk, member block) through the segments' work offsets
     const int G = p.num_q_heads / p.num_kv_heads;
-    const int chunk = blockIdx.x, g = blockIdx.y;
-    const int seg = blockIdx.z / pp.member_blocks, mb = blockIdx.z % pp.member_blocks;
-    if (seg >= pp.num_segments)
-        return;
-    const int32_t *sd = pp.segments + seg * kSegFields;
+    const int g = blockIdx.y;
+    const int unit = blockIdx.x;
+    int lo = 0, hi = pp.num_segments - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pp.segments[mid * kSegFields + kSegWorkBegin] <= unit)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int32_t *sd = pp.segments + lo * kSegFields;
+    const int per_block = 128 / G;
+    const int mblocks = (sd[kSegMemberCount] + per_block - 1) / per_block;
+    const int local = unit - sd[kSegWorkBegin];
+    const int chunk = local / mblocks, mb = local % mblocks;
     const int num_tiles = sd[kSegNumTiles];
     const int t0 = chunk * pp.chunk_tiles;
-    if (t0 >= num_tiles)
+    if (t0 >= num_tiles || local < 0)
         return;
     const int nt = min(pp.chunk_tiles, num_tiles - t0);
-    const int per_block = 128 / G;
     const int m0 = mb * per_block;
     const int n_mem = min(per_block, sd[kSegMemberCount] - m0);
     if (n_mem <= 0)
@@ -125,61 +148,64 @@ __global__ void __launch_bounds__(kPThreads, 1)
         box_rows[i] = (int32_t)((page * p.num_kv_heads + g) * p.page_size + tok % p.page_size);
     }
     if (tid == 0) {
-        for (int i = 0; i < kStagesP; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&stage_free[i], 1);
-        }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4 * kStagesP; ++i)
+            mbar_init(&bars[i], 1);
+        for (int i = 0; i < kSBufs; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], (R + 31) / 32);   // one arrive per softmax warp with live rows
-            mbar_init(&o_full[i], 1);
         }
+        for (int i = 0; i < kPBufs; ++i)
+            mbar_init(&o_full[i], 1);
         *abort_flag = 0;
         mbar_init_fence();
     }
     if (warp == 0)
         tc::tmem_alloc(tslot, kTmemCols);
-    __syncthreads();
-
-    // Query rows r = member * G + head, K-major, 128-byte swizzled (rows >= R unused).
-    for (int i = tid; i < R * 16; i += kPThreads) {
-        const int r = i >> 4, c16 = i & 15;
-        const int b = mem[r / G], h = r % G;
-        const uint4 v = *reinterpret_cast<const uint4 *>(
-            p.q + ((int64_t)b * p.num_q_heads + g * G + h) * 128 + c16 * 8);
-        *reinterpret_cast<uint4 *>(qs + (c16 >> 3) * kHalfQ + tc::sw128_offset(r, (c16 & 7) * 8)) = v;
-    }
-    fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
     bool ok = true;
 
-    if (warp == kLoadWarp) {
-        // ---------------------------------------------------------- TMA producer
-        // Lane j copies box j/4, column block (j/2)&1, of K (j even) or V (j odd).
-        if (lane == 0) {
-            tc::prefetch_tmap(&kmap);
-            tc::prefetch_tmap(&vmap);
+    if (warp < kSoftWarps) {
+        // Query rows r = member * G + head, K-major, 128-byte swizzled (rows >= R unused),
+        // staged while the producers already stream K and V.
+        for (int i = tid; i < R * 16; i += kSoftWarps * 32) {
+            const int r = i >> 4, c16 = i & 15;
+            const int b = mem[r / G], h = r % G;
+            const uint4 v = *reinterpret_cast<const uint4 *>(
+                p.q + ((int64_t)b * p.num_q_heads + g * G + h) * 128 + c16 * 8);
+            *reinterpret_cast<uint4 *>(qs + (c16 >> 3) * kHalfQ + tc::sw128_offset(r, (c16 & 7) * 8)) = v;
         }
+        fence_proxy_async();
+        named_barrier_sync(kQBarrier, (kSoftWarps + 1) * 32);
+    }
+
+    if (warp == kLoadKWarp || warp == kLoadVWarp) {
+        // ------------------------------------------------- TMA producers (K, V)
+        // Lane j copies box j/2, column block j&1 of this warp's tensor.
+        const bool is_v = warp == kLoadVWarp;
+        const CUtensorMap *map = is_v ? &vmap : &kmap;
+        uint64_t *fullx = is_v ? full_v : full_k, *freex = is_v ? free_v : free_k;
+        unsigned char *ring = stages + (is_v ? kStagesP * kKVBytes : 0);
+        if (lane == 0)
+            tc::prefetch_tmap(map);
         int j = 0;
         for (; j < nsub && ok; ++j) {
             const int st = j % kStagesP;
             if (j >= kStagesP)
-                ok = mbar_wait_or_abort(&stage_free[st], ((j / kStagesP) - 1) & 1u, abort_flag);
+                ok = mbar_wait_or_abort(&freex[st], ((j / kStagesP) - 1) & 1u, abort_flag);
             if (!ok)
                 break;
-            unsigned char *kst = stages + st * kStageBytesP;
             const int64_t sub_begin = tok_begin + (int64_t)j * kSub;
             const int nbox = (int)min((int64_t)boxes, (tok_end - sub_begin + BR - 1) / BR);
             if (lane == 0)
-                mbar_arrive_expect_tx(&full[st], (uint32_t)(nbox * BR * 128 * 4));
+                mbar_arrive_expect_tx(&fullx[st], (uint32_t)(nbox * BR * 128 * 2));
             __syncwarp();
-            if (lane < 4 * nbox) {
-                const int box = lane >> 2, half = (lane >> 1) & 1, is_v = lane & 1;
-                tc::tma_load_2d(kst + is_v * kKVBytes + half * kHalfKV + box * BR * 128,
-                                is_v ? &vmap : &kmap, half * 64, box_rows[j * boxes + box], &full[st]);
+            if (lane < 2 * nbox) {
+                const int box = lane >> 1, half = lane & 1;
+                tc::tma_load_2d(ring + st * kKVBytes + half * kHalfKV + box * BR * 128, map, half * 64,
+                                box_rows[j * boxes + box], &fullx[st]);
             }
         }
         if (!ok) {
@@ -187,59 +213,76 @@ __global__ void __launch_bounds__(kPThreads, 1)
             // copies of the last (up to 4) sub-tiles may still be landing: wait for them (bounded)
             if (lane == 0)
                 for (int k = max(0, j - kStagesP); k < j; ++k)
-                    mbar_wait(&full[k % kStagesP], (k / kStagesP) & 1u);
+                    mbar_wait(&fullx[k % kStagesP], (k / kStagesP) & 1u);
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------- MMA issuer
         const uint32_t id_s = tc::instr_desc_bf16(128, kSub, false);
         const uint32_t id_o = tc::instr_desc_bf16(128, 128, true);
         const uint32_t qa = smem_u32(qs), pa = smem_u32(pbuf), sa = smem_u32(stages);
-        auto issue_s = [&](int j) -> bool {   // S_j = Q K_j^T into S[j % 2]
-            const int st = j % kStagesP;
-            if (!mbar_wait_or_abort(&full[st], (j / kStagesP) & 1u, abort_flag))
-                return false;
-            tc::fence_after_sync();
-            if (lane == 0) {
-                const uint32_t ka = sa + st * kStageBytesP;
+        named_barrier_sync(kQBarrier, (kSoftWarps + 1) * 32);   // Q staged
+        // Event loop: issue S_k as soon as K_k has landed and S buffer k%4 is free
+        // (P.V of k-4 issued), and P.V_j as soon as every softmax warp wrote P_j
+        // and V_j has landed.  Probes do not block, so neither waits on the other.
+        int s_next = 0, pv_next = 0;
+        uint64_t t_idle = 0;
+        while (pv_next < nsub) {
+            bool progress = false;
+            if (s_next < nsub && s_next < pv_next + kSBufs &&
+                __all_sync(kFullMask, mbar_test_wait(&full_k[s_next % kStagesP], (s_next / kStagesP) & 1u))) {
+                tc::fence_after_sync();
+                if (lane == 0) {
+                    const uint32_t ka = sa + (s_next % kStagesP) * kKVBytes;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_bf16(tmem + kColS + (j & 1) * kSub,
-                                 tc::smem_desc(qa + (kk >> 2) * kHalfQ + (kk & 3) * 32, 16, 1024),
-                                 tc::smem_desc(ka + (kk >> 2) * kHalfKV + (kk & 3) * 32, 16, 1024), id_s,
-                                 kk > 0);
-                tc::mma_commit(&s_full[j & 1]);
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_bf16(tmem + kColS + (s_next % kSBufs) * kSub,
+                                     tc::smem_desc(qa + (kk >> 2) * kHalfQ + (kk & 3) * 32, 16, 1024),
+                                     tc::smem_desc(ka + (kk >> 2) * kHalfKV + (kk & 3) * 32, 16, 1024), id_s,
+                                     kk > 0);
+                    tc::mma_commit(&s_full[s_next % kSBufs]);
+                    tc::mma_commit(&free_k[s_next % kStagesP]);
+                }
+                __syncwarp();
+                ++s_next;
+                progress = true;
             }
-            __syncwarp();
-            return true;
-        };
-        ok = issue_s(0);
-        if (ok && nsub > 1)
-            ok = issue_s(1);
-        for (int j = 0; j < nsub && ok; ++j) {
-            // P_j written, S[j%2] read and O rescaled where needed by the softmax warps
-            ok = mbar_wait_or_abort(&p_full[j & 1], (j >> 1) & 1u, abort_flag);
-            if (!ok)
-                break;
-            tc::fence_after_sync();
-            if (lane == 0) {
-                const uint32_t va = sa + (j % kStagesP) * kStageBytesP + kKVBytes;
-                const uint32_t pj = pa + (j & 1) * kPBytes;
+            const int j = pv_next;
+            if (j < s_next &&
+                __all_sync(kFullMask, mbar_test_wait(&p_full[j % kSBufs], (j / kSBufs) & 1u) &&
+                                          mbar_test_wait(&full_v[j % kStagesP], (j / kStagesP) & 1u))) {
+                tc::fence_after_sync();
+                if (lane == 0) {
+                    const uint32_t va = sa + (kStagesP + j % kStagesP) * kKVBytes;
+                    const uint32_t pj = pa + (j % kPBufs) * kPBytes;
 #pragma unroll
-                for (int kk = 0; kk < kSub / 16; ++kk)
-                    tc::mma_bf16(tmem + kColO, tc::smem_desc(pj + kk * 32, 16, 1024),
-                                 tc::smem_desc(va + kk * 2048, kHalfKV, 1024), id_o, (j > 0) || (kk > 0));
-                tc::mma_commit(&o_full[j & 1]);
-                tc::mma_commit(&stage_free[j % kStagesP]);
+                    for (int kk = 0; kk < kSub / 16; ++kk)
+                        tc::mma_bf16(tmem + kColO, tc::smem_desc(pj + kk * 32, 16, 1024),
+                                     tc::smem_desc(va + kk * 2048, kHalfKV, 1024), id_o, (j > 0) || (kk > 0));
+                    tc::mma_commit(&o_full[j % kPBufs]);
+                    tc::mma_commit(&free_v[j % kStagesP]);
+                }
+                __syncwarp();
+                ++pv_next;
+                progress = true;
             }
-            __syncwarp();
-            if (j + 2 < nsub)
-                ok = issue_s(j + 2);
+            if (progress) {
+                t_idle = 0;
+            } else {
+                __nanosleep(32);
+                const uint64_t now = global_ns();
+                if (t_idle == 0)
+                    t_idle = now;
+                else if (now - t_idle > kWaitLimitNs || *abort_flag != 0) {
+                    ok = false;
+                    break;
+                }
+            }
         }
         if (!ok) {
             *abort_flag = 1;
             // let issued MMAs finish before the CTA gives up its shared memory (bounded)
-            if (lane == 0)
-                mbar_wait(&stage_free[0], 0);    // returns at once or after the time limit
+            if (lane == 0 && pv_next > 0)
+                mbar_wait(&o_full[(pv_next - 1) % kPBufs], ((pv_next - 1) / kPBufs) & 1u);
         }
     } else if (warp * 32 < R) {
         // ------------------------------------------- softmax warps with live rows
@@ -248,12 +291,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
         float m_ref = -CUDART_INF_F, l_run = 0.f;
 
         for (int j = 0; j < nsub && ok; ++j) {
-            ok = mbar_wait_or_abort(&s_full[j & 1], (j >> 1) & 1u, abort_flag);
+            ok = mbar_wait_or_abort(&s_full[j % kSBufs], (j / kSBufs) & 1u, abort_flag);
             if (!ok)
                 break;
             tc::fence_after_sync();
             float v[64];
-            tc::tmem_ld64(t_lane + kColS + (j & 1) * kSub, v);
+            tc::tmem_ld64(t_lane + kColS + (j % kSBufs) * kSub, v);
             const int valid = (int)min((int64_t)kSub, tok_end - (tok_begin + (int64_t)j * kSub));
             if (valid < kSub) {
                 // ragged end of a private tail: mask the missing tokens, and zero their V
@@ -262,7 +305,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 for (int i = 0; i < 64; ++i)
                     v[i] = i < valid ? v[i] : -CUDART_INF_F;
                 if (warp == 0) {
-                    unsigned char *vst = stages + (j % kStagesP) * kStageBytesP + kKVBytes;
+                    // after this sub-tile's V copy has landed (it may write garbage rows too)
+                    ok = __all_sync(kFullMask, mbar_wait_or_abort(&full_v[j % kStagesP], (j / kStagesP) & 1u,
+                                                                  abort_flag));
+                    if (!ok)
+                        break;
+                    unsigned char *vst = stages + (kStagesP + j % kStagesP) * kKVBytes;
                     for (int c = lane; c < (kSub - valid) * 16; c += 32) {
                         const int r = valid + c / 16, c16 = c % 16;
                         *reinterpret_cast<uint4 *>(vst + (c16 >> 3) * kHalfKV + r * 128 + (c16 & 7) * 16) =
@@ -280,7 +328,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const float scale_o = exp2f(m_ref - m_next);   // 1 if the reference stays, 0 at first
             if (__any_sync(kFullMask, up) && j > 0) {
                 // rescale this row's O (PV of sub-tile j-1 must have landed)
-                ok = mbar_wait_or_abort(&o_full[(j - 1) & 1], ((j - 1) >> 1) & 1u, abort_flag);
+                ok = mbar_wait_or_abort(&o_full[(j - 1) % kPBufs], ((j - 1) / kPBufs) & 1u, abort_flag);
                 if (!__all_sync(kFullMask, ok)) {
                     ok = false;
                     break;
@@ -308,15 +356,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 w[i] = cvt_bf16x2(p0, p1);
             }
             l_run += lsum;
-            if (j >= 2) {   // P[j%2] was read by the PV of sub-tile j-2
-                ok = mbar_wait_or_abort(&o_full[j & 1], ((j - 2) >> 1) & 1u, abort_flag);
+            if (j >= kPBufs) {   // P[j%3] was read by the P.V of sub-tile j-3
+                ok = mbar_wait_or_abort(&o_full[j % kPBufs], ((j - kPBufs) / kPBufs) & 1u, abort_flag);
                 if (!__all_sync(kFullMask, ok)) {
                     ok = false;
                     break;
                 }
             }
             if (row < R) {
-                unsigned char *pj = pbuf + (j & 1) * kPBytes;
+                unsigned char *pj = pbuf + (j % kPBufs) * kPBytes;
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8)
                     *reinterpret_cast<uint4 *>(pj + tc::sw128_offset(row, c8 * 8)) =
@@ -326,10 +374,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&p_full[j & 1]);
+                mbar_arrive(&p_full[j % kSBufs]);
         }
         if (ok) {
-            ok = mbar_wait_or_abort(&o_full[(nsub - 1) & 1], ((nsub - 1) >> 1) & 1u, abort_flag);
+            ok = mbar_wait_or_abort(&o_full[(nsub - 1) % kPBufs], ((nsub - 1) / kPBufs) & 1u, abort_flag);
             ok = __all_sync(kFullMask, ok);
         }
         if (!ok)
@@ -412,11 +460,10 @@ bool prefix_supported(int head_dim, int group, int page_size)
 
 size_t prefix_smem_bytes(int, int) { return kSmemP; }
 
-cudaError_t launch_prefix(const DecodeParams &p, const PrefixParams &pp, int max_chunks,
-                          const void *k_bank, const void *v_bank, int64_t bank_rows,
-                          cudaStream_t stream)
+cudaError_t launch_prefix(const DecodeParams &p, const PrefixParams &pp, const void *k_bank,
+                          const void *v_bank, int64_t bank_rows, cudaStream_t stream)
 {
-    if (pp.num_segments == 0 || max_chunks == 0)
+    if (pp.num_segments == 0 || pp.work_units == 0)
         return cudaSuccess;
     if (pp.chunk_tiles < 1 || pp.chunk_tiles > kMaxChunkTiles || bank_rows >= (int64_t(1) << 31))
         return cudaErrorInvalidValue;
@@ -436,7 +483,7 @@ cudaError_t launch_prefix(const DecodeParams &p, const PrefixParams &pp, int max
             return e;
         configured.fetch_or(bit);
     }
-    const dim3 grid(max_chunks, p.num_kv_heads, pp.num_segments * pp.member_blocks);
+    const dim3 grid(pp.work_units, p.num_kv_heads, 1);
     decode_prefix_kernel<<<grid, kPThreads, kSmemP, stream>>>(kmap, vmap, p, pp);
     return cudaGetLastError();
 }
@@ -448,14 +495,16 @@ cudaError_t launch_prefix(const DecodeParams &p, const PrefixParams &pp, int max
 extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t max_pages,
                                               const int32_t *seq_lens, int32_t batch,
                                               int32_t page_size, int32_t chunk_tiles,
-                                              int32_t private_tails, int32_t *segments,
+                                              int32_t query_group, int32_t private_tails,
+                                              int32_t *segments,
                                               int32_t max_segments, int32_t *members,
                                               int32_t max_member_entries, int32_t *request_prefix,
                                               int32_t *sizes)
 {
     using rlt::kPrefixTile;
     if (batch < 0 || max_pages < 0 || page_size < 1 || chunk_tiles < 1 ||
-        chunk_tiles > rlt::kMaxChunkTiles || max_segments < 0 || max_member_entries < 0 ||
+        chunk_tiles > rlt::kMaxChunkTiles || query_group < 1 || query_group > 128 ||
+        max_segments < 0 || max_member_entries < 0 ||
         sizes == nullptr || (batch > 0 && (page_table == nullptr || seq_lens == nullptr ||
                                            request_prefix == nullptr)))
         return RLT_ERR_INVALID_ARG;
@@ -548,11 +597,18 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
         max_chunks = std::max(max_chunks, chunks[s]);
         max_members = std::max(max_members, (int)segs[s].mem.size());
     }
+    // work units: (segment, chunk, member block); a member block holds 128 / query_group members
+    const int per_block = 128 / query_group;
+    std::vector<int64_t> work_begin(nseg + 1, 0);
+    for (int s = 0; s < nseg; ++s)
+        work_begin[s + 1] = work_begin[s] + (int64_t)chunks[s] *
+                                                ((segs[s].mem.size() + per_block - 1) / per_block);
     sizes[0] = nseg;
     sizes[1] = (int32_t)member_entries;
     sizes[2] = max_chunks;
     sizes[3] = 0;
     sizes[4] = max_members;
+    sizes[6] = (int32_t)work_begin[nseg];
     int max_slots = 0;
     int64_t max_rest = 0;
     for (int b = 0; b < batch; ++b) {
@@ -577,6 +633,7 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
         row[rlt::kSegMemberCount] = (int32_t)segs[s].mem.size();
         row[rlt::kSegPageRow] = segs[s].mem[0];
         row[rlt::kSegEndToken] = (int32_t)segs[s].end_token;
+        row[rlt::kSegWorkBegin] = (int32_t)work_begin[s];
         for (int b : segs[s].mem)
             members[m++] = b;
     }

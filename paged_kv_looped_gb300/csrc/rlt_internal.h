@@ -42,21 +42,20 @@ constexpr int kPrefixTile = 128;
 
 // Fields of one segment of a prefix plan (rlt_plan_prefix).
 enum PrefixSegField { kSegFirstTile = 0, kSegNumTiles, kSegSlotBase, kSegMemberBegin,
-                      kSegMemberCount, kSegPageRow, kSegEndToken, kSegFields };
+                      kSegMemberCount, kSegPageRow, kSegEndToken, kSegWorkBegin, kSegFields };
 
 struct PrefixParams {
     const int32_t *segments;     // [num_segments][kSegFields]
     const int32_t *members;      // request ids, grouped by segment
     int32_t num_segments;
     int32_t chunk_tiles;         // 128-token tiles per CTA
-    int32_t member_blocks;       // CTAs per segment along the members
+    int32_t work_units;          // (segment, chunk, member block) items: the grid's x extent
 };
 
 bool prefix_supported(int head_dim, int group, int page_size);
 size_t prefix_smem_bytes(int chunk_tiles, int page_size);
-cudaError_t launch_prefix(const DecodeParams &p, const PrefixParams &pp, int max_chunks,
-                          const void *k_bank, const void *v_bank, int64_t bank_rows,
-                          cudaStream_t stream);
+cudaError_t launch_prefix(const DecodeParams &p, const PrefixParams &pp, const void *k_bank,
+                          const void *v_bank, int64_t bank_rows, cudaStream_t stream);
 
 // Split-K plan for one decode call.
 struct DecodePlan {

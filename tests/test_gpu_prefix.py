@@ -24,7 +24,7 @@ def run_both(case, h, device, chunk_tiles=4, split_tokens=0, private_tails=False
     pt = i32_dev(case.page_table, device)
     sl = i32_dev(case.seq_lens, device)
     plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, chunk_tiles,
-                               private_tails).to(device)
+                               private_tails, case.group).to(device)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=device)
     out = rlt.rlt_paged_decode_attn_prefix(pool, 0, q, pt, sl, case.max_seq_len, plan, lse_out=lse,
                                            split_tokens=split_tokens)
@@ -120,7 +120,8 @@ def test_longctx_full_size_sampled(cuda_device):
     q = bf16_dev(q_bits, cuda_device)
     pt = i32_dev(case.page_table, cuda_device)
     sl = i32_dev(case.seq_lens, cuda_device)
-    plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, 8).to(cuda_device)
+    plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, 8,
+                               query_group=case.group).to(cuda_device)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=cuda_device)
     got = rlt.rlt_paged_decode_attn_prefix(pool, 0, q, pt, sl, case.max_seq_len, plan, lse_out=lse)
     got = got.float().cpu().numpy()

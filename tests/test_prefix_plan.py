@@ -47,7 +47,7 @@ def check_plan(case, chunk_tiles=4):
     # segments: members share the segment's tiles page for page, and nobody else does
     seg_of_tile = {}
     for s in range(plan.num_segments):
-        first, n, base, mb, mc, row, end = plan.segments[s]
+        first, n, base, mb, mc, row, end, work = plan.segments[s]
         assert end == (first + n) * TILE
         mem = plan.members[mb: mb + mc]
         assert mc >= 2 and row in mem and list(mem) == sorted(mem)
@@ -67,6 +67,12 @@ def check_plan(case, chunk_tiles=4):
             slots += list(range(base, base + -(-n // chunk_tiles)))
         assert slots == list(range(len(slots))) and len(slots) == plan.request_prefix[b, 1]
     assert plan.max_prefix_slots == (plan.request_prefix[:, 1].max() if B else 0)
+    # work units: chunks x member blocks per segment, numbered in segment order
+    units = 0
+    for s in range(plan.num_segments):
+        assert plan.segments[s][7] == units
+        units += -(-int(plan.segments[s][1]) // chunk_tiles) * -(-int(plan.segments[s][4]) // 128)
+    assert plan.work_units == units
     return plan
 
 
@@ -133,10 +139,10 @@ def test_private_tails_cover_every_token(name):
     assert np.array_equal(plan.request_prefix[:, 0], sl)
     # the shared segments are unchanged; one tail per request follows them
     n = shared.num_segments
-    assert np.array_equal(plan.segments[:n], shared.segments)
+    assert np.array_equal(plan.segments[:n, :7], shared.segments[:, :7])
     tails = plan.segments[n:]
     assert len(tails) == sum(1 for b in range(case.batch) if sl[b] > shared.request_prefix[b, 0])
-    for first, ntiles, base, mb, mc, row, end in tails:
+    for first, ntiles, base, mb, mc, row, end, work in tails:
         b = plan.members[mb]
         assert mc == 1 and row == b and end == sl[b]
         assert first * TILE == shared.request_prefix[b, 0]
