@@ -76,6 +76,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                          const __grid_constant__ CUtensorMap vmap, const DecodeParams p,
                          const PrefixParams pp)
 {
+    // the split-K kernel that follows may start on SMs this grid leaves idle
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
