@@ -143,16 +143,19 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(kernel_src: str):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on this source."""
+def profiled_traffic(workload: str, cascade: bool):
+    """Per-launch DRAM bytes of the call's dominant kernel from the committed ncu summary,
+    if it was taken on this workload and on the kernel's current source."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "attn_traffic.txt")
+    name, src = (("prefix_traffic.txt", "attn_prefix.cu") if cascade else ("attn_traffic.txt", "attn.cu"))
     try:
-        lines = dict(l.split(":", 1) for l in open(path).read().splitlines() if ":" in l)
+        text = open(os.path.join(ROOT, "profiles", name)).read()
     except OSError:
         return None
-    digest = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
-    if lines.get("source_sha256_16", "").strip() != digest:
+    lines = {k.strip(): v.strip() for k, v in (l.split(":", 1) for l in text.splitlines() if ":" in l)}
+    src_path = os.path.join(ROOT, "paged_kv_looped_gb300", "csrc", src)
+    digest = hashlib.sha256(open(src_path, "rb").read()).hexdigest()[:16]
+    if lines.get("source_sha256_16") != digest or lines.get("workload") != workload:
         return None
     try:
         return float(lines["dram_bytes_per_full_launch"])
@@ -244,23 +247,23 @@ def run_gpu(args, rank, world):
 
     ev_attn = []
 
-    def step(time_attn=False):
+    def step(st, time_attn=False):
         if nz is not None:
-            rlt.rlt_latent_noise_init(seeds, pos, nz.channels, nz.initializer_range, out=noise, stream=stream)
+            rlt.rlt_latent_noise_init(seeds, pos, nz.channels, nz.initializer_range, out=noise, stream=st)
         for i, bank in enumerate(banks):
-            rlt.rlt_kv_append(pool, bank, kn[i], vn[i], loc, stream=stream)
+            rlt.rlt_kv_append(pool, bank, kn[i], vn[i], loc, stream=st)
             if time_attn:
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
+                e0.record(st)
             if plan is not None:
                 rlt.rlt_paged_decode_attn_prefix(pool, bank, q[i], pt, sl, case.max_seq_len, plan, out=out[i],
-                                                 workspace=ws, split_tokens=args.split_tokens, stream=stream)
+                                                 workspace=ws, split_tokens=args.split_tokens, stream=st)
             else:
                 rlt.rlt_paged_decode_attn(pool, bank, q[i], pt, sl, case.max_seq_len, out=out[i], workspace=ws,
-                                          split_tokens=args.split_tokens, stream=stream)
+                                          split_tokens=args.split_tokens, stream=st)
             if time_attn:
-                e1.record(stream)
+                e1.record(st)
                 ev_attn.append((e0, e1))
 
     def barrier():
@@ -271,8 +274,27 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize(dev)
 
     for _ in range(args.warmup):
-        step()
+        step(stream)
     assert rlt.rlt_get_device_error() == 0
+
+    # the whole step as one CUDA-graph submission (every call is stream-capturable)
+    graph = None
+    if args.graph == "on":
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            step(side)
+        stream.wait_stream(side)
+        for _ in range(args.warmup):
+            graph.replay()
+        assert rlt.rlt_get_device_error() == 0
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step(stream)
 
     # ---- timed region: inputs resident in HBM; each bank's KV (> L2) is read once per step
     gpu_id = gpu_id_for_smi(torch, dev)
@@ -282,8 +304,12 @@ def run_gpu(args, rank, world):
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for _ in range(args.steps):
-            step(time_attn=True)
+            run_step()
         t1.record(stream)
+        barrier()
+        # the attention calls one by one (eager launches, an event pair around each) for the roofline
+        for _ in range(args.steps):
+            step(stream, time_attn=True)
         barrier()
     ms_total = t0.elapsed_time(t1)
     attn_ms = [a.elapsed_time(b) for a, b in ev_attn]
@@ -298,6 +324,9 @@ def run_gpu(args, rank, world):
         if plan is not None:        # the host plans the step from its page tables, then ships the plan
             p2 = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, args.chunk_tiles, tails,
                                      case.group)
+            # a captured step stays valid while the plan's shape (grid, slots) is unchanged
+            assert graph is None or (p2.num_segments, p2.work_units, p2.max_prefix_slots, p2.max_rest_len) == \
+                (plan.num_segments, plan.work_units, plan.max_prefix_slots, plan.max_rest_len)
             for host, arr, devt in zip(plan_h, (p2.segments, p2.members, p2.request_prefix), plan.dev):
                 host.numpy()[:] = np.ascontiguousarray(arr, np.int32).reshape(-1)
                 devt.copy_(host, non_blocking=True)
@@ -310,7 +339,7 @@ def run_gpu(args, rank, world):
         if nz is not None:
             seeds.copy_(seeds_h, non_blocking=True)
             pos.copy_(pos_h, non_blocking=True)
-        step()
+        run_step()
         out_h.copy_(out, non_blocking=True)
         if nz is not None:
             noise_h.copy_(noise, non_blocking=True)
@@ -329,7 +358,7 @@ def run_gpu(args, rank, world):
         per_lp = 3 if ws_bytes > 0 else 2
     combine = ws_bytes > 0
     launches = args.steps * (len(banks) * per_lp + (1 if nz is not None else 0))
-    return dict(case=case, banks=banks, cascade=plan is not None, ms_total=ms_total, attn_ms=attn_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+    return dict(case=case, banks=banks, cascade=plan is not None, graph=graph is not None, ms_total=ms_total, attn_ms=attn_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                 clocks=clocks.summary(), launches=launches, combine=combine, ws_bytes=ws_bytes)
 
 
@@ -407,7 +436,7 @@ def config_dict(case, args):
             "unique_kv_tokens_per_layer_plane": case.unique_tokens(),
             "split_tokens": args.split_tokens or "auto",
             "cascade": args.cascade, "chunk_tiles": args.chunk_tiles, "tails": args.tails,
-            "banks_run": args.banks or "all",
+            "banks_run": args.banks or "all", "cuda_graph": args.graph,
             "l2": "inputs larger than L2: every bank's KV exceeds the 129 MB L2 and each is read once per step"}
 
 
@@ -447,6 +476,8 @@ def main():
     ap.add_argument("--tails", default="auto", choices=["auto", "on", "off"],
                     help="also send each request's unshared tokens through the tensor-core kernel "
                          "(auto: when a kv head serves >= 8 query heads)")
+    ap.add_argument("--graph", default="on", choices=["on", "off"],
+                    help="submit each decode step as one captured CUDA graph (on) or as eager launches")
     ap.add_argument("--banks", type=int, default=0,
                     help="run only the first N layer-plane banks (small-footprint case for profilers); 0 = all")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU time for cpu_baseline")
@@ -476,7 +507,7 @@ def main():
     a_bytes = attn_bytes(case)
     peak, peak_kind = hbm_peak()
     achieved = a_bytes / (attn_launch_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(os.path.join(ROOT, "paged_kv_looped_gb300", "csrc", "attn.cu"))
+    traffic = profiled_traffic(case.name, r["cascade"])
 
     cpu = None
     if rank == 0 and args.cpu_budget > 0:

@@ -13,6 +13,15 @@
  * time is skipped and recorded in the device error word
  * (rlt_get_device_error).
  *
+ * CUDA graphs: every compute call may be recorded by stream capture, so that a
+ * whole decode step (every layer-plane bank's append and attention, the noise)
+ * is one graph submission, as the pages' engines run decode ([FFM] "Recurrent
+ * depth": the decode CUDA graph; vllm-rlt PR #148, decode loops fused into one
+ * submission).  Make each kind of call once on the device before capturing it
+ * (the first call sets per-device kernel attributes).  A replay reads the
+ * arrays' contents at replay time; shapes, max_seq_len, split_tokens and a
+ * shared-prefix plan's sizes are fixed at capture.
+ *
  * Sources (page title, section):
  *  [FFM]   "Faster fuzzy minds" (dibbla.space/posts/matrices/fast_subconscious)
  *          - "When scheduler does the work": paged KV cache = a flat pool of
