@@ -166,12 +166,14 @@ def profiled_traffic(workload: str, cascade: bool):
 # ------------------------------------------------------------ GPU arm
 
 def auto_chunk_tiles(rlt, case, tails, num_sms):
-    """Tiles per CTA of the tensor-core kernel: the largest power of two (4..16) that
-    still leaves two CTAs per SM over all (segment, kv head) work."""
+    """Tiles per work item of the persistent tensor-core kernel: the largest power of two
+    (1..16) that still gives every CTA (one per SM) at least 16 items, so that the
+    item-granular split of the work across the CTAs stays within a few percent."""
     p1 = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, 1, tails, case.group)
-    units = int(sum(int(s[1]) for s in p1.segments)) * case.num_kv_heads
+    per_block = 128 // case.group
+    tiles = sum(int(s[1]) * -(-int(s[4]) // per_block) for s in p1.segments) * case.num_kv_heads
     chunk = 16
-    while chunk > 4 and units / chunk < 2 * num_sms:
+    while chunk > 1 and tiles / chunk < 16 * num_sms:
         chunk //= 2
     return chunk
 
@@ -215,18 +217,19 @@ def run_gpu(args, rank, world):
     out_h = torch.empty_like(out, device="cpu").pin_memory()
     # shared-prefix plan (the scheduler's radix tree, recovered from the page tables)
     plan = None
-    G = case.num_q_heads // case.num_kv_heads
-    tails = args.tails == "on" or (args.tails == "auto" and G >= 8)
+    tails = args.tails != "off"
     if args.cascade != "off":
-        if args.chunk_tiles == 0:
-            args.chunk_tiles = auto_chunk_tiles(rlt, case, tails, torch.cuda.get_device_properties(dev).multi_processor_count)
-        plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, args.chunk_tiles, tails,
-                                   case.group)
-        if plan.num_segments == 0 or (args.cascade == "auto" and not tails and
-                                      plan.max_rest_len == case.max_seq_len):
-            plan = None
-        else:
-            plan.to(dev)
+        shared = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, 1, False, case.group)
+        if shared.num_segments > 0 or args.cascade == "on":
+            if args.chunk_tiles == 0:
+                args.chunk_tiles = auto_chunk_tiles(rlt, case, tails,
+                                                    torch.cuda.get_device_properties(dev).multi_processor_count)
+            plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, args.chunk_tiles, tails,
+                                       case.group)
+            if plan.num_segments == 0:
+                plan = None
+            else:
+                plan.to(dev)
     if plan is not None:
         ws_bytes = rlt.rlt_paged_decode_prefix_workspace_size(B, Hq, Hkv, D, plan.max_rest_len,
                                                               plan.max_prefix_slots, args.split_tokens)
@@ -258,7 +261,8 @@ def run_gpu(args, rank, world):
                 e0.record(st)
             if plan is not None:
                 rlt.rlt_paged_decode_attn_prefix(pool, bank, q[i], pt, sl, case.max_seq_len, plan, out=out[i],
-                                                 workspace=ws, split_tokens=args.split_tokens, stream=st)
+                                                 workspace=ws, split_tokens=args.split_tokens,
+                                                 max_ctas=args.prefix_ctas, stream=st)
             else:
                 rlt.rlt_paged_decode_attn(pool, bank, q[i], pt, sl, case.max_seq_len, out=out[i], workspace=ws,
                                           split_tokens=args.split_tokens, stream=st)
@@ -436,6 +440,7 @@ def config_dict(case, args):
             "unique_kv_tokens_per_layer_plane": case.unique_tokens(),
             "split_tokens": args.split_tokens or "auto",
             "cascade": args.cascade, "chunk_tiles": args.chunk_tiles, "tails": args.tails,
+            "prefix_ctas": args.prefix_ctas or "one per SM",
             "banks_run": args.banks or "all", "cuda_graph": args.graph,
             "l2": "inputs larger than L2: every bank's KV exceeds the 129 MB L2 and each is read once per step"}
 
@@ -472,12 +477,14 @@ def main():
     ap.add_argument("--cascade", default="auto", choices=["auto", "on", "off"],
                     help="read shared-prefix tiles once (tensor-core cascade) when the page tables share them")
     ap.add_argument("--chunk-tiles", type=int, default=0,
-                    help="128-token tiles per CTA of the tensor-core kernel (0 = from the plan's size)")
+                    help="128-token tiles per work item of the tensor-core kernel (0 = from the plan's size)")
     ap.add_argument("--tails", default="auto", choices=["auto", "on", "off"],
-                    help="also send each request's unshared tokens through the tensor-core kernel "
-                         "(auto: when a kv head serves >= 8 query heads)")
+                    help="with a shared prefix, also send each request's unshared tokens through the "
+                         "tensor-core kernel (auto = on); off leaves them to the split-K kernel")
     ap.add_argument("--graph", default="on", choices=["on", "off"],
                     help="submit each decode step as one captured CUDA graph (on) or as eager launches")
+    ap.add_argument("--prefix-ctas", type=int, default=0,
+                    help="CTAs of the persistent tensor-core kernel (0 = one per SM)")
     ap.add_argument("--banks", type=int, default=0,
                     help="run only the first N layer-plane banks (small-footprint case for profilers); 0 = all")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU time for cpu_baseline")

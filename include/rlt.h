@@ -226,7 +226,9 @@ RLT_API size_t rlt_paged_decode_prefix_workspace_size(int32_t batch, int32_t num
  * max_prefix_slots, max_rest_len are sizes[0], [6], [3], [5] of the plan,
  * which must have been built with this call's query group, and chunk_tiles
  * the value it was built with; max_rest_len == 0 (private tails) launches no
- * split-K kernel.  Other arguments as
+ * split-K kernel.  The tensor-core kernel is persistent: max_ctas CTAs (0 = one
+ * per SM; fewer leave SMs to other streams) share the num_kv_heads x
+ * work_units work items in contiguous runs.  Other arguments as
  * rlt_paged_decode_attn; the workspace (rlt_paged_decode_prefix_workspace_size
  * bytes) is required.  num_segments == 0 runs rlt_paged_decode_attn.
  * Supported: head_dim 128, num_q_heads/num_kv_heads in {1, 2, 4, 8}, page_size
@@ -238,7 +240,8 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     int32_t max_seq_len, const int32_t *segments, const int32_t *members,
     const int32_t *request_prefix, int32_t num_segments, int32_t work_units,
     int32_t max_prefix_slots, int32_t chunk_tiles, int32_t max_rest_len, float scale, void *out,
-    float *lse_out, void *workspace, size_t workspace_bytes, int32_t split_tokens, void *stream);
+    float *lse_out, void *workspace, size_t workspace_bytes, int32_t split_tokens, int32_t max_ctas,
+    void *stream);
 
 /* Size of the scratch array rlt_paged_decode_attn_noalloc uses (64 MiB). */
 #define RLT_NOALLOC_SCRATCH_BYTES (64u << 20)

@@ -87,7 +87,7 @@ def load():
         "rlt_plan_prefix": (ctypes.c_int, [P, i32, P, i32, i32, i32, i32, i32, P, i32, P, i32, P, P]),
         "rlt_paged_decode_prefix_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, i32]),
         "rlt_paged_decode_attn_prefix": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, P, i32, i32, P, P, P, i32,
-                                                        i32, i32, i32, i32, f32, P, P, P, sz, i32, P]),
+                                                        i32, i32, i32, i32, f32, P, P, P, sz, i32, i32, P]),
         "rlt_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     }
     for name, (res, args) in sigs.items():
@@ -370,7 +370,7 @@ def rlt_paged_decode_prefix_workspace_size(batch, num_q_heads, num_kv_heads, hea
 
 def rlt_paged_decode_attn_prefix(pool: KVPool, bank: int, q, page_table, seq_lens, max_seq_len: int,
                                  plan: PrefixPlan, out=None, lse_out=None, workspace=None, scale: float = 0.0,
-                                 split_tokens: int = 0, stream=None):
+                                 split_tokens: int = 0, max_ctas: int = 0, stream=None):
     """Paged decode attention reading shared-prefix tiles once (plan from rlt_plan_prefix, .to(device))."""
     import torch
     B, Hq, D = q.shape
@@ -395,6 +395,6 @@ def rlt_paged_decode_attn_prefix(pool: KVPool, bank: int, q, page_table, seq_len
         _dev(req, torch.int32, "request_prefix"), plan.num_segments, plan.work_units,
         plan.max_prefix_slots, plan.chunk_tiles, rest, float(scale),
         _dev(out, torch.bfloat16, "out"), lse_ptr, ctypes.c_void_p(workspace.data_ptr()),
-        workspace.numel() * workspace.element_size(), int(split_tokens), _stream(stream)),
+        workspace.numel() * workspace.element_size(), int(split_tokens), int(max_ctas), _stream(stream)),
         "rlt_paged_decode_attn_prefix")
     return out

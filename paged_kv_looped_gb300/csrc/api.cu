@@ -233,8 +233,11 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     int32_t max_seq_len, const int32_t *segments, const int32_t *members,
     const int32_t *request_prefix, int32_t num_segments, int32_t work_units,
     int32_t max_prefix_slots, int32_t chunk_tiles, int32_t max_rest_len, float scale, void *out,
-    float *lse_out, void *workspace, size_t workspace_bytes, int32_t split_tokens, void *stream)
+    float *lse_out, void *workspace, size_t workspace_bytes, int32_t split_tokens, int32_t max_ctas,
+    void *stream)
 {
+    if (max_ctas < 0)
+        return RLT_ERR_INVALID_ARG;
     if (num_segments == 0)      // nothing shared: the plain kernel computes the same thing
         return rlt_paged_decode_attn(pool, bank, q, num_q_heads, page_table, max_pages, seq_lens,
                                      batch, max_seq_len, scale, out, lse_out, workspace,
@@ -307,6 +310,8 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     pp.num_segments = num_segments;
     pp.chunk_tiles = chunk_tiles;
     pp.work_units = work_units;
+    pp.ctas = (int32_t)std::min<int64_t>(max_ctas > 0 ? std::min(max_ctas, sms) : sms,
+                                         (int64_t)pool->num_kv_heads * work_units);
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = rlt::launch_prefix(p, pp, p.k_bank, p.v_bank, bank_rows, cs);

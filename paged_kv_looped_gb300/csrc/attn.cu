@@ -421,9 +421,9 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
 }
 
 // Merge the partials of one (request, query head): its shared-prefix slots
-// [0, n_pre) and split-K slots [prefix_slots, prefix_slots + n).  Four warps per
-// pair take every fourth slot (lanes over the D dims, loads of two slots in
-// flight), then fold their (max, sum, vector) through shared memory.
+// [0, n_pre) and split-K slots [prefix_slots, prefix_slots + n); a slot whose
+// lse is -inf holds no partial and is skipped.  Four warps per pair (lanes over
+// the D dims), then their (max, sum, vector) fold through shared memory.
 constexpr int kCombineWarps = 4;
 
 template <int D>
@@ -488,15 +488,28 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
         }
     };
     if (M != -CUDART_INF_F) {
-        int s = warp;
-        for (; s + kCombineWarps < total; s += 2 * kCombineWarps) {
-            const int64_t s0 = slot_of(s), s1 = slot_of(s + kCombineWarps);
-            const float l0 = p.lse_part[s0], l1 = p.lse_part[s1];
-            add(s0, l0);
-            add(s1, l1);
+        // Warps take 32-slot blocks in turn: one coalesced read of the block's lse values,
+        // then only the slots that hold a partial (finite lse; a tensor-core run marks the
+        // chunk slots it merged with -inf) are read, two at a time.
+        for (int s0 = warp * 32; s0 < total; s0 += kCombineWarps * 32) {
+            const int s = s0 + lane;
+            const float l = s < total ? p.lse_part[slot_of(s)] : -CUDART_INF_F;
+            unsigned int live = __ballot_sync(kFullMask, l != -CUDART_INF_F);
+            while (live != 0u) {
+                const int k0 = __ffs(live) - 1;
+                live &= live - 1u;
+                const float l0 = __shfl_sync(kFullMask, l, k0);
+                if (live != 0u) {
+                    const int k1 = __ffs(live) - 1;
+                    live &= live - 1u;
+                    const float l1 = __shfl_sync(kFullMask, l, k1);
+                    add(slot_of(s0 + k0), l0);
+                    add(slot_of(s0 + k1), l1);
+                } else {
+                    add(slot_of(s0 + k0), l0);
+                }
+            }
         }
-        if (s < total)
-            add(slot_of(s), p.lse_part[slot_of(s)]);
     }
     if (lane == 0)
         red_l[warp] = ls;

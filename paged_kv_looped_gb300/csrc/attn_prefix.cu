@@ -11,9 +11,10 @@
 //     O = P V     (M = 128 query rows, N = D, K = 128 tokens)
 // on the 5th-generation tensor cores (tcgen05.mma, fp32 accumulators in TMEM),
 // with K and V tiles brought in by TMA tensor copies in 128-byte-swizzled
-// shared memory.  Each CTA writes one (o, log2-sum-exp) partial per query row;
-// the split-K kernel covers each request's remaining tokens and the combine
-// kernel merges everything.
+// shared memory.  Each run of work (below) writes one (o, log2-sum-exp)
+// partial per query row; with private tails every request's own tokens are
+// segments too, otherwise the split-K kernel covers them; the combine kernel
+// merges everything.
 #include <math_constants.h>
 
 #include <algorithm>
@@ -30,73 +31,94 @@
 namespace rlt {
 namespace {
 
-// Roles: warps 0-3 own query rows 0..127 (softmax, rescale, output; warp w may
-// only touch TMEM lanes 32w..32w+31), warp 4 issues the MMAs, warp 5 issues the
-// TMA copies.  Work goes in 64-token sub-tiles (half a planner tile).
-constexpr int kSoftWarps = 4;
-constexpr int kPThreads = (kSoftWarps + 3) * 32;
-// The MMA warp spins on its barriers: it shares a scheduler (warp id mod 4) with softmax warp 2,
-// which has live rows only for more than 64 query rows.
-constexpr int kLoadVWarp = kSoftWarps, kLoadKWarp = kSoftWarps + 1, kMmaWarp = kSoftWarps + 2;
-constexpr int kSub = 64;                    // tokens per sub-tile
-constexpr int kStagesP = 4;                 // K/V sub-tile ring depth
-constexpr int kHalfQ = 128 * 128;           // one 64-element column block of the 128 Q rows
-constexpr int kHalfKV = kSub * 128;         // one 64-dim column block of a sub-tile (64 rows x 128 B)
+// Persistent CTAs, one per SM.  The work is a list of items (kv head, segment,
+// member block, chunk of chunk_tiles 128-token tiles), kv-head-major; CTA c
+// takes the contiguous c-th share of it.  Consecutive items of one (kv head,
+// segment, member block) form a "run": one accumulation over their tokens and
+// one partial, so a CTA pays its start-up once and its pipeline never drains
+// between items.
+//
+// On this part a kind::f16 tcgen05.mma with M = 128 occupies the tensor pipe
+// about equally long for N = 64, 128 or 256, so every MMA here has N = 128:
+// S = Q K^T over a 128-token sub-tile (A = Q from TMEM), O += P V with N = D
+// (A = P from TMEM, written over the S it came from).  Shared memory holds
+// only the K and V rings.  Roles (8 warps):
+//   warps 0-7  softmax: warp w owns query rows 32(w%4)..+31 (the TMEM lanes it may
+//              touch) and the columns half w/4 of each sub-tile; the two warps of a
+//              row quarter swap row maxima and sums through shared memory.  They
+//              also write the next run's Q rows into TMEM.
+//   warp 8/9   TMA copies of V / K sub-tiles (128 tokens) into 4- / 2-slot rings
+//   warp 10    MMA issue: S into 2 TMEM S/P buffers, O += P V into the O buffer
+//   warp 11    scheduler: decodes the runs into a 4-deep ring of descriptors in
+//              shared memory, with the members' request ids
+constexpr int kSoftWarps = 8;
+constexpr int kLoadVWarp = 8, kLoadKWarp = 9, kMmaWarp = 10, kSchedWarp = 11;
+constexpr int kPThreads = 12 * 32;
+constexpr int kSub = 128;                   // tokens per sub-tile (= one planner tile)
+constexpr int kStagesK = 2, kStagesV = 4;   // ring depths (sub-tiles); a K slot frees sooner
+constexpr int kHalfKV = kSub * 128;         // one 64-dim column block of a sub-tile (128 rows x 128 B)
 constexpr int kKVBytes = 2 * kHalfKV;       // K (or V) of one sub-tile
-constexpr int kStageBytesP = 2 * kKVBytes;  // one K slot + one V slot
-constexpr int kPBytes = 128 * kSub * 2;     // P of one sub-tile: 128 rows x 64 tokens, bf16
+constexpr int kSBufs = 2;                   // S/P buffers in TMEM
+constexpr int kQBufs = 2;
+constexpr int kDescs = 4;                   // run descriptors published ahead
+constexpr int kDescConsumers = 4 + kSoftWarps;   // K and V producers, the MMA's two cursors, softmax warps
 constexpr int kMaxChunkTiles = 32;
-constexpr int kMaxBoxes = 2 * kMaxChunkTiles * 4;   // sub-tiles x boxes (page_size 16: 4 per sub-tile)
-constexpr int kQOff = 0;
-constexpr int kSBufs = 4;                   // S buffers in TMEM: S runs up to 4 sub-tiles ahead
-constexpr int kPBufs = 3;                   // P buffers in shared memory
-constexpr int kPOff = kQOff + 2 * kHalfQ;
-constexpr int kStageOff = kPOff + kPBufs * kPBytes;
-constexpr int kRowsOff = kStageOff + kStagesP * kStageBytesP;
-constexpr int kMemOff = kRowsOff + kMaxBoxes * 4;
-constexpr int kBarOff = kMemOff + 128 * 4;
-// K and V have rings of their own: a K slot is free once S has read it, a V slot once P.V has
-constexpr int kNumBars = 4 * kStagesP + 2 * kSBufs + kPBufs;   // K/V rings, s_full, p_full, o_full
-constexpr int kSmemP = kBarOff + kNumBars * 8 + 16 + 1024;
-constexpr uint32_t kTmemCols = 512;         // S[4] x 64 cols, O x 128 cols
-constexpr uint32_t kColS = 0, kColO = kSBufs * kSub;
+constexpr int kKOff = 0;
+constexpr int kVOff = kKOff + kStagesK * kKVBytes;
+constexpr int kBarOff = kVOff + kStagesV * kKVBytes;
+enum PrefixBar {
+    kBarFullK = 0,                          // K slot landed (TMA transaction count)
+    kBarFreeK = kBarFullK + kStagesK,       // K slot read by its S MMA
+    kBarFullV = kBarFreeK + kStagesK,
+    kBarFreeV = kBarFullV + kStagesV,       // V slot read by its P.V MMA
+    kBarSFull = kBarFreeV + kStagesV,       // S of the sub-tile in buffer i written
+    kBarPFull = kBarSFull + kSBufs,         // its P written over it by all 4 softmax warps
+    kBarPvDone = kBarPFull + kSBufs,        // its P.V complete
+    kBarQFull = kBarPvDone + kSBufs,        // Q buffer i written by all 4 softmax warps
+    kBarOFree = kBarQFull + kQBufs,         // O read out by all 4 softmax warps
+    kBarDescFull = kBarOFree + 1,           // descriptor i published
+    kBarDescFree = kBarDescFull + kDescs,   // descriptor i copied by every consumer
+    kBarPair = kBarDescFree + kDescs,       // the two softmax warps of row quarter i meet
+    kNumBars = kBarPair + 4
+};
+constexpr int kFlagOff = kBarOff + kNumBars * 8;   // TMEM base address, abort flag
+constexpr int kDescOff = (kFlagOff + 16 + 63) / 64 * 64;
+constexpr int kMemOff = kDescOff + kDescs * 64;    // request ids of each descriptor's members
+constexpr int kXMaxOff = kMemOff + kDescs * 128 * 2;   // row maxima [sub-tile parity][column half][row]
+constexpr int kXSumOff = kXMaxOff + 2 * 2 * 128 * 4;   // row sums [column half][row]
+constexpr int kSmemP = kXSumOff + 2 * 128 * 4 + 1024;
+// TMEM columns: Q[2] (128 rows x 128 bf16, two per column), S/P[2], O
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColQ = 0, kColS = kColQ + kQBufs * 64, kColO = kColS + kSBufs * kSub;
+static_assert(kColO + 128 == kTmemCols, "TMEM plan");
 // O accumulates in TMEM against a per-row reference max that moves only when
 // the row's running max exceeds it by more than this (log2 units): p <= 2^8.
 constexpr float kRescaleThreshold = 8.f;
 
-constexpr int kQBarrier = 1;                // named barrier: Q staged (softmax warps + MMA warp)
+static_assert(kSmemP <= 227 * 1024, "shared memory of one CTA");
+static_assert(kVOff % 1024 == 0, "swizzled operands");
 
-__device__ __forceinline__ void named_barrier_sync(int id, int threads)
+// One run: tokens [tok_begin, tok_end) of a segment for kv head g and n_mem of
+// its members; the partial goes to chunk slot `slot` of each member's (b, h)
+// (the nchunks - 1 following slots are marked empty).
+struct RunDesc {
+    int64_t tok_begin, tok_end;
+    int32_t g, nsub, page_row, n_mem, slot, nchunks;
+};
+static_assert(sizeof(RunDesc) <= 64, "descriptor slot");
+
+struct Run {
+    RunDesc d;
+    int32_t member_begin;
+    int next_item;
+};
+
+// The run that starts at work item `item` of a CTA whose items end at item_end.
+__device__ __forceinline__ Run decode_run(const PrefixParams &pp, int G, int item, int item_end)
 {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-__global__ void __launch_bounds__(kPThreads, 1)
-    decode_prefix_kernel(const __grid_constant__ CUtensorMap kmap,
-                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p,
-                         const PrefixParams pp)
-{
-    // the split-K kernel that follows may start on SMs this grid leaves idle
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *base =
-        reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    unsigned char *qs = base + kQOff;
-    unsigned char *pbuf = base + kPOff;
-    unsigned char *stages = base + kStageOff;
-    int32_t *box_rows = reinterpret_cast<int32_t *>(base + kRowsOff);
-    int32_t *mem = reinterpret_cast<int32_t *>(base + kMemOff);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(base + kBarOff);
-    uint64_t *full_k = bars, *free_k = bars + kStagesP, *full_v = bars + 2 * kStagesP,
-             *free_v = bars + 3 * kStagesP;
-    uint64_t *s_full = bars + 4 * kStagesP, *p_full = s_full + kSBufs, *o_full = p_full + kSBufs;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + kNumBars);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
-
-    // work unit -> (segment, chunk, member block) through the segments' work offsets
-    const int G = p.num_q_heads / p.num_kv_heads;
-    const int g = blockIdx.y;
-    const int unit = blockIdx.x;
+    Run r;
+    r.d.g = item / pp.work_units;
+    const int unit = item - r.d.g * pp.work_units;
     int lo = 0, hi = pp.num_segments - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -106,58 +128,136 @@ __global__ void __launch_bounds__(kPThreads, 1)
             hi = mid - 1;
     }
     const int32_t *sd = pp.segments + lo * kSegFields;
-    const int per_block = 128 / G;
-    const int mblocks = (sd[kSegMemberCount] + per_block - 1) / per_block;
-    const int local = unit - sd[kSegWorkBegin];
-    const int chunk = local / mblocks, mb = local % mblocks;
     const int num_tiles = sd[kSegNumTiles];
-    const int t0 = chunk * pp.chunk_tiles;
-    if (t0 >= num_tiles || local < 0)
-        return;
-    const int nt = min(pp.chunk_tiles, num_tiles - t0);
+    const int nchunks_seg = max(1, (num_tiles + pp.chunk_tiles - 1) / pp.chunk_tiles);
+    const int local = max(0, unit - sd[kSegWorkBegin]);
+    const int mb = local / nchunks_seg;
+    const int chunk0 = local - mb * nchunks_seg;
+    r.d.nchunks = min(nchunks_seg - chunk0, item_end - item);   // items of one member block
+    const int per_block = 128 / G;
     const int m0 = mb * per_block;
-    const int n_mem = min(per_block, sd[kSegMemberCount] - m0);
-    if (n_mem <= 0)
-        return;
-    const int R = n_mem * G;                    // live query rows of this CTA
-    const int page_row = sd[kSegPageRow];
-    const int first_tile = sd[kSegFirstTile] + t0;
-    // tokens [tok_begin, tok_end) of this CTA; a private tail segment ends mid-tile
-    const int64_t tok_begin = (int64_t)first_tile * kPrefixTile;
-    const int64_t tok_end = min((int64_t)(first_tile + nt) * kPrefixTile, (int64_t)sd[kSegEndToken]);
-    if (tok_end <= tok_begin)
-        return;
-    const int nsub = (int)((tok_end - tok_begin + kSub - 1) / kSub);   // 64-token sub-tiles
+    r.d.n_mem = min(per_block, sd[kSegMemberCount] - m0);
+    r.member_begin = sd[kSegMemberBegin] + m0;
+    r.d.page_row = sd[kSegPageRow];
+    r.d.slot = sd[kSegSlotBase] + chunk0;
+    const int t_first = sd[kSegFirstTile] + chunk0 * pp.chunk_tiles;
+    const int t_last = sd[kSegFirstTile] + min(num_tiles, (chunk0 + r.d.nchunks) * pp.chunk_tiles);
+    r.d.tok_begin = (int64_t)t_first * kPrefixTile;
+    r.d.tok_end = min((int64_t)t_last * kPrefixTile, (int64_t)sd[kSegEndToken]);
+    r.d.nsub = (r.d.n_mem > 0 && r.d.tok_end > r.d.tok_begin)
+                   ? (int)((r.d.tok_end - r.d.tok_begin + kSub - 1) / kSub) : 0;
+    r.next_item = item + max(1, r.d.nchunks);
+    return r;
+}
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int BR = p.page_size < kSub ? p.page_size : kSub;    // rows per TMA box
-    const int boxes = kSub / BR;                                // boxes per sub-tile
-
-    for (int i = tid; i < n_mem; i += kPThreads)
-        mem[i] = pp.members[sd[kSegMemberBegin] + m0 + i];
-    for (int i = tid; i < nsub * boxes; i += kPThreads) {
-        const int64_t tok = tok_begin + (int64_t)(i / boxes) * kSub + (i % boxes) * BR;
-        if (tok >= tok_end) {
-            box_rows[i] = -1;                    // past the request's last token: not loaded
-            continue;
-        }
-        const int64_t idx = tok / p.page_size;
-        int64_t page = idx < p.max_pages ? p.page_table[(int64_t)page_row * p.max_pages + idx] : -1;
-        if (page < 0 || page >= p.num_pages) {
-            record_error(p.err, RLT_DEVERR_BAD_PAGE);
-            page = 0;                            // stay in bounds; the result is flagged
-        }
-        box_rows[i] = (int32_t)((page * p.num_kv_heads + g) * p.page_size + tok % p.page_size);
+// The next run with work at or after *item; false when the CTA's items are done.
+__device__ __forceinline__ bool next_run(const PrefixParams &pp, int G, int &item, int item_end, Run &r)
+{
+    while (item < item_end) {
+        r = decode_run(pp, G, item, item_end);
+        item = r.next_item;
+        if (r.d.nsub > 0)
+            return true;
     }
+    return false;
+}
+
+// Warp-uniform bounded wait (every lane gets the same answer).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const volatile int *abort)
+{
+    return __all_sync(kFullMask, mbar_wait_or_abort(bar, parity, abort));
+}
+
+// Copy run descriptor r (and, for mrow >= 0, the request id of member mrow) and release
+// its slot.  Warp-collective; false if the wait gave up.
+__device__ __forceinline__ bool take_desc(uint64_t *bars, const unsigned char *base, int r, RunDesc &out,
+                                          int mrow, int &member, const volatile int *abort, int lane)
+{
+    if (!warp_wait(&bars[kBarDescFull + r % kDescs], (r / kDescs) & 1u, abort))
+        return false;
+    out = reinterpret_cast<const RunDesc *>(base + kDescOff)[r % kDescs];
+    if (mrow >= 0 && mrow < out.n_mem)
+        member = reinterpret_cast<const uint16_t *>(base + kMemOff)[(r % kDescs) * 128 + mrow];
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(&bars[kBarDescFree + r % kDescs]);
+    return true;
+}
+
+// Dims 64*half..64*half+63 of this thread's query row (member row / G, head row % G of
+// run d) into columns 32*half.. of the TMEM Q buffer at t_q, as packed bf16 pairs (the
+// A operand layout of S = Q K^T); rows past the run's members are zero.  Then the
+// warp's arrive on the buffer's barrier.
+__device__ __forceinline__ void stage_q(const DecodeParams &p, const RunDesc &d, int G, int row, int member,
+                                        int half, uint32_t t_q, uint64_t *bar, int lane)
+{
+    const bool live = row < d.n_mem * G;
+    const uint4 *src = reinterpret_cast<const uint4 *>(
+        p.q + ((int64_t)member * p.num_q_heads + d.g * G + row % G) * 128 + half * 64);
+    uint32_t w[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint4 v = live ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+        w[4 * i] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+    }
+    tc::tmem_st32u(t_q + half * 32, w);
+    tc::fence_before_sync();
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(bar);
+}
+
+// The two softmax warps of a row quarter meet (their k-th meeting; k counts from 0 in
+// both): shared-memory writes before it are visible to the other warp after it.
+// Bounded, like every wait here; false if it gave up.
+__device__ __forceinline__ bool pair_sync(uint64_t *bar, int &k, const volatile int *abort, int lane)
+{
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(bar);
+    return warp_wait(bar, (uint32_t)(k++) & 1u, abort);
+}
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    decode_prefix_kernel(const __grid_constant__ CUtensorMap kmap,
+                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p,
+                         const PrefixParams pp)
+{
+    // the split-K kernel that may follow starts as soon as SMs free up
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *base =
+        reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + kBarOff);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(base + kFlagOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + kFlagOff + 4);
+
+    const int G = p.num_q_heads / p.num_kv_heads;
+    const int64_t n_items = (int64_t)p.num_kv_heads * pp.work_units;
+    const int item_begin = (int)((int64_t)blockIdx.x * n_items / gridDim.x);
+    const int item_end = (int)((int64_t)(blockIdx.x + 1) * n_items / gridDim.x);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
     if (tid == 0) {
-        for (int i = 0; i < 4 * kStagesP; ++i)
+        for (int i = 0; i < kBarSFull; ++i)
             mbar_init(&bars[i], 1);
         for (int i = 0; i < kSBufs; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], (R + 31) / 32);   // one arrive per softmax warp with live rows
+            mbar_init(&bars[kBarSFull + i], 1);
+            mbar_init(&bars[kBarPFull + i], kSoftWarps);
+            mbar_init(&bars[kBarPvDone + i], 1);
         }
-        for (int i = 0; i < kPBufs; ++i)
-            mbar_init(&o_full[i], 1);
+        for (int i = 0; i < kQBufs; ++i)
+            mbar_init(&bars[kBarQFull + i], kSoftWarps);
+        mbar_init(&bars[kBarOFree], kSoftWarps);
+        for (int i = 0; i < kDescs; ++i) {
+            mbar_init(&bars[kBarDescFull + i], 1);
+            mbar_init(&bars[kBarDescFree + i], kDescConsumers);
+        }
+        for (int i = 0; i < 4; ++i)
+            mbar_init(&bars[kBarPair + i], 2);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -168,104 +268,196 @@ __global__ void __launch_bounds__(kPThreads, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
     bool ok = true;
+    int unused = 0;
 
-    if (warp < kSoftWarps) {
-        // Query rows r = member * G + head, K-major, 128-byte swizzled (rows >= R unused),
-        // staged while the producers already stream K and V.
-        for (int i = tid; i < R * 16; i += kSoftWarps * 32) {
-            const int r = i >> 4, c16 = i & 15;
-            const int b = mem[r / G], h = r % G;
-            const uint4 v = *reinterpret_cast<const uint4 *>(
-                p.q + ((int64_t)b * p.num_q_heads + g * G + h) * 128 + c16 * 8);
-            *reinterpret_cast<uint4 *>(qs + (c16 >> 3) * kHalfQ + tc::sw128_offset(r, (c16 & 7) * 8)) = v;
+    if (warp == kSchedWarp) {
+        // ---------------------------------------------------------- scheduler
+        // Publishes descriptor d once every consumer has copied descriptor d - kDescs.
+        RunDesc *descs = reinterpret_cast<RunDesc *>(base + kDescOff);
+        uint16_t *dmem = reinterpret_cast<uint16_t *>(base + kMemOff);
+        int item = item_begin;
+        for (int d = 0;; ++d) {
+            if (d >= kDescs &&
+                !(ok = warp_wait(&bars[kBarDescFree + d % kDescs], ((d - kDescs) / kDescs) & 1u, abort_flag)))
+                break;
+            Run r;
+            const bool has = next_run(pp, G, item, item_end, r);
+            if (!has)
+                r.d.nsub = 0;                    // the terminal descriptor
+            if (lane == 0)
+                descs[d % kDescs] = r.d;
+            for (int i = lane; has && i < r.d.n_mem; i += 32) {
+                int b = pp.members[r.member_begin + i];
+                if (b < 0 || b >= p.batch) {
+                    record_error(p.err, RLT_DEVERR_BAD_SLOT);
+                    b = 0;
+                }
+                dmem[(d % kDescs) * 128 + i] = (uint16_t)b;
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars[kBarDescFull + d % kDescs]);
+            if (!has)
+                break;
         }
-        fence_proxy_async();
-        named_barrier_sync(kQBarrier, (kSoftWarps + 1) * 32);
-    }
-
-    if (warp == kLoadKWarp || warp == kLoadVWarp) {
+        if (!ok)
+            *abort_flag = 1;
+    } else if (warp == kLoadKWarp || warp == kLoadVWarp) {
         // ------------------------------------------------- TMA producers (K, V)
-        // Lane j copies box j/2, column block j&1 of this warp's tensor.
+        // Lane j copies box j/2, column block j&1 of each sub-tile of this warp's tensor.
+        // The page-table read for the next sub-tile (of this run or the next) is
+        // issued before the wait for the current sub-tile's slot.
         const bool is_v = warp == kLoadVWarp;
+        const int stages = is_v ? kStagesV : kStagesK;
         const CUtensorMap *map = is_v ? &vmap : &kmap;
-        uint64_t *fullx = is_v ? full_v : full_k, *freex = is_v ? free_v : free_k;
-        unsigned char *ring = stages + (is_v ? kStagesP * kKVBytes : 0);
+        uint64_t *fullx = bars + (is_v ? kBarFullV : kBarFullK);
+        uint64_t *freex = bars + (is_v ? kBarFreeV : kBarFreeK);
+        unsigned char *ring = base + (is_v ? kVOff : kKOff);
         if (lane == 0)
             tc::prefetch_tmap(map);
-        int j = 0;
-        for (; j < nsub && ok; ++j) {
-            const int st = j % kStagesP;
-            if (j >= kStagesP)
-                ok = mbar_wait_or_abort(&freex[st], ((j / kStagesP) - 1) & 1u, abort_flag);
-            if (!ok)
+        const int BR = p.page_size < kSub ? p.page_size : kSub;   // rows per TMA box
+        const int boxes = kSub / BR;
+        // pool row of this lane's box in sub-tile j of run d (-1: no box)
+        auto lane_row = [&](const RunDesc &d, int j) -> int {
+            if (lane >= 2 * boxes)
+                return -1;
+            const int64_t tok = d.tok_begin + (int64_t)j * kSub + (lane >> 1) * BR;
+            if (tok >= d.tok_end)
+                return -1;
+            const int64_t idx = tok / p.page_size;
+            int64_t page = -1;
+            if (d.page_row >= 0 && d.page_row < p.batch && idx < p.max_pages)
+                page = p.page_table[(int64_t)d.page_row * p.max_pages + idx];
+            if (page < 0 || page >= p.num_pages) {
+                record_error(p.err, RLT_DEVERR_BAD_PAGE);
+                page = 0;                        // stay in bounds; the result is flagged
+            }
+            return (int)((page * p.num_kv_heads + d.g) * p.page_size + tok % p.page_size);
+        };
+        int n = 0, r = 0, j = 0;                 // sub-tiles issued; current run and sub-tile
+        RunDesc cur;
+        ok = take_desc(bars, base, r, cur, -1, unused, abort_flag, lane);
+        int row_next = ok && cur.nsub > 0 ? lane_row(cur, 0) : -1;
+        while (ok && cur.nsub > 0) {
+            const int row = row_next;
+            const int64_t sub_begin = cur.tok_begin + (int64_t)j * kSub, tok_end = cur.tok_end;
+            if (j + 1 < cur.nsub) {
+                row_next = lane_row(cur, ++j);
+            } else {
+                j = 0;
+                if (!(ok = take_desc(bars, base, ++r, cur, -1, unused, abort_flag, lane)))
+                    break;
+                if (cur.nsub > 0)
+                    row_next = lane_row(cur, 0);
+            }
+            const int st = n % stages;
+            if (n >= stages && !(ok = warp_wait(&freex[st], ((n / stages) - 1) & 1u, abort_flag)))
                 break;
-            const int64_t sub_begin = tok_begin + (int64_t)j * kSub;
             const int nbox = (int)min((int64_t)boxes, (tok_end - sub_begin + BR - 1) / BR);
             if (lane == 0)
                 mbar_arrive_expect_tx(&fullx[st], (uint32_t)(nbox * BR * 128 * 2));
             __syncwarp();
-            if (lane < 2 * nbox) {
-                const int box = lane >> 1, half = lane & 1;
-                tc::tma_load_2d(ring + st * kKVBytes + half * kHalfKV + box * BR * 128, map, half * 64,
-                                box_rows[j * boxes + box], &fullx[st]);
-            }
+            if (lane < 2 * nbox)
+                tc::tma_load_2d(ring + st * kKVBytes + (lane & 1) * kHalfKV + (lane >> 1) * BR * 128, map,
+                                (lane & 1) * 64, row, &fullx[st]);
+            ++n;
         }
         if (!ok) {
             *abort_flag = 1;
-            // copies of the last (up to 4) sub-tiles may still be landing: wait for them (bounded)
+            // copies of the last sub-tiles may still be landing: wait for them (bounded)
             if (lane == 0)
-                for (int k = max(0, j - kStagesP); k < j; ++k)
-                    mbar_wait(&fullx[k % kStagesP], (k / kStagesP) & 1u);
+                for (int k = max(0, n - stages); k < n; ++k)
+                    mbar_wait(&fullx[k % stages], (k / stages) & 1u);
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------- MMA issuer
-        const uint32_t id_s = tc::instr_desc_bf16(128, kSub, false);
-        const uint32_t id_o = tc::instr_desc_bf16(128, 128, true);
-        const uint32_t qa = smem_u32(qs), pa = smem_u32(pbuf), sa = smem_u32(stages);
-        named_barrier_sync(kQBarrier, (kSoftWarps + 1) * 32);   // Q staged
-        // Event loop: issue S_k as soon as K_k has landed and S buffer k%4 is free
-        // (P.V of k-4 issued), and P.V_j as soon as every softmax warp wrote P_j
-        // and V_j has landed.  Probes do not block, so neither waits on the other.
-        int s_next = 0, pv_next = 0;
+        // Event loop over two cursors on the run sequence: S of sub-tile n as soon as
+        // K_n has landed, S/P buffer n%2 is free (P.V of n-2 issued; tcgen05 MMAs run
+        // in issue order, so S cannot overwrite P before that P.V has read it) and, at
+        // a run's start, its Q is written; P.V of sub-tile n as soon as every softmax
+        // warp wrote P_n and V_n has landed (and, at a run's start, O was read out).
+        // Probes do not block, so neither cursor waits on the other.
+        const uint32_t id = tc::instr_desc_bf16(128, 128, false);      // S: B = K, K-major
+        const uint32_t id_o = tc::instr_desc_bf16(128, 128, true);     // O: B = V, MN-major
+        const uint32_t ka = smem_u32(base + kKOff), va = smem_u32(base + kVOff);
+        const RunDesc *descs = reinterpret_cast<const RunDesc *>(base + kDescOff);
+        RunDesc sd{}, pd{};
+        bool s_have = false, p_have = false, s_done = false, p_done = false;
+        int s_r = 0, p_r = 0, s_j = 0, p_j = 0, s_n = 0, p_n = 0;
         uint64_t t_idle = 0;
-        while (pv_next < nsub) {
+        // take the next descriptor for a cursor if it is published (non-blocking)
+        auto try_take = [&](int r, RunDesc &out, bool &have, bool &done) -> bool {
+            if (!__all_sync(kFullMask, mbar_test_wait(&bars[kBarDescFull + r % kDescs], (r / kDescs) & 1u)))
+                return false;
+            out = descs[r % kDescs];
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars[kBarDescFree + r % kDescs]);
+            if (out.nsub > 0)
+                have = true;
+            else
+                done = true;
+            return true;
+        };
+        while (!p_done) {
             bool progress = false;
-            if (s_next < nsub && s_next < pv_next + kSBufs &&
-                __all_sync(kFullMask, mbar_test_wait(&full_k[s_next % kStagesP], (s_next / kStagesP) & 1u))) {
-                tc::fence_after_sync();
-                if (lane == 0) {
-                    const uint32_t ka = sa + (s_next % kStagesP) * kKVBytes;
+            if (!s_done && !s_have)
+                progress |= try_take(s_r, sd, s_have, s_done);
+            if (s_have && s_n < p_n + kSBufs) {
+                bool ready = mbar_test_wait(&bars[kBarFullK + s_n % kStagesK], (s_n / kStagesK) & 1u);
+                if (s_j == 0)
+                    ready = ready && mbar_test_wait(&bars[kBarQFull + s_r % kQBufs], (s_r / kQBufs) & 1u);
+                if (__all_sync(kFullMask, ready)) {
+                    tc::fence_after_sync();
+                    if (lane == 0) {
+                        const uint32_t qt = tmem + kColQ + (s_r % kQBufs) * 64;
+                        const uint32_t kb = ka + (s_n % kStagesK) * kKVBytes;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_bf16(tmem + kColS + (s_next % kSBufs) * kSub,
-                                     tc::smem_desc(qa + (kk >> 2) * kHalfQ + (kk & 3) * 32, 16, 1024),
-                                     tc::smem_desc(ka + (kk >> 2) * kHalfKV + (kk & 3) * 32, 16, 1024), id_s,
-                                     kk > 0);
-                    tc::mma_commit(&s_full[s_next % kSBufs]);
-                    tc::mma_commit(&free_k[s_next % kStagesP]);
+                        for (int kk = 0; kk < 8; ++kk)
+                            tc::mma_bf16_ta(tmem + kColS + (s_n % kSBufs) * kSub, qt + kk * 8,
+                                            tc::smem_desc(kb + (kk >> 2) * kHalfKV + (kk & 3) * 32, 16, 1024), id,
+                                            kk > 0);
+                        tc::mma_commit(&bars[kBarSFull + s_n % kSBufs]);
+                        tc::mma_commit(&bars[kBarFreeK + s_n % kStagesK]);
+                    }
+                    __syncwarp();
+                    ++s_n;
+                    if (++s_j == sd.nsub) {
+                        s_j = 0;
+                        s_have = false;
+                        ++s_r;
+                    }
+                    progress = true;
                 }
-                __syncwarp();
-                ++s_next;
-                progress = true;
             }
-            const int j = pv_next;
-            if (j < s_next &&
-                __all_sync(kFullMask, mbar_test_wait(&p_full[j % kSBufs], (j / kSBufs) & 1u) &&
-                                          mbar_test_wait(&full_v[j % kStagesP], (j / kStagesP) & 1u))) {
-                tc::fence_after_sync();
-                if (lane == 0) {
-                    const uint32_t va = sa + (kStagesP + j % kStagesP) * kKVBytes;
-                    const uint32_t pj = pa + (j % kPBufs) * kPBytes;
+            if (!p_done && !p_have)
+                progress |= try_take(p_r, pd, p_have, p_done);
+            if (p_have && p_n < s_n) {
+                bool ready = mbar_test_wait(&bars[kBarPFull + p_n % kSBufs], (p_n / kSBufs) & 1u) &&
+                             mbar_test_wait(&bars[kBarFullV + p_n % kStagesV], (p_n / kStagesV) & 1u);
+                if (p_j == 0 && p_r >= 1)
+                    ready = ready && mbar_test_wait(&bars[kBarOFree], (p_r - 1) & 1u);
+                if (__all_sync(kFullMask, ready)) {
+                    tc::fence_after_sync();
+                    if (lane == 0) {
+                        const uint32_t pt = tmem + kColS + (p_n % kSBufs) * kSub;
+                        const uint32_t vb = va + (p_n % kStagesV) * kKVBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kSub / 16; ++kk)
-                        tc::mma_bf16(tmem + kColO, tc::smem_desc(pj + kk * 32, 16, 1024),
-                                     tc::smem_desc(va + kk * 2048, kHalfKV, 1024), id_o, (j > 0) || (kk > 0));
-                    tc::mma_commit(&o_full[j % kPBufs]);
-                    tc::mma_commit(&free_v[j % kStagesP]);
+                        for (int kk = 0; kk < kSub / 16; ++kk)
+                            tc::mma_bf16_ta(tmem + kColO, pt + kk * 8, tc::smem_desc(vb + kk * 2048, kHalfKV, 1024),
+                                            id_o, (p_j > 0) || (kk > 0));
+                        tc::mma_commit(&bars[kBarPvDone + p_n % kSBufs]);
+                        tc::mma_commit(&bars[kBarFreeV + p_n % kStagesV]);
+                    }
+                    __syncwarp();
+                    ++p_n;
+                    if (++p_j == pd.nsub) {
+                        p_j = 0;
+                        p_have = false;
+                        ++p_r;
+                    }
+                    progress = true;
                 }
-                __syncwarp();
-                ++pv_next;
-                progress = true;
             }
             if (progress) {
                 t_idle = 0;
@@ -274,137 +466,166 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const uint64_t now = global_ns();
                 if (t_idle == 0)
                     t_idle = now;
-                else if (now - t_idle > kWaitLimitNs || *abort_flag != 0) {
+                else if (__any_sync(kFullMask, now - t_idle > kWaitLimitNs || *abort_flag != 0)) {
                     ok = false;
                     break;
                 }
             }
         }
-        if (!ok) {
+        // every issued MMA must be complete before the CTA gives up its memory: the last
+        // P.V commit covers all earlier MMAs (bounded wait; on the normal path it has arrived)
+        if (lane == 0 && p_n > 0)
+            mbar_wait(&bars[kBarPvDone + (p_n - 1) % kSBufs], ((p_n - 1) / kSBufs) & 1u);
+        if (lane == 0 && s_n > p_n)
+            mbar_wait(&bars[kBarSFull + (s_n - 1) % kSBufs], ((s_n - 1) / kSBufs) & 1u);
+        __syncwarp();
+        if (!ok)
             *abort_flag = 1;
-            // let issued MMAs finish before the CTA gives up its shared memory (bounded)
-            if (lane == 0 && pv_next > 0)
-                mbar_wait(&o_full[(pv_next - 1) % kPBufs], ((pv_next - 1) / kPBufs) & 1u);
-        }
-    } else if (warp * 32 < R) {
-        // ------------------------------------------- softmax warps with live rows
-        const int row = warp * 32 + lane;
-        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
-        float m_ref = -CUDART_INF_F, l_run = 0.f;
-
-        for (int j = 0; j < nsub && ok; ++j) {
-            ok = mbar_wait_or_abort(&s_full[j % kSBufs], (j / kSBufs) & 1u, abort_flag);
+    } else {
+        // ------------------------------------------------------------- softmax
+        const int quarter = warp & 3, half = warp >> 2;
+        const int row = quarter * 32 + lane;
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        float *xmax = reinterpret_cast<float *>(base + kXMaxOff);
+        float *xsum = reinterpret_cast<float *>(base + kXSumOff);
+        uint64_t *pair = &bars[kBarPair + quarter];
+        int n = 0, meets = 0;
+        RunDesc rd, rn;
+        int b_row = 0, b_next = 0;
+        // run 0's Q; each later run's Q is written while the run before it computes
+        ok = take_desc(bars, base, 0, rd, row / G, b_row, abort_flag, lane);
+        if (ok && rd.nsub > 0)
+            stage_q(p, rd, G, row, b_row, half, t_lane + kColQ, &bars[kBarQFull], lane);
+        for (int r = 0; ok && rd.nsub > 0; ++r) {
+            const int R = rd.n_mem * G;
+            const bool live = quarter * 32 < R;  // uniform over the quarter's two warps; quarter 0 is live
+            float m_ref = -CUDART_INF_F, l_run = 0.f;   // l_run: this warp's columns only
+            for (int j = 0; j < rd.nsub; ++j, ++n) {
+                if (!(ok = warp_wait(&bars[kBarSFull + n % kSBufs], (n / kSBufs) & 1u, abort_flag)))
+                    break;
+                const uint32_t t_s = t_lane + kColS + (n % kSBufs) * kSub;
+                if (live) {
+                    tc::fence_after_sync();
+                    const int valid = (int)min((int64_t)kSub, rd.tok_end - (rd.tok_begin + (int64_t)j * kSub)) -
+                                      half * 64;       // valid columns of this warp's half
+                    if (valid + half * 64 < kSub && warp == 0) {
+                        // ragged end of a private tail: zero the V rows past it, whose memory may
+                        // hold anything (0 * NaN would poison O), once this V copy has landed
+                        if (!(ok = warp_wait(&bars[kBarFullV + n % kStagesV], (n / kStagesV) & 1u, abort_flag)))
+                            break;
+                        const int vr = valid;           // warp 0: half 0, so valid counts from token 0
+                        unsigned char *vst = base + kVOff + (n % kStagesV) * kKVBytes;
+                        for (int c = lane; c < (kSub - vr) * 16; c += 32) {
+                            const int rr = vr + c / 16, c16 = c % 16;
+                            *reinterpret_cast<uint4 *>(vst + (c16 >> 3) * kHalfKV + rr * 128 + (c16 & 7) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async();     // zeroed rows (generic) -> P.V MMA (async proxy)
+                    }
+                    float v[64];
+                    tc::tmem_ld64(t_s + half * 64, v);
+                    float mx = -CUDART_INF_F;
+#pragma unroll
+                    for (int i = 0; i < 64; ++i)
+                        if (i < valid)
+                            mx = fmaxf(mx, v[i]);
+                    // the row max over both halves of the sub-tile
+                    xmax[((n & 1) * 2 + half) * 128 + row] = mx;
+                    if (!(ok = pair_sync(pair, meets, abort_flag, lane)))
+                        break;
+                    mx = fmaxf(mx, xmax[((n & 1) * 2 + (half ^ 1)) * 128 + row]) * p.qscale;
+                    const bool up = mx > m_ref + kRescaleThreshold;
+                    const float m_next = up ? mx : m_ref;   // rows >= R hold garbage and are never stored
+                    const float scale_o = exp2f(m_ref - m_next);   // 1 if the reference stays, 0 at first
+                    if (__any_sync(kFullMask, up) && j > 0) {
+                        // rescale this warp's half of the row's O (P.V of the previous sub-tile landed)
+                        if (!(ok = warp_wait(&bars[kBarPvDone + (n - 1) % kSBufs], ((n - 1) / kSBufs) & 1u,
+                                             abort_flag)))
+                            break;
+                        tc::fence_after_sync();
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            float o[32];
+                            tc::tmem_ld32(t_lane + kColO + half * 64 + c * 32, o);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                o[i] *= scale_o;
+                            tc::tmem_st32(t_lane + kColO + half * 64 + c * 32, o);
+                        }
+                    }
+                    l_run *= scale_o;
+                    m_ref = m_next;
+                    // P = 2^(s - m) as bf16 pairs over columns this quarter pair has read
+                    float lsum = 0.f;
+                    uint32_t w[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float p0 = 2 * i < valid ? fast_exp2(fmaf(v[2 * i], p.qscale, -m_ref)) : 0.f;
+                        const float p1 = 2 * i + 1 < valid ? fast_exp2(fmaf(v[2 * i + 1], p.qscale, -m_ref)) : 0.f;
+                        lsum += p0 + p1;
+                        w[i] = cvt_bf16x2(p0, p1);
+                    }
+                    tc::tmem_st32u(t_s + half * 32, w);
+                    l_run += lsum;
+                    tc::fence_before_sync();
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars[kBarPFull + n % kSBufs]);
+                if (j == 0) {
+                    // the S MMAs of the previous run are complete, so its Q buffer takes the
+                    // next run's Q now
+                    if (!(ok = take_desc(bars, base, r + 1, rn, row / G, b_next, abort_flag, lane)))
+                        break;
+                    if (rn.nsub > 0)
+                        stage_q(p, rn, G, row, b_next, half, t_lane + kColQ + ((r + 1) % kQBufs) * 64,
+                                &bars[kBarQFull + (r + 1) % kQBufs], lane);
+                }
+            }
             if (!ok)
                 break;
+            // run epilogue: O / l -> the run's partial slot; O is free afterwards
+            if (!(ok = warp_wait(&bars[kBarPvDone + (n - 1) % kSBufs], ((n - 1) / kSBufs) & 1u, abort_flag)))
+                break;
             tc::fence_after_sync();
-            float v[64];
-            tc::tmem_ld64(t_lane + kColS + (j % kSBufs) * kSub, v);
-            const int valid = (int)min((int64_t)kSub, tok_end - (tok_begin + (int64_t)j * kSub));
-            if (valid < kSub) {
-                // ragged end of a private tail: mask the missing tokens, and zero their V
-                // rows, whose memory may hold anything (0 * NaN would poison O)
+            const int64_t slot =
+                ((int64_t)b_row * p.num_q_heads + rd.g * G + row % G) * p.part_stride + rd.slot;
+            float l_tot = l_run;
+            if (live) {
+                xsum[half * 128 + row] = l_run;
+                if (!(ok = pair_sync(pair, meets, abort_flag, lane)))
+                    break;
+                l_tot = l_run + xsum[(half ^ 1) * 128 + row];
+                const float inv = 1.f / l_tot;
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    v[i] = i < valid ? v[i] : -CUDART_INF_F;
-                if (warp == 0) {
-                    // after this sub-tile's V copy has landed (it may write garbage rows too)
-                    ok = __all_sync(kFullMask, mbar_wait_or_abort(&full_v[j % kStagesP], (j / kStagesP) & 1u,
-                                                                  abort_flag));
-                    if (!ok)
-                        break;
-                    unsigned char *vst = stages + (kStagesP + j % kStagesP) * kKVBytes;
-                    for (int c = lane; c < (kSub - valid) * 16; c += 32) {
-                        const int r = valid + c / 16, c16 = c % 16;
-                        *reinterpret_cast<uint4 *>(vst + (c16 >> 3) * kHalfKV + r * 128 + (c16 & 7) * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
+                for (int c = 0; c < 2; ++c) {
+                    float o[32];
+                    tc::tmem_ld32(t_lane + kColO + half * 64 + c * 32, o);
+                    if (row < R) {
+                        float4 *dst = reinterpret_cast<float4 *>(p.o_part + slot * 128 + half * 64 + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                                 o[4 * i + 3] * inv);
                     }
                 }
             }
-            float mx = -CUDART_INF_F;
-#pragma unroll
-            for (int i = 0; i < 64; ++i)
-                mx = fmaxf(mx, v[i]);
-            mx *= p.qscale;
-            const bool up = mx > m_ref + kRescaleThreshold;
-            const float m_next = up ? mx : m_ref;   // rows >= R hold garbage and are never stored
-            const float scale_o = exp2f(m_ref - m_next);   // 1 if the reference stays, 0 at first
-            if (__any_sync(kFullMask, up) && j > 0) {
-                // rescale this row's O (PV of sub-tile j-1 must have landed)
-                ok = mbar_wait_or_abort(&o_full[(j - 1) % kPBufs], ((j - 1) / kPBufs) & 1u, abort_flag);
-                if (!__all_sync(kFullMask, ok)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float o[32];
-                    tc::tmem_ld32(t_lane + kColO + c * 32, o);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        o[i] *= scale_o;
-                    tc::tmem_st32(t_lane + kColO + c * 32, o);
-                }
-            }
-            l_run *= scale_o;
-            m_ref = m_next;
-            float lsum = 0.f;
-            uint32_t w[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float p0 = fast_exp2(fmaf(v[2 * i], p.qscale, -m_ref));
-                const float p1 = fast_exp2(fmaf(v[2 * i + 1], p.qscale, -m_ref));
-                lsum += p0 + p1;
-                w[i] = cvt_bf16x2(p0, p1);
-            }
-            l_run += lsum;
-            if (j >= kPBufs) {   // P[j%3] was read by the P.V of sub-tile j-3
-                ok = mbar_wait_or_abort(&o_full[j % kPBufs], ((j - kPBufs) / kPBufs) & 1u, abort_flag);
-                if (!__all_sync(kFullMask, ok)) {
-                    ok = false;
-                    break;
-                }
-            }
-            if (row < R) {
-                unsigned char *pj = pbuf + (j % kPBufs) * kPBytes;
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8)
-                    *reinterpret_cast<uint4 *>(pj + tc::sw128_offset(row, c8 * 8)) =
-                        make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
-            }
-            fence_proxy_async();                // P (generic writes) -> MMA (async proxy)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&p_full[j % kSBufs]);
-        }
-        if (ok) {
-            ok = mbar_wait_or_abort(&o_full[(nsub - 1) % kPBufs], ((nsub - 1) / kPBufs) & 1u, abort_flag);
-            ok = __all_sync(kFullMask, ok);
+                mbar_arrive(&bars[kBarOFree]);
+            if (live && half == 0 && row < R) {
+                p.lse_part[slot] = m_ref + log2f(l_tot);
+                for (int k = 1; k < rd.nchunks; ++k)   // chunks merged into this run's partial
+                    p.lse_part[slot + k] = -CUDART_INF_F;
+            }
+            if (live && !(ok = pair_sync(pair, meets, abort_flag, lane)))   // xsum read by both before
+                break;                                                       // the next run writes it
+            rd = rn;
+            b_row = b_next;
         }
         if (!ok)
             *abort_flag = 1;
-        if (__all_sync(kFullMask, ok && *abort_flag == 0)) {   // warp-uniform: TMEM loads below
-            tc::fence_after_sync();
-            const int b = row < R ? mem[row / G] : 0, h = row % G;
-            const int64_t slot = ((int64_t)b * p.num_q_heads + g * G + h) * p.part_stride +
-                                 sd[kSegSlotBase] + chunk;
-            const float inv = 1.f / l_run;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float o[32];
-                tc::tmem_ld32(t_lane + kColO + c * 32, o);
-                if (row < R) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.o_part + slot * 128 + c * 32);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
-                                             o[4 * i + 3] * inv);
-                }
-            }
-            if (row < R)
-                p.lse_part[slot] = m_ref + log2f(l_run);
-        }
     }
 
     tc::fence_before_sync();
@@ -485,8 +706,9 @@ cudaError_t launch_prefix(const DecodeParams &p, const PrefixParams &pp, const v
             return e;
         configured.fetch_or(bit);
     }
-    const dim3 grid(pp.work_units, p.num_kv_heads, 1);
-    decode_prefix_kernel<<<grid, kPThreads, kSmemP, stream>>>(kmap, vmap, p, pp);
+    if (pp.ctas < 1)
+        return cudaErrorInvalidValue;
+    decode_prefix_kernel<<<pp.ctas, kPThreads, kSmemP, stream>>>(kmap, vmap, p, pp);
     return cudaGetLastError();
 }
 

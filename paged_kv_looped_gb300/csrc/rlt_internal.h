@@ -49,7 +49,8 @@ struct PrefixParams {
     const int32_t *members;      // request ids, grouped by segment
     int32_t num_segments;
     int32_t chunk_tiles;         // 128-token tiles per CTA
-    int32_t work_units;          // (segment, chunk, member block) items: the grid's x extent
+    int32_t work_units;          // (segment, member block, chunk) units per kv head
+    int32_t ctas;                // persistent CTAs sharing the num_kv_heads x work_units items
 };
 
 bool prefix_supported(int head_dim, int group, int page_size);

@@ -18,7 +18,7 @@ from helpers import attn_close, bf16_dev, bits_host, i32_dev
 pytestmark = pytest.mark.gpu
 
 
-def run_both(case, h, device, chunk_tiles=4, split_tokens=0, private_tails=False):
+def run_both(case, h, device, chunk_tiles=4, split_tokens=0, private_tails=False, max_ctas=0):
     pool = rlt.KVPool(bf16_dev(h.k_pool, device)[None].contiguous(), bf16_dev(h.v_pool, device)[None].contiguous())
     q = bf16_dev(h.q, device)
     pt = i32_dev(case.page_table, device)
@@ -27,7 +27,7 @@ def run_both(case, h, device, chunk_tiles=4, split_tokens=0, private_tails=False
                                private_tails, case.group).to(device)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=device)
     out = rlt.rlt_paged_decode_attn_prefix(pool, 0, q, pt, sl, case.max_seq_len, plan, lse_out=lse,
-                                           split_tokens=split_tokens)
+                                           split_tokens=split_tokens, max_ctas=max_ctas)
     lse_p = torch.empty_like(lse)
     plain = rlt.rlt_paged_decode_attn(pool, 0, q, pt, sl, case.max_seq_len, lse_out=lse_p)
     assert rlt.rlt_get_device_error() == 0
@@ -164,3 +164,26 @@ def test_private_tails_with_empty_and_nan_padding(cuda_device):
     assert np.all(got[0] == 0) and np.all(got[4] == 0)
     assert np.all(np.isfinite(got))
     check(got[[1, 2, 3, 5]], ref[[1, 2, 3, 5]], lse[[1, 2, 3, 5]], ref_lse[[1, 2, 3, 5]])
+
+
+@pytest.mark.parametrize("max_ctas", [1, 2, 7])
+@pytest.mark.parametrize("tails,chunk_tiles", [(False, 1), (True, 1), (True, 3)])
+def test_persistent_ctas_with_many_runs(cuda_device, max_ctas, tails, chunk_tiles):
+    # few CTAs: each walks many runs (kv heads, segments, member blocks, merged chunks) through one
+    # pipeline, reusing its Q, O, S, P buffers and K/V rings across runs
+    lens = [2900, 3100, 1500, 700, 2333, 129, 128, 4000, 3999]
+    case = W.custom(B=len(lens), Hq=4, Hkv=2, D=128, ps=16, seq_lens=lens, shared_frac=0.8, seed=max_ctas)
+    h = W.host_tensors(case)
+    plan, got, lse, _, _ = run_both(case, h, cuda_device, chunk_tiles, private_tails=tails, max_ctas=max_ctas)
+    assert plan.num_segments > 0
+    ref, ref_lse = oracle.decode_attn(h.q, h.k_pool, h.v_pool, case.page_table, case.seq_lens)
+    check(got, ref, lse, ref_lse)
+
+
+def test_huginn_full_size_all_tensor_core_few_ctas(cuda_device):
+    case = W.config("huginn")
+    h = W.host_tensors(case)
+    plan, got, lse, _, _ = run_both(case, h, cuda_device, 1, private_tails=True, max_ctas=5)
+    assert plan.max_rest_len == 0
+    ref, ref_lse = oracle.decode_attn(h.q, h.k_pool, h.v_pool, case.page_table, case.seq_lens)
+    check(got, ref, lse, ref_lse)
