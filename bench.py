@@ -248,17 +248,15 @@ def run_gpu(args, rank, world):
     stream = torch.cuda.current_stream(dev)
     banks = [int(bmap[l, t]) for (l, t) in lp]
 
-    ev_attn = []
 
-    def step(st, time_attn=False):
+    def step(st, events=None):
+        """One decode step; with ``events`` (one pair per bank), each attention call is bracketed."""
         if nz is not None:
             rlt.rlt_latent_noise_init(seeds, pos, nz.channels, nz.initializer_range, out=noise, stream=st)
         for i, bank in enumerate(banks):
             rlt.rlt_kv_append(pool, bank, kn[i], vn[i], loc, stream=st)
-            if time_attn:
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(st)
+            if events is not None:
+                events[i][0].record(st)
             if plan is not None:
                 rlt.rlt_paged_decode_attn_prefix(pool, bank, q[i], pt, sl, case.max_seq_len, plan, out=out[i],
                                                  workspace=ws, split_tokens=args.split_tokens,
@@ -266,9 +264,13 @@ def run_gpu(args, rank, world):
             else:
                 rlt.rlt_paged_decode_attn(pool, bank, q[i], pt, sl, case.max_seq_len, out=out[i], workspace=ws,
                                           split_tokens=args.split_tokens, stream=st)
-            if time_attn:
-                e1.record(st)
-                ev_attn.append((e0, e1))
+            if events is not None:
+                events[i][1].record(st)
+
+    def new_events(external):
+        kw = {"external": True} if external else {}
+        return [(torch.cuda.Event(enable_timing=True, **kw), torch.cuda.Event(enable_timing=True, **kw))
+                for _ in banks]
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -281,15 +283,24 @@ def run_gpu(args, rank, world):
         step(stream)
     assert rlt.rlt_get_device_error() == 0
 
-    # the whole step as one CUDA-graph submission (every call is stream-capturable)
-    graph = None
+    # the whole step as one CUDA-graph submission (every call is stream-capturable); a second
+    # capture brackets each attention call with event-record nodes, for the roofline timing
+    graph = timed_graph = graph_events = None
     if args.graph == "on":
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(stream)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=side):
-            step(side)
-        stream.wait_stream(side)
+        def capture(events=None):
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(stream)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                step(side, events)
+            stream.wait_stream(side)
+            return g
+        graph = capture()
+        try:
+            graph_events = new_events(external=True)
+            timed_graph = capture(graph_events)
+        except TypeError:              # a torch without graph-recordable events: time eager calls
+            graph_events = timed_graph = None
         for _ in range(args.warmup):
             graph.replay()
         assert rlt.rlt_get_device_error() == 0
@@ -311,12 +322,21 @@ def run_gpu(args, rank, world):
             run_step()
         t1.record(stream)
         barrier()
-        # the attention calls one by one (eager launches, an event pair around each) for the roofline
+        # each attention call on the device, an event pair around it, step by step
+        attn_ms = []
         for _ in range(args.steps):
-            step(stream, time_attn=True)
+            if timed_graph is not None:
+                timed_graph.replay()
+                torch.cuda.synchronize(dev)
+                attn_ms += [a.elapsed_time(b) for a, b in graph_events]
+            else:
+                events = new_events(external=False)
+                step(stream, events)
+                torch.cuda.synchronize(dev)
+                attn_ms += [a.elapsed_time(b) for a, b in events]
         barrier()
     ms_total = t0.elapsed_time(t1)
-    attn_ms = [a.elapsed_time(b) for a, b in ev_attn]
+    attn_timing = "CUDA-graph event nodes" if timed_graph is not None else "eager event pairs"
     assert rlt.rlt_get_device_error() == 0
 
     # ---- end to end: this step's inputs from pinned host memory, outputs back to the host
@@ -362,7 +382,8 @@ def run_gpu(args, rank, world):
         per_lp = 3 if ws_bytes > 0 else 2
     combine = ws_bytes > 0
     launches = args.steps * (len(banks) * per_lp + (1 if nz is not None else 0))
-    return dict(case=case, banks=banks, cascade=plan is not None, graph=graph is not None, ms_total=ms_total, attn_ms=attn_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+    return dict(case=case, banks=banks, cascade=plan is not None, graph=graph is not None, attn_timing=attn_timing,
+                ms_total=ms_total, attn_ms=attn_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                 clocks=clocks.summary(), launches=launches, combine=combine, ws_bytes=ws_bytes)
 
 
@@ -537,7 +558,8 @@ def main():
                                 if r["cascade"] else "rlt_paged_decode_attn (split-K partial + combine)"),
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": f"{peak_kind} (HBM copy)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": a_bytes, "launch_us": round(attn_launch_ms * 1e3, 2)},
+                     "algorithmic_bytes_per_launch": a_bytes, "launch_us": round(attn_launch_ms * 1e3, 2),
+                     "timing": r["attn_timing"]},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"]},
