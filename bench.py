@@ -217,7 +217,9 @@ def run_gpu(args, rank, world):
     out_h = torch.empty_like(out, device="cpu").pin_memory()
     # shared-prefix plan (the scheduler's radix tree, recovered from the page tables)
     plan = None
-    tails = args.tails != "off"
+    # every token on tensor cores once a kv head serves >= 8 query heads; below that the
+    # private rest goes to the split-K kernel, run beside the tensor-core kernel
+    tails = args.tails == "on" or (args.tails == "auto" and case.group >= 8)
     if args.cascade != "off":
         shared = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, 1, False, case.group)
         if shared.num_segments > 0 or args.cascade == "on":
@@ -501,7 +503,7 @@ def main():
                     help="128-token tiles per work item of the tensor-core kernel (0 = from the plan's size)")
     ap.add_argument("--tails", default="auto", choices=["auto", "on", "off"],
                     help="with a shared prefix, also send each request's unshared tokens through the "
-                         "tensor-core kernel (auto = on); off leaves them to the split-K kernel")
+                         "tensor-core kernel (auto: when a kv head serves >= 8 query heads)")
     ap.add_argument("--graph", default="on", choices=["on", "off"],
                     help="submit each decode step as one captured CUDA graph (on) or as eager launches")
     ap.add_argument("--prefix-ctas", type=int, default=0,

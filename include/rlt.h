@@ -4,7 +4,9 @@
  * One shared library (librlt.so, sm_103a) with plain pointers and sizes: no
  * C++ or framework types cross this boundary.  All array arguments of the
  * compute entry points are DEVICE pointers owned by the caller; the library
- * allocates nothing and keeps no state besides a per-device error word.
+ * allocates no device memory and keeps no state besides a per-device error
+ * word and, once a shared-prefix call needs it, a per-device side stream with
+ * two events (rlt_paged_decode_attn_prefix).
  * Every compute call is enqueued on the caller's stream (a cudaStream_t passed
  * as void*; NULL = the legacy default stream), returns without waiting for the
  * GPU, and makes no host/device synchronisation.  Arguments are checked on
@@ -18,7 +20,8 @@
  * is one graph submission, as the pages' engines run decode ([FFM] "Recurrent
  * depth": the decode CUDA graph; vllm-rlt PR #148, decode loops fused into one
  * submission).  Make each kind of call once on the device before capturing it
- * (the first call sets per-device kernel attributes).  A replay reads the
+ * (the first call sets per-device kernel attributes and creates the side
+ * stream).  A replay reads the
  * arrays' contents at replay time; shapes, max_seq_len, split_tokens and a
  * shared-prefix plan's sizes are fixed at capture.
  *
@@ -226,9 +229,13 @@ RLT_API size_t rlt_paged_decode_prefix_workspace_size(int32_t batch, int32_t num
  * max_prefix_slots, max_rest_len are sizes[0], [6], [3], [5] of the plan,
  * which must have been built with this call's query group, and chunk_tiles
  * the value it was built with; max_rest_len == 0 (private tails) launches no
- * split-K kernel.  The tensor-core kernel is persistent: max_ctas CTAs (0 = one
- * per SM; fewer leave SMs to other streams) share the num_kv_heads x
- * work_units work items in contiguous runs.  Other arguments as
+ * split-K kernel.  Otherwise the split-K kernel runs at the same time as the
+ * tensor-core kernel, on the library's side stream for this device (forked
+ * from and joined back to `stream` with events, so stream capture records both
+ * branches).  The tensor-core kernel is persistent: max_ctas CTAs (0 = the
+ * library's choice: one per SM alone, or the SMs split between the two kernels
+ * in proportion to their estimated tokens) share the num_kv_heads x work_units
+ * work items in contiguous runs.  Other arguments as
  * rlt_paged_decode_attn; the workspace (rlt_paged_decode_prefix_workspace_size
  * bytes) is required.  num_segments == 0 runs rlt_paged_decode_attn.
  * Supported: head_dim 128, num_q_heads/num_kv_heads in {1, 2, 4, 8}, page_size

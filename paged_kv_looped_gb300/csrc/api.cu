@@ -47,6 +47,34 @@ rlt_status device_info(unsigned int **err, int *num_sms)
     return RLT_OK;
 }
 
+// A second stream and two events per device: in shared-prefix mode the split-K
+// kernel runs beside the tensor-core kernel (fork from the caller's stream, join
+// back before the combine).  Created on the first such call on the device.
+struct SideStream {
+    cudaStream_t stream;
+    cudaEvent_t fork, join;
+};
+SideStream g_side[kMaxDevices];
+
+rlt_status side_stream(SideStream **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return RLT_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    SideStream &s = g_side[dev];
+    if (s.stream == nullptr) {
+        SideStream n{};
+        if (cudaStreamCreateWithFlags(&n.stream, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) != cudaSuccess)
+            return RLT_ERR_CUDA;
+        s = n;
+    }
+    *out = &s;
+    return RLT_OK;
+}
+
 int current_sms()
 {
     int sms = 0;
@@ -310,13 +338,41 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     pp.num_segments = num_segments;
     pp.chunk_tiles = chunk_tiles;
     pp.work_units = work_units;
-    pp.ctas = (int32_t)std::min<int64_t>(max_ctas > 0 ? std::min(max_ctas, sms) : sms,
-                                         (int64_t)pool->num_kv_heads * work_units);
+    const int64_t items = (int64_t)pool->num_kv_heads * work_units;
+    int ctas = sms;
+    if (max_ctas > 0) {
+        ctas = std::min(max_ctas, sms);
+    } else if (max_rest_len > 0 && sms > 1) {
+        // both kernels at once: SMs in proportion to their tokens (the rest's length is
+        // its longest, 3/4 of it on average), weighted 3:1 for the tensor-core kernel's
+        // lower rate per SM on the short runs a split plan leaves it
+        const double pre = (double)work_units * chunk_tiles * rlt::kPrefixTile;
+        const double rest = 0.75 * (double)batch * max_rest_len;
+        const double share = std::min(1.0, 3.0 * pre / (pre + rest));
+        ctas = std::max(1, std::min(sms - 1, (int)std::ceil(sms * share)));
+    }
+    pp.ctas = (int32_t)std::min<int64_t>(ctas, items);
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    cudaError_t e = rlt::launch_prefix(p, pp, p.k_bank, p.v_bank, bank_rows, cs);
-    if (e == cudaSuccess && max_rest_len > 0)
-        e = rlt::launch_decode(p, pool->head_dim, group, cs);
+    cudaError_t e = cudaSuccess;
+    if (max_rest_len > 0) {
+        SideStream *side = nullptr;
+        if ((st = side_stream(&side)) != RLT_OK)
+            return st;
+        e = cudaEventRecord(side->fork, cs);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+        if (e == cudaSuccess)
+            e = rlt::launch_prefix(p, pp, p.k_bank, p.v_bank, bank_rows, cs);
+        if (e == cudaSuccess)
+            e = rlt::launch_decode(p, pool->head_dim, group, side->stream);
+        if (e == cudaSuccess)
+            e = cudaEventRecord(side->join, side->stream);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(cs, side->join, 0);
+    } else {
+        e = rlt::launch_prefix(p, pp, p.k_bank, p.v_bank, bank_rows, cs);
+    }
     if (e == cudaSuccess)
         e = rlt::launch_combine(p, pool->head_dim, cs);
     return from_cuda(e);

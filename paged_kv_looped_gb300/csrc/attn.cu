@@ -127,16 +127,13 @@ __device__ __forceinline__ void pv_tile(const unsigned char *vs, const float *pb
 template <int D, int G>
 __device__ __forceinline__ void decode_partial_body(const DecodeParams &p);
 
-// The split-K kernel.  In shared-prefix mode it is launched as a programmatic
-// dependent of the tensor-core prefix kernel, so its CTAs can run on SMs the
-// prefix kernel leaves idle; every CTA then waits for that kernel before it
-// exits, so that whatever follows in the stream (the combine) sees both
-// kernels' partials.  Without such a launch the wait returns at once.
+// The split-K kernel.  In shared-prefix mode it covers each request's tokens
+// past its shared segments and runs beside the tensor-core kernel, on a second
+// stream; the combine waits for both.
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads) decode_partial_kernel(const DecodeParams p)
 {
     decode_partial_body<D, G>(p);
-    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int D, int G>
@@ -573,24 +570,7 @@ cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream)
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     const dim3 grid(p.max_splits, p.num_kv_heads, p.batch);
-    if (p.request_prefix == nullptr) {
-        kernel<<<grid, kThreads, C::kSmemBytes, stream>>>(p);
-    } else {
-        // overlap with the shared-prefix kernel launched just before on this stream
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = grid;
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = C::kSmemBytes;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, kernel, p);
-        if (e != cudaSuccess)
-            return e;
-    }
+    kernel<<<grid, kThreads, C::kSmemBytes, stream>>>(p);
     e = cudaGetLastError();
     // plain decode merges here; shared-prefix mode merges after the prefix kernel
     if (e != cudaSuccess || p.max_splits <= 1 || p.request_prefix != nullptr)

@@ -185,16 +185,13 @@ __device__ __forceinline__ bool take_desc(uint64_t *bars, const unsigned char *b
 }
 
 // Dims 64*half..64*half+63 of this thread's query row (member row / G, head row % G of
-// run d) into columns 32*half.. of the TMEM Q buffer at t_q, as packed bf16 pairs (the
-// A operand layout of S = Q K^T); rows past the run's members are zero.  Then the
-// warp's arrive on the buffer's barrier.
-__device__ __forceinline__ void stage_q(const DecodeParams &p, const RunDesc &d, int G, int row, int member,
-                                        int half, uint32_t t_q, uint64_t *bar, int lane)
+// run d) as 32 words of packed bf16 pairs; zero for rows past the run's members.
+__device__ __forceinline__ void load_q(const DecodeParams &p, const RunDesc &d, int G, int row, int member,
+                                       int half, uint32_t (&w)[32])
 {
-    const bool live = row < d.n_mem * G;
+    const bool live = d.nsub > 0 && row < d.n_mem * G;
     const uint4 *src = reinterpret_cast<const uint4 *>(
         p.q + ((int64_t)member * p.num_q_heads + d.g * G + row % G) * 128 + half * 64);
-    uint32_t w[32];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const uint4 v = live ? src[i] : make_uint4(0u, 0u, 0u, 0u);
@@ -203,6 +200,14 @@ __device__ __forceinline__ void stage_q(const DecodeParams &p, const RunDesc &d,
         w[4 * i + 2] = v.z;
         w[4 * i + 3] = v.w;
     }
+}
+
+// Those words into columns 32*half.. of the TMEM Q buffer at t_q (the A operand
+// layout of S = Q K^T: a row's dims in order, two per column, the lower in the low
+// half), then the warp's arrive on the buffer's barrier.
+__device__ __forceinline__ void store_q(const uint32_t (&w)[32], int half, uint32_t t_q, uint64_t *bar,
+                                        int lane)
+{
     tc::tmem_st32u(t_q + half * 32, w);
     tc::fence_before_sync();
     __syncwarp();
@@ -226,8 +231,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
                          const __grid_constant__ CUtensorMap vmap, const DecodeParams p,
                          const PrefixParams pp)
 {
-    // the split-K kernel that may follow starts as soon as SMs free up
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -483,6 +486,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
             *abort_flag = 1;
     } else {
         // ------------------------------------------------------------- softmax
+        // Run r: its first sub-tile's S is waited for with the next run's Q rows already
+        // loaded, so that Q goes into TMEM at once (the previous run's S MMAs are then
+        // complete); the epilogue of run r-1 is deferred until after run r's first P,
+        // so the tensor pipe computes that P.V while O is read out.
         const int quarter = warp & 3, half = warp >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
@@ -492,16 +499,70 @@ __global__ void __launch_bounds__(kPThreads, 1)
         int n = 0, meets = 0;
         RunDesc rd, rn;
         int b_row = 0, b_next = 0;
-        // run 0's Q; each later run's Q is written while the run before it computes
+        // the run whose epilogue is pending
+        RunDesc ed{};
+        int e_b = 0, e_last = -1;
+        float e_m = 0.f, e_l = 0.f;
+        auto epilogue = [&]() -> bool {
+            if (!warp_wait(&bars[kBarPvDone + e_last % kSBufs], (e_last / kSBufs) & 1u, abort_flag))
+                return false;
+            tc::fence_after_sync();
+            const int R = ed.n_mem * G;
+            const bool live = quarter * 32 < R;
+            const int64_t slot = ((int64_t)e_b * p.num_q_heads + ed.g * G + row % G) * p.part_stride + ed.slot;
+            float l_tot = e_l;
+            if (live) {
+                xsum[half * 128 + row] = e_l;
+                if (!pair_sync(pair, meets, abort_flag, lane))
+                    return false;
+                l_tot = e_l + xsum[(half ^ 1) * 128 + row];
+                const float inv = 1.f / l_tot;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    float o[32];
+                    tc::tmem_ld32(t_lane + kColO + half * 64 + c * 32, o);
+                    if (row < R) {
+                        float4 *dst = reinterpret_cast<float4 *>(p.o_part + slot * 128 + half * 64 + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                                 o[4 * i + 3] * inv);
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars[kBarOFree]);
+            if (live && half == 0 && row < R) {
+                p.lse_part[slot] = e_m + log2f(l_tot);
+                for (int k = 1; k < ed.nchunks; ++k)   // chunks merged into this run's partial
+                    p.lse_part[slot + k] = -CUDART_INF_F;
+            }
+            // both warps have read xsum before a later epilogue writes it
+            return !live || pair_sync(pair, meets, abort_flag, lane);
+        };
+
+        uint32_t qw[32];
         ok = take_desc(bars, base, 0, rd, row / G, b_row, abort_flag, lane);
-        if (ok && rd.nsub > 0)
-            stage_q(p, rd, G, row, b_row, half, t_lane + kColQ, &bars[kBarQFull], lane);
+        if (ok && rd.nsub > 0) {
+            load_q(p, rd, G, row, b_row, half, qw);
+            store_q(qw, half, t_lane + kColQ, &bars[kBarQFull], lane);
+        }
         for (int r = 0; ok && rd.nsub > 0; ++r) {
+            // the next run's Q rows, loaded while this run's first S is computed
+            if (!(ok = take_desc(bars, base, r + 1, rn, row / G, b_next, abort_flag, lane)))
+                break;
+            load_q(p, rn, G, row, b_next, half, qw);
             const int R = rd.n_mem * G;
             const bool live = quarter * 32 < R;  // uniform over the quarter's two warps; quarter 0 is live
             float m_ref = -CUDART_INF_F, l_run = 0.f;   // l_run: this warp's columns only
+            if (!(ok = warp_wait(&bars[kBarSFull + n % kSBufs], (n / kSBufs) & 1u, abort_flag)))
+                break;
+            if (rn.nsub > 0)   // the previous run's S MMAs are complete: its Q buffer is free
+                store_q(qw, half, t_lane + kColQ + ((r + 1) % kQBufs) * 64, &bars[kBarQFull + (r + 1) % kQBufs], lane);
             for (int j = 0; j < rd.nsub; ++j, ++n) {
-                if (!(ok = warp_wait(&bars[kBarSFull + n % kSBufs], (n / kSBufs) & 1u, abort_flag)))
+                if (j > 0 && !(ok = warp_wait(&bars[kBarSFull + n % kSBufs], (n / kSBufs) & 1u, abort_flag)))
                     break;
                 const uint32_t t_s = t_lane + kColS + (n % kSBufs) * kSub;
                 if (live) {
@@ -513,10 +574,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         // hold anything (0 * NaN would poison O), once this V copy has landed
                         if (!(ok = warp_wait(&bars[kBarFullV + n % kStagesV], (n / kStagesV) & 1u, abort_flag)))
                             break;
-                        const int vr = valid;           // warp 0: half 0, so valid counts from token 0
                         unsigned char *vst = base + kVOff + (n % kStagesV) * kKVBytes;
-                        for (int c = lane; c < (kSub - vr) * 16; c += 32) {
-                            const int rr = vr + c / 16, c16 = c % 16;
+                        for (int c = lane; c < (kSub - valid) * 16; c += 32) {
+                            const int rr = valid + c / 16, c16 = c % 16;
                             *reinterpret_cast<uint4 *>(vst + (c16 >> 3) * kHalfKV + rr * 128 + (c16 & 7) * 16) =
                                 make_uint4(0u, 0u, 0u, 0u);
                         }
@@ -572,58 +632,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&bars[kBarPFull + n % kSBufs]);
-                if (j == 0) {
-                    // the S MMAs of the previous run are complete, so its Q buffer takes the
-                    // next run's Q now
-                    if (!(ok = take_desc(bars, base, r + 1, rn, row / G, b_next, abort_flag, lane)))
+                if (j == 0 && e_last >= 0) {
+                    // run r-1's epilogue: its last P.V ran while this P was being made
+                    if (!(ok = epilogue()))
                         break;
-                    if (rn.nsub > 0)
-                        stage_q(p, rn, G, row, b_next, half, t_lane + kColQ + ((r + 1) % kQBufs) * 64,
-                                &bars[kBarQFull + (r + 1) % kQBufs], lane);
+                    e_last = -1;
                 }
             }
             if (!ok)
                 break;
-            // run epilogue: O / l -> the run's partial slot; O is free afterwards
-            if (!(ok = warp_wait(&bars[kBarPvDone + (n - 1) % kSBufs], ((n - 1) / kSBufs) & 1u, abort_flag)))
-                break;
-            tc::fence_after_sync();
-            const int64_t slot =
-                ((int64_t)b_row * p.num_q_heads + rd.g * G + row % G) * p.part_stride + rd.slot;
-            float l_tot = l_run;
-            if (live) {
-                xsum[half * 128 + row] = l_run;
-                if (!(ok = pair_sync(pair, meets, abort_flag, lane)))
-                    break;
-                l_tot = l_run + xsum[(half ^ 1) * 128 + row];
-                const float inv = 1.f / l_tot;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    float o[32];
-                    tc::tmem_ld32(t_lane + kColO + half * 64 + c * 32, o);
-                    if (row < R) {
-                        float4 *dst = reinterpret_cast<float4 *>(p.o_part + slot * 128 + half * 64 + c * 32);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
-                                                 o[4 * i + 3] * inv);
-                    }
-                }
-            }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&bars[kBarOFree]);
-            if (live && half == 0 && row < R) {
-                p.lse_part[slot] = m_ref + log2f(l_tot);
-                for (int k = 1; k < rd.nchunks; ++k)   // chunks merged into this run's partial
-                    p.lse_part[slot + k] = -CUDART_INF_F;
-            }
-            if (live && !(ok = pair_sync(pair, meets, abort_flag, lane)))   // xsum read by both before
-                break;                                                       // the next run writes it
+            ed = rd;
+            e_b = b_row;
+            e_m = m_ref;
+            e_l = l_run;
+            e_last = n - 1;
             rd = rn;
             b_row = b_next;
         }
+        if (ok && e_last >= 0)
+            ok = epilogue();
         if (!ok)
             *abort_flag = 1;
     }
