@@ -68,6 +68,11 @@ def _load():
             "oracle_noise_hash24": (None, [P, P, i64, i32, P]),
             "oracle_noise_value": (f64, [ctypes.c_uint32, f64]),
             "oracle_latent_noise_init": (None, [P, P, i64, i32, f64, P]),
+            "oracle_bf16_round": (ctypes.c_uint16, [f64]),
+            "oracle_rope": (None, [P, i32, i32, f64, i64, P]),
+            "oracle_kv_append_rope": (None, [P, P, i64, i32, i32, i32, i32, P, P, P, P, i32, i32, f64]),
+            "oracle_mark_written": (None, [P, i32, i32, P, P, P, i32]),
+            "oracle_publishable_prefix": (None, [P, i32, i32, P, i32, i32, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -207,4 +212,51 @@ def latent_noise_init(seeds, positions, channels: int, initializer_range: float)
     out = np.empty((s.size, channels), np.float64)
     _load().oracle_latent_noise_init(_ptr(s), _ptr(p), s.size, channels, float(initializer_range),
                                      _ptr(out))
+    return out
+
+
+# ------------------------------------------------------- RoPE, fused append
+
+def bf16_round(x: float) -> int:
+    """Correctly rounded (nearest, ties to even) bf16 bits of a double."""
+    return int(_load().oracle_bf16_round(float(x)))
+
+
+def rope(x, pos: int, rot_dim: int, base: float):
+    """fp64 rotate-half RoPE of one row x[head_dim] at sequence position pos."""
+    xx = _c(x, np.float64)
+    out = np.empty_like(xx)
+    _load().oracle_rope(_ptr(xx), xx.size, rot_dim, float(base), int(pos), _ptr(out))
+    return out
+
+
+def kv_append_rope(k_pool, v_pool, k_new, v_new, positions, out_loc, rot_dim: int, base: float, bank: int = 0):
+    """In-place store_kv with the keys rotated at their positions (bf16 bits)."""
+    assert k_pool.dtype == np.uint16 and k_pool.flags.c_contiguous
+    assert v_pool.dtype == np.uint16 and v_pool.flags.c_contiguous
+    nb, P, Hkv, ps, D = _pool_dims(k_pool)
+    kn = _c(k_new, np.uint16)
+    vn = _c(v_new, np.uint16)
+    pos = _c(positions, np.int64)
+    loc = _c(out_loc, np.int64)
+    _load().oracle_kv_append_rope(_ptr(k_pool), _ptr(v_pool), P, Hkv, ps, D, bank, _ptr(kn), _ptr(vn),
+                                  _ptr(pos), _ptr(loc), loc.size, rot_dim, float(base))
+
+
+# ------------------------------------------------------ prefix publication
+
+def mark_written(written, bank: int, request, positions, out_loc):
+    """In place: written[bank][r] = max(written[bank][r], p + 1) for each appended token."""
+    assert written.dtype == np.int32 and written.flags.c_contiguous
+    req = _c(request, np.int32)
+    _load().oracle_mark_written(_ptr(written), written.shape[1], bank, _ptr(req), _ptr(_c(positions, np.int64)),
+                                _ptr(_c(out_loc, np.int64)), req.size)
+
+
+def publishable_prefix(bank_map_, written, page_size: int):
+    """Tokens per request written in every held (layer, plane) bank, in whole pages."""
+    m = _c(bank_map_, np.int32)
+    w = _c(written, np.int32)
+    out = np.empty(w.shape[1], np.int32)
+    _load().oracle_publishable_prefix(_ptr(m), m.shape[0], m.shape[1], _ptr(w), w.shape[1], page_size, _ptr(out))
     return out

@@ -278,3 +278,137 @@ void oracle_latent_noise_init(const uint64_t *seeds, const int64_t *positions, i
             out[r * channels + c] = oracle_noise_value(h24, initializer_range);
         }
 }
+
+/* ------------------------------------------- RoPE at the token's position */
+
+/*
+ * Correctly rounded (nearest, ties to even) bf16 bit pattern of a double: the
+ * value is scaled by the bf16 quantum of its binade (a power of two, so the
+ * scaling is exact), rounded to an integer, and scaled back.
+ */
+static uint16_t bf16_round(double x)
+{
+    if (isnan(x))
+        return 0x7FC0;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double ax = fabs(x);
+    if (ax == 0.0)
+        return sign;
+    int e;
+    frexp(ax, &e);                        /* ax = m * 2^e, m in [1/2, 1) */
+    int qe = e - 8;                       /* 8 significant bits */
+    if (qe < -133)
+        qe = -133;                        /* subnormal quantum 2^-133 */
+    double r = rint(ldexp(ax, -qe));      /* default rounding: nearest, ties to even */
+    double v = ldexp(r, qe);
+    if (v >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7F80); /* overflow: infinity */
+    float f = (float)v;                   /* exact: v has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (u >> 16));
+}
+
+uint16_t oracle_bf16_round(double x) { return bf16_round(x); }
+
+/*
+ * Rotary position embedding of one head row x[head_dim] at sequence position
+ * pos, as the fused append applies it to keys.  [FFM] "Recurrent depth": a
+ * token keeps one RoPE position across all T of its banks, so pos is the
+ * token's index in its sequence, never its loop depth.  Rotate-half pairing:
+ * for i < rot_dim / 2 the pair (x[i], x[i + rot_dim/2]) turns by the angle
+ * pos * base^(-2i / rot_dim); dims rot_dim .. head_dim-1 are copied.  fp64.
+ */
+void oracle_rope(const double *x, int32_t head_dim, int32_t rot_dim, double base, int64_t pos,
+                 double *out)
+{
+    int32_t half = rot_dim / 2;
+    for (int32_t d = 0; d < head_dim; ++d)
+        out[d] = x[d];
+    for (int32_t i = 0; i < half; ++i) {
+        double angle = (double)pos * pow(base, -2.0 * i / rot_dim);
+        double c = cos(angle), s = sin(angle);
+        out[i] = x[i] * c - x[i + half] * s;
+        out[i + half] = x[i] * s + x[i + half] * c;
+    }
+}
+
+/*
+ * store_kv with the keys rotated first: token i's K rows (bf16 [Hkv][D]) turn
+ * by RoPE at positions[i] and are rounded to bf16 (nearest even); its V rows
+ * are copied.  Written to slot out_loc[i] of the bank; slots below zero are
+ * skipped.
+ */
+void oracle_kv_append_rope(uint16_t *k_pool, uint16_t *v_pool, int64_t num_pages,
+                           int32_t num_kv_heads, int32_t page_size, int32_t head_dim, int32_t bank,
+                           const uint16_t *k_new, const uint16_t *v_new, const int64_t *positions,
+                           const int64_t *out_loc, int32_t n_tokens, int32_t rot_dim, double base)
+{
+    double x[1024], y[1024];
+    if (head_dim > 1024)
+        return;
+    for (int32_t i = 0; i < n_tokens; ++i) {
+        int64_t slot = out_loc[i];
+        if (slot < 0)
+            continue;
+        int64_t page = slot / page_size, offset = slot % page_size;
+        for (int32_t g = 0; g < num_kv_heads; ++g) {
+            int64_t dst = pool_row(bank, page, g, offset, num_pages, num_kv_heads, page_size,
+                                   head_dim);
+            int64_t src = ((int64_t)i * num_kv_heads + g) * head_dim;
+            for (int32_t d = 0; d < head_dim; ++d)
+                x[d] = bf16_value(k_new[src + d]);
+            oracle_rope(x, head_dim, rot_dim, base, positions[i], y);
+            for (int32_t d = 0; d < head_dim; ++d) {
+                k_pool[dst + d] = bf16_round(y[d]);
+                v_pool[dst + d] = v_new[src + d];
+            }
+        }
+    }
+}
+
+/* --------------------------------------- prefix publication [PR152] */
+
+/*
+ * Written-prefix counters: written[bank * batch + r] is the length of the
+ * prefix of request r that the bank holds.  Appends come in sequence order
+ * (a decode token, or a prefill chunk), so each appended token at position p
+ * extends the counter to at least p + 1.  Tokens with out_loc < 0 are skipped.
+ */
+void oracle_mark_written(int32_t *written, int32_t batch, int32_t bank, const int32_t *request,
+                         const int64_t *positions, const int64_t *out_loc, int32_t n_tokens)
+{
+    for (int32_t i = 0; i < n_tokens; ++i) {
+        if (out_loc[i] < 0)
+            continue;
+        int32_t *w = &written[(int64_t)bank * batch + request[i]];
+        if (*w < positions[i] + 1)
+            *w = (int32_t)(positions[i] + 1);
+    }
+}
+
+/*
+ * Tokens of each request that may be published to the prefix cache: the
+ * prefix written in every (layer, plane) bank the model holds, in whole pages.
+ * [PR152] Summary (per-plane coverage, "all layers at depth 0, the recurrent
+ * layers deeper"): planes that do not hold a layer (map -1) are not asked for
+ * it.  A model holding no bank publishes nothing.
+ */
+void oracle_publishable_prefix(const int32_t *map, int32_t num_layers, int32_t num_planes,
+                               const int32_t *written, int32_t batch, int32_t page_size,
+                               int32_t *out)
+{
+    for (int32_t b = 0; b < batch; ++b) {
+        int64_t m = -1;
+        for (int32_t l = 0; l < num_layers; ++l)
+            for (int32_t t = 0; t < num_planes; ++t) {
+                int32_t bank = map[l * num_planes + t];
+                if (bank < 0)
+                    continue;
+                int64_t w = written[(int64_t)bank * batch + b];
+                if (m < 0 || w < m)
+                    m = w;
+            }
+        out[b] = m < 0 ? 0 : (int32_t)(m / page_size * page_size);
+    }
+}
