@@ -249,6 +249,10 @@ def run_gpu(args, rank, world):
         noise_h = torch.empty_like(noise, device="cpu").pin_memory()
     stream = torch.cuda.current_stream(dev)
     banks = [int(bmap[l, t]) for (l, t) in lp]
+    # fused RoPE append: each new token at its sequence position (the last of its request)
+    new_pos = torch.from_numpy(np.maximum(case.seq_lens.astype(np.int64) - 1, 0)).to(dev)
+    req_ids = torch.arange(B, dtype=torch.int32, device=dev)
+    written = torch.zeros((nbanks, B), dtype=torch.int32, device=dev)
 
 
     def step(st, events=None):
@@ -256,7 +260,11 @@ def run_gpu(args, rank, world):
         if nz is not None:
             rlt.rlt_latent_noise_init(seeds, pos, nz.channels, nz.initializer_range, out=noise, stream=st)
         for i, bank in enumerate(banks):
-            rlt.rlt_kv_append(pool, bank, kn[i], vn[i], loc, stream=st)
+            if args.append == "rope":
+                rlt.rlt_kv_append_rope(pool, bank, kn[i], vn[i], new_pos, loc, case.head_dim, 10000.0,
+                                       request=req_ids, written=written, stream=st)
+            else:
+                rlt.rlt_kv_append(pool, bank, kn[i], vn[i], loc, stream=st)
             if events is not None:
                 events[i][0].record(st)
             if plan is not None:
@@ -464,7 +472,7 @@ def config_dict(case, args):
             "split_tokens": args.split_tokens or "auto",
             "cascade": args.cascade, "chunk_tiles": args.chunk_tiles, "tails": args.tails,
             "prefix_ctas": args.prefix_ctas or "one per SM",
-            "banks_run": args.banks or "all", "cuda_graph": args.graph,
+            "banks_run": args.banks or "all", "cuda_graph": args.graph, "append": args.append,
             "l2": "inputs larger than L2: every bank's KV exceeds the 129 MB L2 and each is read once per step"}
 
 
@@ -506,6 +514,8 @@ def main():
                          "tensor-core kernel (auto: when a kv head serves >= 8 query heads)")
     ap.add_argument("--graph", default="on", choices=["on", "off"],
                     help="submit each decode step as one captured CUDA graph (on) or as eager launches")
+    ap.add_argument("--append", default="plain", choices=["plain", "rope"],
+                    help="store_kv as given (plain) or with RoPE fused on the keys and written-prefix counters")
     ap.add_argument("--prefix-ctas", type=int, default=0,
                     help="CTAs of the persistent tensor-core kernel (0 = one per SM)")
     ap.add_argument("--banks", type=int, default=0,

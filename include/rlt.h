@@ -125,6 +125,45 @@ RLT_API rlt_status rlt_kv_append(const rlt_kv_pool *pool, int32_t bank, const vo
                          void *stream);
 
 /*
+ * KV append with RoPE fused on the keys ([FFM] "Recurrent depth": a token keeps
+ * one RoPE position across all T of its banks -- its index in its sequence,
+ * never its loop depth -- so every plane's append of the token turns its key
+ * by the same angles; [FFM] "LOTUS": store_kv to the handed slots).  As
+ * rlt_kv_append, except that each key row is rotated first: for i < rot_dim/2
+ * the pair (k[i], k[i + rot_dim/2]) turns by positions[i_token] *
+ * rope_base^(-2i/rot_dim) (rotate-half pairing); dims rot_dim.. are stored as
+ * given; the result is rounded to bf16 (nearest even).  V rows are stored as
+ * given.  The angle is formed and reduced mod 2 pi in fp64, sin/cos and the
+ * rotation in fp32: within one bf16 ulp of the exact rotation.
+ *   positions  int64 [n_tokens], device: sequence position of each token
+ *   rot_dim    even, 2 .. head_dim;  rope_base > 0
+ *   written    NULL, or int32 [num_banks][batch] device written-prefix
+ *              counters (rlt_publishable_prefix): written[bank][request[i]]
+ *              becomes at least positions[i] + 1 for every appended token
+ *              (appends come in sequence order); request int32 [n_tokens]
+ *              gives each token's request, in [0, batch) (others are skipped
+ *              and set RLT_DEVERR_BAD_SLOT).
+ */
+RLT_API rlt_status rlt_kv_append_rope(const rlt_kv_pool *pool, int32_t bank, const void *k_new,
+                                      const void *v_new, const int64_t *positions,
+                                      const int64_t *out_loc, int32_t n_tokens, int32_t rot_dim,
+                                      double rope_base, const int32_t *request, int32_t *written,
+                                      int32_t batch, void *stream);
+
+/*
+ * Prefix-cache publication coverage ([PR152] Summary: publication needs a
+ * contiguous written prefix in every layer of every plane the model HOLDS --
+ * all layers at depth 0, the recurrent layers deeper -- so a partially looped
+ * model such as Huginn can publish).  Banks exist exactly for the held
+ * (layer, plane) pairs (rlt_bank_map), so out[b] = min over banks of
+ * written[bank][b], floored to whole pages of page_size tokens (0 when
+ * num_banks == 0).  written int32 [num_banks][batch], out int32 [batch], both
+ * device.
+ */
+RLT_API rlt_status rlt_publishable_prefix(const int32_t *written, int32_t num_banks, int32_t batch,
+                                          int32_t page_size, int32_t *out, void *stream);
+
+/*
  * Bytes of device workspace rlt_paged_decode_attn needs for these sizes
  * (split-K partial outputs and log-sum-exps).  split_tokens as passed to
  * rlt_paged_decode_attn (0 = the library's choice).  Returns 0 for invalid

@@ -29,7 +29,7 @@ __all__ = [
     "rlt_latent_noise_init",
     "rlt_noise_hash24", "rlt_paged_gather", "rlt_validate_batch", "rlt_get_device_error",
     "rlt_version", "PrefixPlan", "rlt_plan_prefix", "rlt_paged_decode_attn_prefix",
-    "rlt_paged_decode_prefix_workspace_size", "DEVERR_BAD_PAGE", "DEVERR_BAD_SLOT", "DEVERR_TIMEOUT", "DEVERR_BAD_LEN",
+    "rlt_paged_decode_prefix_workspace_size", "rlt_kv_append_rope", "rlt_publishable_prefix", "DEVERR_BAD_PAGE", "DEVERR_BAD_SLOT", "DEVERR_TIMEOUT", "DEVERR_BAD_LEN",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -89,6 +89,8 @@ def load():
         "rlt_paged_decode_attn_prefix": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, P, i32, i32, P, P, P, i32,
                                                         i32, i32, i32, i32, f32, P, P, P, sz, i32, i32, P]),
         "rlt_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
+        "rlt_kv_append_rope": (ctypes.c_int, [pool_p, i32, P, P, P, P, i32, i32, ctypes.c_double, P, P, i32, P]),
+        "rlt_publishable_prefix": (ctypes.c_int, [P, i32, i32, i32, P, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -193,6 +195,32 @@ def rlt_kv_append(pool: KVPool, bank: int, k_new, v_new, out_loc, stream=None):
     _check(load().rlt_kv_append(ctypes.byref(pool.struct), bank, _dev(k_new, torch.bfloat16, "k_new"),
                                 _dev(v_new, torch.bfloat16, "v_new"), _dev(out_loc, torch.int64, "out_loc"),
                                 n, _stream(stream)), "rlt_kv_append")
+
+
+def rlt_kv_append_rope(pool: KVPool, bank: int, k_new, v_new, positions, out_loc, rot_dim: int,
+                       rope_base: float, request=None, written=None, stream=None):
+    """store_kv with RoPE on the keys at each token's sequence position (same for every plane)."""
+    import torch
+    n = int(out_loc.numel())
+    batch = int(written.shape[1]) if written is not None else 0
+    _check(load().rlt_kv_append_rope(
+        ctypes.byref(pool.struct), bank, _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _dev(positions, torch.int64, "positions"), _dev(out_loc, torch.int64, "out_loc"), n, int(rot_dim),
+        float(rope_base), _dev(request, torch.int32, "request") if request is not None else ctypes.c_void_p(0),
+        _dev(written, torch.int32, "written") if written is not None else ctypes.c_void_p(0), batch,
+        _stream(stream)), "rlt_kv_append_rope")
+
+
+def rlt_publishable_prefix(written, page_size: int, out=None, stream=None):
+    """Tokens per request written in every bank (every held layer-plane), in whole pages."""
+    import torch
+    num_banks, batch = int(written.shape[0]), int(written.shape[1])
+    if out is None:
+        out = torch.empty(batch, dtype=torch.int32, device=written.device)
+    _check(load().rlt_publishable_prefix(_dev(written, torch.int32, "written") if num_banks else ctypes.c_void_p(0),
+                                         num_banks, batch, int(page_size), _dev(out, torch.int32, "out"),
+                                         _stream(stream)), "rlt_publishable_prefix")
+    return out
 
 
 def rlt_paged_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,

@@ -161,6 +161,51 @@ RLT_API rlt_status rlt_kv_append(const rlt_kv_pool *pool, int32_t bank, const vo
         static_cast<cudaStream_t>(stream)));
 }
 
+RLT_API rlt_status rlt_kv_append_rope(const rlt_kv_pool *pool, int32_t bank, const void *k_new,
+                                      const void *v_new, const int64_t *positions,
+                                      const int64_t *out_loc, int32_t n_tokens, int32_t rot_dim,
+                                      double rope_base, const int32_t *request, int32_t *written,
+                                      int32_t batch, void *stream)
+{
+    rlt_status st = check_pool(pool, bank);
+    if (st != RLT_OK)
+        return st;
+    if (n_tokens < 0 || rot_dim < 2 || rot_dim % 2 != 0 || rot_dim > pool->head_dim ||
+        !(rope_base > 0.0) || !std::isfinite(rope_base) || (written != nullptr && (request == nullptr || batch < 1)))
+        return RLT_ERR_INVALID_ARG;
+    if (n_tokens == 0)
+        return RLT_OK;
+    if (k_new == nullptr || v_new == nullptr || out_loc == nullptr || positions == nullptr)
+        return RLT_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || reinterpret_cast<uintptr_t>(out_loc) % 8 != 0 ||
+        reinterpret_cast<uintptr_t>(positions) % 8 != 0 ||
+        (written != nullptr && (reinterpret_cast<uintptr_t>(written) % 4 != 0 ||
+                                reinterpret_cast<uintptr_t>(request) % 4 != 0)))
+        return RLT_ERR_INVALID_ARG;
+    unsigned int *err = nullptr;
+    if ((st = device_info(&err, nullptr)) != RLT_OK)
+        return st;
+    const int64_t off = bank * bank_elems(pool);
+    return from_cuda(rlt::launch_append_rope(
+        static_cast<uint16_t *>(pool->k) + off, static_cast<uint16_t *>(pool->v) + off,
+        static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new), positions, out_loc,
+        n_tokens, pool->num_kv_heads, pool->page_size, pool->head_dim, pool->num_pages, rot_dim, rope_base,
+        request, written != nullptr ? written + (int64_t)bank * batch : nullptr, batch, err,
+        static_cast<cudaStream_t>(stream)));
+}
+
+RLT_API rlt_status rlt_publishable_prefix(const int32_t *written, int32_t num_banks, int32_t batch,
+                                          int32_t page_size, int32_t *out, void *stream)
+{
+    if (num_banks < 0 || batch < 0 || page_size < 1 || (batch > 0 && (out == nullptr ||
+                                                                       (num_banks > 0 && written == nullptr))))
+        return RLT_ERR_INVALID_ARG;
+    if (batch == 0)
+        return RLT_OK;
+    return from_cuda(rlt::launch_publishable(written, num_banks, batch, page_size, out,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 RLT_API size_t rlt_paged_decode_workspace_size(int32_t batch, int32_t num_q_heads,
                                                int32_t num_kv_heads, int32_t head_dim,
                                                int32_t max_seq_len, int32_t split_tokens)

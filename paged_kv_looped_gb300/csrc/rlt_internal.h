@@ -78,6 +78,16 @@ cudaError_t launch_append(uint16_t *k_bank, uint16_t *v_bank, const uint16_t *k_
                           int32_t num_kv_heads, int32_t page_size, int32_t head_dim,
                           int64_t num_pages, unsigned int *err, cudaStream_t stream);
 
+cudaError_t launch_append_rope(uint16_t *k_bank, uint16_t *v_bank, const uint16_t *k_new,
+                               const uint16_t *v_new, const int64_t *positions, const int64_t *out_loc,
+                               int32_t n_tokens, int32_t num_kv_heads, int32_t page_size,
+                               int32_t head_dim, int64_t num_pages, int32_t rot_dim, double rope_base,
+                               const int32_t *request, int32_t *written, int32_t batch,
+                               unsigned int *err, cudaStream_t stream);
+
+cudaError_t launch_publishable(const int32_t *written, int32_t num_banks, int32_t batch,
+                               int32_t page_size, int32_t *out, cudaStream_t stream);
+
 cudaError_t launch_gather(const uint16_t *k_bank, const uint16_t *v_bank,
                           const int32_t *page_table, int32_t max_pages, const int32_t *seq_lens,
                           int32_t batch, int32_t max_len, uint16_t *k_out, uint16_t *v_out,
