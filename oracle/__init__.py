@@ -260,3 +260,26 @@ def publishable_prefix(bank_map_, written, page_size: int):
     out = np.empty(w.shape[1], np.int32)
     _load().oracle_publishable_prefix(_ptr(m), m.shape[0], m.shape[1], _ptr(w), w.shape[1], page_size, _ptr(out))
     return out
+
+
+# --------------------------------------------- extend (span) attention
+
+def extend_rows(page_table, seq_lens, new_lens):
+    """Per new query token: (request, its key count = causal limit).  Request b's n_b new
+    tokens are its last n_b positions; the i-th sees keys 0 .. L_b - n_b + i."""
+    req, lim = [], []
+    for b, (L, n) in enumerate(zip(np.asarray(seq_lens), np.asarray(new_lens))):
+        assert 0 <= n <= L
+        for i in range(int(n)):
+            req.append(b)
+            lim.append(int(L) - int(n) + i + 1)
+    return np.array(req, np.int64), np.array(lim, np.int32)
+
+
+def extend_attn(q_ext, k_pool, v_pool, page_table, seq_lens, new_lens, bank: int = 0, scale: float = 0.0):
+    """fp64 (out [N][Hq][D], lse [N][Hq]) of causal attention for every new token of every request
+    ("Faster fuzzy minds", LOTUS: re-forwarding a span is an extend-prefill).  Each new token is a
+    decode query over its own causal prefix, so this is decode_attn on per-token rows."""
+    req, lim = extend_rows(page_table, seq_lens, new_lens)
+    pt = np.ascontiguousarray(np.asarray(page_table, np.int32)[req])
+    return decode_attn(q_ext, k_pool, v_pool, pt, lim, bank, scale)
