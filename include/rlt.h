@@ -289,6 +289,52 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     float *lse_out, void *workspace, size_t workspace_bytes, int32_t split_tokens, int32_t max_ctas,
     void *stream);
 
+/*
+ * Causal extend (span) attention over the paged pool ([FFM] "LOTUS":
+ * re-forwarding a block of positions is one parallel extend-prefill over all
+ * of them, their K/V already written -- in place -- to the block's slots;
+ * packed prefill is the same call for a whole prompt).  Request b's
+ * new_lens[b] new tokens are its last positions; new token i (0-based) sees
+ * keys 0 .. seq_lens[b] - new_lens[b] + i.  For every new token and query
+ * head h:  out = softmax(scale <q, K>) V over those keys, GQA as in
+ * rlt_paged_decode_attn.  q and out are bf16 [num_rows][num_q_heads][D], the
+ * new tokens packed request by request; lse_out (nullable) fp32
+ * [num_rows][num_q_heads], natural log.
+ *
+ * rlt_plan_extend (HOST arrays) lays the work out for the tcgen05 kernel of
+ * rlt_paged_decode_attn_prefix: one segment per request with new tokens,
+ * covering its keys, whose members are its new tokens with their causal
+ * limits; each block of 128 / query_group new tokens reads keys only up to its
+ * last token's limit.  Outputs: segments [sizes[0]][8], members and
+ * member_limit [sizes[1]], row_prefix [num_rows][2] and row_len [num_rows];
+ * sizes[0..6] = segments, rows, max chunks, partial slots per row, max
+ * members, 0, work units.  Returns RLT_ERR_OUT_OF_RANGE (sizes filled) when
+ * the arrays are too small, RLT_ERR_INVALID_ARG for new_lens[b] outside
+ * [0, seq_lens[b]].  Same page_size rule as rlt_plan_prefix.
+ *
+ * rlt_paged_extend_attn takes the plan's arrays as DEVICE copies (plus
+ * sizes[0], [6], [3] as num_segments, work_units, max_slots and the
+ * chunk_tiles the plan was built with) and a workspace of
+ * rlt_paged_extend_workspace_size bytes; page_table is int32 [batch][max_pages]
+ * of the requests.  max_ctas as rlt_paged_decode_attn_prefix.  Supported:
+ * head_dim 128, num_q_heads/num_kv_heads in {1, 2, 4, 8}.
+ */
+RLT_API rlt_status rlt_plan_extend(const int32_t *seq_lens, const int32_t *new_lens, int32_t batch,
+                                   int32_t page_size, int32_t chunk_tiles, int32_t query_group,
+                                   int32_t *segments, int32_t max_segments, int32_t *members,
+                                   int32_t *member_limit, int32_t max_member_entries,
+                                   int32_t *row_prefix, int32_t *row_len, int32_t *sizes);
+
+RLT_API size_t rlt_paged_extend_workspace_size(int32_t num_rows, int32_t num_q_heads, int32_t head_dim,
+                                               int32_t max_slots);
+
+RLT_API rlt_status rlt_paged_extend_attn(
+    const rlt_kv_pool *pool, int32_t bank, const void *q, int32_t num_q_heads, int32_t num_rows,
+    const int32_t *page_table, int32_t max_pages, int32_t batch, const int32_t *segments,
+    const int32_t *members, const int32_t *member_limit, const int32_t *row_prefix, const int32_t *row_len,
+    int32_t num_segments, int32_t work_units, int32_t max_slots, int32_t chunk_tiles, float scale, void *out,
+    float *lse_out, void *workspace, size_t workspace_bytes, int32_t max_ctas, void *stream);
+
 /* Size of the scratch array rlt_paged_decode_attn_noalloc uses (64 MiB). */
 #define RLT_NOALLOC_SCRATCH_BYTES (64u << 20)
 

@@ -29,7 +29,8 @@ __all__ = [
     "rlt_latent_noise_init",
     "rlt_noise_hash24", "rlt_paged_gather", "rlt_validate_batch", "rlt_get_device_error",
     "rlt_version", "PrefixPlan", "rlt_plan_prefix", "rlt_paged_decode_attn_prefix",
-    "rlt_paged_decode_prefix_workspace_size", "rlt_kv_append_rope", "rlt_publishable_prefix", "DEVERR_BAD_PAGE", "DEVERR_BAD_SLOT", "DEVERR_TIMEOUT", "DEVERR_BAD_LEN",
+    "rlt_paged_decode_prefix_workspace_size", "rlt_kv_append_rope", "rlt_publishable_prefix",
+    "ExtendPlan", "rlt_plan_extend", "rlt_paged_extend_attn", "DEVERR_BAD_PAGE", "DEVERR_BAD_SLOT", "DEVERR_TIMEOUT", "DEVERR_BAD_LEN",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -91,6 +92,10 @@ def load():
         "rlt_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
         "rlt_kv_append_rope": (ctypes.c_int, [pool_p, i32, P, P, P, P, i32, i32, ctypes.c_double, P, P, i32, P]),
         "rlt_publishable_prefix": (ctypes.c_int, [P, i32, i32, i32, P, P]),
+        "rlt_plan_extend": (ctypes.c_int, [P, P, i32, i32, i32, i32, P, i32, P, P, i32, P, P, P]),
+        "rlt_paged_extend_workspace_size": (sz, [i32, i32, i32, i32]),
+        "rlt_paged_extend_attn": (ctypes.c_int, [pool_p, i32, P, i32, i32, P, i32, i32, P, P, P, P, P, i32, i32,
+                                                 i32, i32, f32, P, P, P, sz, i32, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -425,4 +430,78 @@ def rlt_paged_decode_attn_prefix(pool: KVPool, bank: int, q, page_table, seq_len
         _dev(out, torch.bfloat16, "out"), lse_ptr, ctypes.c_void_p(workspace.data_ptr()),
         workspace.numel() * workspace.element_size(), int(split_tokens), int(max_ctas), _stream(stream)),
         "rlt_paged_decode_attn_prefix")
+    return out
+
+
+# ------------------------------------------------------ extend attention
+
+class ExtendPlan:
+    """Host output of rlt_plan_extend; .to(device) uploads it for rlt_paged_extend_attn."""
+
+    def __init__(self, segments, members, member_limit, row_prefix, row_len, sizes, chunk_tiles, query_group):
+        self.segments, self.members, self.member_limit = segments, members, member_limit
+        self.row_prefix, self.row_len = row_prefix, row_len
+        (self.num_segments, self.num_rows, self.max_chunks, self.max_slots, self.max_members, _,
+         self.work_units) = (int(x) for x in sizes)
+        self.chunk_tiles, self.query_group = chunk_tiles, query_group
+        self.dev = None
+
+    def to(self, device):
+        import torch
+        self.dev = [torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(device)
+                    for a in (self.segments, self.members, self.member_limit, self.row_prefix, self.row_len)]
+        return self
+
+
+def rlt_plan_extend(seq_lens, new_lens, page_size: int, chunk_tiles: int = 4, query_group: int = 1) -> ExtendPlan:
+    """Lay out causal extend attention (new_lens[b] last tokens of request b) for the tensor-core kernel."""
+    sl, _ = _host(seq_lens, np.int32)
+    nl, _ = _host(new_lens, np.int32)
+    B = sl.size
+    sizes = np.zeros(7, np.int32)
+    args = lambda seg, mem, lim, rp, rl, ms, mm: (
+        sl.ctypes.data_as(ctypes.c_void_p), nl.ctypes.data_as(ctypes.c_void_p), B, page_size, chunk_tiles,
+        query_group, seg, ms, mem, lim, mm, rp, rl, sizes.ctypes.data_as(ctypes.c_void_p))
+    z = ctypes.c_void_p(0)
+    st = load().rlt_plan_extend(*args(z, z, z, z, z, 0, 0))
+    if st not in (0, 2):
+        _check(st, "rlt_plan_extend")
+    nseg, rows = int(sizes[0]), int(sizes[1])
+    seg = np.zeros((max(nseg, 1), 8), np.int32)
+    mem = np.zeros(max(rows, 1), np.int32)
+    lim = np.zeros(max(rows, 1), np.int32)
+    rp = np.zeros((max(rows, 1), 2), np.int32)
+    rl = np.zeros(max(rows, 1), np.int32)
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    _check(load().rlt_plan_extend(*args(p(seg), p(mem), p(lim), p(rp), p(rl), seg.shape[0], mem.size)),
+           "rlt_plan_extend")
+    return ExtendPlan(seg[:nseg], mem[:rows], lim[:rows], rp[:rows], rl[:rows], sizes, chunk_tiles, query_group)
+
+
+def rlt_paged_extend_attn(pool: KVPool, bank: int, q, page_table, plan: ExtendPlan, out=None, lse_out=None,
+                          workspace=None, scale: float = 0.0, max_ctas: int = 0, stream=None):
+    """Causal extend attention: q/out bf16 [new tokens][Hq][D] packed request by request."""
+    import torch
+    N, Hq, D = q.shape
+    if plan.num_rows != N:
+        raise ValueError("the plan was built for another number of new tokens")
+    if plan.num_segments and plan.query_group != Hq // pool.num_kv_heads:
+        raise ValueError("the plan was built for another query group")
+    if plan.dev is None:
+        plan.to(q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    need = int(load().rlt_paged_extend_workspace_size(N, Hq, D, max(plan.max_slots, 1)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    lse_ptr = _dev(lse_out, torch.float32, "lse_out") if lse_out is not None else ctypes.c_void_p(0)
+    seg, mem, lim, rp, rl = plan.dev
+    _check(load().rlt_paged_extend_attn(
+        ctypes.byref(pool.struct), bank, _dev(q, torch.bfloat16, "q"), Hq, N,
+        _dev(page_table, torch.int32, "page_table"), page_table.shape[1], page_table.shape[0],
+        _dev(seg, torch.int32, "segments"), _dev(mem, torch.int32, "members"), _dev(lim, torch.int32, "member_limit"),
+        _dev(rp, torch.int32, "row_prefix"), _dev(rl, torch.int32, "row_len"), plan.num_segments, plan.work_units,
+        max(plan.max_slots, 1), plan.chunk_tiles, float(scale), _dev(out, torch.bfloat16, "out"), lse_ptr,
+        ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(), int(max_ctas),
+        _stream(stream)), "rlt_paged_extend_attn")
     return out

@@ -380,6 +380,8 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     rlt::PrefixParams pp{};
     pp.segments = segments;
     pp.members = members;
+    pp.member_limit = nullptr;
+    pp.num_rows = batch;
     pp.num_segments = num_segments;
     pp.chunk_tiles = chunk_tiles;
     pp.work_units = work_units;
@@ -420,6 +422,97 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     }
     if (e == cudaSuccess)
         e = rlt::launch_combine(p, pool->head_dim, cs);
+    return from_cuda(e);
+}
+
+RLT_API size_t rlt_paged_extend_workspace_size(int32_t num_rows, int32_t num_q_heads, int32_t head_dim,
+                                               int32_t max_slots)
+{
+    if (num_rows < 0 || num_q_heads < 1 || head_dim < 1 || max_slots < 0)
+        return 0;
+    const size_t n = (size_t)num_rows * num_q_heads * max_slots;
+    return (n * sizeof(float) + 255) / 256 * 256 + n * head_dim * sizeof(float);
+}
+
+RLT_API rlt_status rlt_paged_extend_attn(
+    const rlt_kv_pool *pool, int32_t bank, const void *q, int32_t num_q_heads, int32_t num_rows,
+    const int32_t *page_table, int32_t max_pages, int32_t batch, const int32_t *segments,
+    const int32_t *members, const int32_t *member_limit, const int32_t *row_prefix, const int32_t *row_len,
+    int32_t num_segments, int32_t work_units, int32_t max_slots, int32_t chunk_tiles, float scale, void *out,
+    float *lse_out, void *workspace, size_t workspace_bytes, int32_t max_ctas, void *stream)
+{
+    rlt_status st = check_pool(pool, bank);
+    if (st != RLT_OK)
+        return st;
+    if (num_rows < 0 || batch < 0 || max_pages < 1 || num_q_heads < 1 || num_segments < 0 || work_units < 0 ||
+        max_slots < 0 || chunk_tiles < 1 || max_ctas < 0 || num_q_heads % pool->num_kv_heads != 0 ||
+        !std::isfinite(scale))
+        return RLT_ERR_INVALID_ARG;
+    if (num_rows == 0 || num_segments == 0)
+        return RLT_OK;
+    const int group = num_q_heads / pool->num_kv_heads;
+    if (!rlt::prefix_supported(pool->head_dim, group, pool->page_size) || pool->num_kv_heads > 65535)
+        return RLT_ERR_UNSUPPORTED;
+    if (q == nullptr || page_table == nullptr || out == nullptr || segments == nullptr || members == nullptr ||
+        member_limit == nullptr || row_prefix == nullptr || row_len == nullptr || workspace == nullptr ||
+        max_slots < 1)
+        return RLT_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace))
+        return RLT_ERR_INVALID_ARG;
+    if (workspace_bytes < rlt_paged_extend_workspace_size(num_rows, num_q_heads, pool->head_dim, max_slots))
+        return RLT_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t bank_rows = pool->num_pages * pool->num_kv_heads * (int64_t)pool->page_size;
+    if (bank_rows >= (int64_t(1) << 31))
+        return RLT_ERR_UNSUPPORTED;
+    unsigned int *err = nullptr;
+    int sms = 0;
+    if ((st = device_info(&err, &sms)) != RLT_OK)
+        return st;
+    const size_t n = (size_t)num_rows * num_q_heads * max_slots;
+    rlt::DecodeParams p{};
+    const int64_t off = bank * bank_elems(pool);
+    p.k_bank = static_cast<const uint16_t *>(pool->k) + off;
+    p.v_bank = static_cast<const uint16_t *>(pool->v) + off;
+    p.q = static_cast<const uint16_t *>(q);
+    p.page_table = page_table;
+    p.out = static_cast<uint16_t *>(out);
+    p.lse_out = lse_out;
+    p.lse_part = static_cast<float *>(workspace);
+    p.o_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + (n * sizeof(float) + 255) / 256 * 256);
+    p.err = err;
+    p.num_pages = pool->num_pages;
+    p.num_kv_heads = pool->num_kv_heads;
+    p.num_q_heads = num_q_heads;
+    p.page_size = pool->page_size;
+    p.max_pages = max_pages;
+    p.batch = batch;                     // requests: page-table rows
+    p.tiles_per_split = 1;
+    p.max_splits = 1;
+    const double s = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)pool->head_dim);
+    p.qscale = (float)(s * 1.4426950408889634);
+    p.prefix_slots = max_slots;
+    p.part_stride = max_slots;
+
+    rlt::PrefixParams pp{};
+    pp.segments = segments;
+    pp.members = members;
+    pp.member_limit = member_limit;
+    pp.num_rows = num_rows;
+    pp.num_segments = num_segments;
+    pp.chunk_tiles = chunk_tiles;
+    pp.work_units = work_units;
+    pp.ctas = (int32_t)std::min<int64_t>(max_ctas > 0 ? std::min(max_ctas, sms) : sms,
+                                         (int64_t)pool->num_kv_heads * work_units);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = rlt::launch_prefix(p, pp, p.k_bank, p.v_bank, bank_rows, cs);
+    if (e == cudaSuccess) {
+        // the merge runs over the new tokens: each row's "request" is its causal prefix
+        rlt::DecodeParams pc = p;
+        pc.batch = num_rows;
+        pc.seq_lens = row_len;
+        pc.request_prefix = row_prefix;
+        e = rlt::launch_combine(pc, pool->head_dim, cs);
+    }
     return from_cuda(e);
 }
 

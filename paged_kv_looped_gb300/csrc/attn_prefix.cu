@@ -83,8 +83,9 @@ enum PrefixBar {
 };
 constexpr int kFlagOff = kBarOff + kNumBars * 8;   // TMEM base address, abort flag
 constexpr int kDescOff = (kFlagOff + 16 + 63) / 64 * 64;
-constexpr int kMemOff = kDescOff + kDescs * 64;    // request ids of each descriptor's members
-constexpr int kXMaxOff = kMemOff + kDescs * 128 * 2;   // row maxima [sub-tile parity][column half][row]
+constexpr int kMemOff = kDescOff + kDescs * 64;    // q rows of each descriptor's members
+constexpr int kLimOff = kMemOff + kDescs * 128 * 4;  // their key counts (causal limits)
+constexpr int kXMaxOff = kLimOff + kDescs * 128 * 4;   // row maxima [sub-tile parity][column half][row]
 constexpr int kXSumOff = kXMaxOff + 2 * 2 * 128 * 4;   // row sums [column half][row]
 constexpr int kSmemP = kXSumOff + 2 * 128 * 4 + 1024;
 // TMEM columns: Q[2] (128 rows x 128 bf16, two per column), S/P[2], O
@@ -144,6 +145,8 @@ __device__ __forceinline__ Run decode_run(const PrefixParams &pp, int G, int ite
     const int t_last = sd[kSegFirstTile] + min(num_tiles, (chunk0 + r.d.nchunks) * pp.chunk_tiles);
     r.d.tok_begin = (int64_t)t_first * kPrefixTile;
     r.d.tok_end = min((int64_t)t_last * kPrefixTile, (int64_t)sd[kSegEndToken]);
+    if (pp.member_limit != nullptr && r.d.n_mem > 0)   // extend: no key past the block's last query
+        r.d.tok_end = min(r.d.tok_end, (int64_t)pp.member_limit[r.member_begin + r.d.n_mem - 1]);
     r.d.nsub = (r.d.n_mem > 0 && r.d.tok_end > r.d.tok_begin)
                    ? (int)((r.d.tok_end - r.d.tok_begin + kSub - 1) / kSub) : 0;
     r.next_item = item + max(1, r.d.nchunks);
@@ -168,16 +171,18 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
     return __all_sync(kFullMask, mbar_wait_or_abort(bar, parity, abort));
 }
 
-// Copy run descriptor r (and, for mrow >= 0, the request id of member mrow) and release
-// its slot.  Warp-collective; false if the wait gave up.
+// Copy run descriptor r (and, for mrow >= 0, the q row and key count of member mrow) and
+// release its slot.  Warp-collective; false if the wait gave up.
 __device__ __forceinline__ bool take_desc(uint64_t *bars, const unsigned char *base, int r, RunDesc &out,
-                                          int mrow, int &member, const volatile int *abort, int lane)
+                                          int mrow, int &member, int &limit, const volatile int *abort, int lane)
 {
     if (!warp_wait(&bars[kBarDescFull + r % kDescs], (r / kDescs) & 1u, abort))
         return false;
     out = reinterpret_cast<const RunDesc *>(base + kDescOff)[r % kDescs];
-    if (mrow >= 0 && mrow < out.n_mem)
-        member = reinterpret_cast<const uint16_t *>(base + kMemOff)[(r % kDescs) * 128 + mrow];
+    if (mrow >= 0 && mrow < out.n_mem) {
+        member = reinterpret_cast<const int32_t *>(base + kMemOff)[(r % kDescs) * 128 + mrow];
+        limit = reinterpret_cast<const int32_t *>(base + kLimOff)[(r % kDescs) * 128 + mrow];
+    }
     __syncwarp();
     if (lane == 0)
         mbar_arrive(&bars[kBarDescFree + r % kDescs]);
@@ -277,7 +282,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // ---------------------------------------------------------- scheduler
         // Publishes descriptor d once every consumer has copied descriptor d - kDescs.
         RunDesc *descs = reinterpret_cast<RunDesc *>(base + kDescOff);
-        uint16_t *dmem = reinterpret_cast<uint16_t *>(base + kMemOff);
+        int32_t *dmem = reinterpret_cast<int32_t *>(base + kMemOff);
+        int32_t *dlim = reinterpret_cast<int32_t *>(base + kLimOff);
         int item = item_begin;
         for (int d = 0;; ++d) {
             if (d >= kDescs &&
@@ -291,11 +297,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 descs[d % kDescs] = r.d;
             for (int i = lane; has && i < r.d.n_mem; i += 32) {
                 int b = pp.members[r.member_begin + i];
-                if (b < 0 || b >= p.batch) {
+                if (b < 0 || b >= pp.num_rows) {
                     record_error(p.err, RLT_DEVERR_BAD_SLOT);
                     b = 0;
                 }
-                dmem[(d % kDescs) * 128 + i] = (uint16_t)b;
+                dmem[(d % kDescs) * 128 + i] = b;
+                dlim[(d % kDescs) * 128 + i] =
+                    pp.member_limit != nullptr ? pp.member_limit[r.member_begin + i] : INT32_MAX;
             }
             __syncwarp();
             if (lane == 0)
@@ -339,7 +347,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         };
         int n = 0, r = 0, j = 0;                 // sub-tiles issued; current run and sub-tile
         RunDesc cur;
-        ok = take_desc(bars, base, r, cur, -1, unused, abort_flag, lane);
+        ok = take_desc(bars, base, r, cur, -1, unused, unused, abort_flag, lane);
         int row_next = ok && cur.nsub > 0 ? lane_row(cur, 0) : -1;
         while (ok && cur.nsub > 0) {
             const int row = row_next;
@@ -348,7 +356,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 row_next = lane_row(cur, ++j);
             } else {
                 j = 0;
-                if (!(ok = take_desc(bars, base, ++r, cur, -1, unused, abort_flag, lane)))
+                if (!(ok = take_desc(bars, base, ++r, cur, -1, unused, unused, abort_flag, lane)))
                     break;
                 if (cur.nsub > 0)
                     row_next = lane_row(cur, 0);
@@ -498,7 +506,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         uint64_t *pair = &bars[kBarPair + quarter];
         int n = 0, meets = 0;
         RunDesc rd, rn;
-        int b_row = 0, b_next = 0;
+        int b_row = 0, b_next = 0, lim_row = INT32_MAX, lim_next = INT32_MAX;
         // the run whose epilogue is pending
         RunDesc ed{};
         int e_b = 0, e_last = -1;
@@ -516,7 +524,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 if (!pair_sync(pair, meets, abort_flag, lane))
                     return false;
                 l_tot = e_l + xsum[(half ^ 1) * 128 + row];
-                const float inv = 1.f / l_tot;
+                const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;   // a row with no key: o = 0
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     float o[32];
@@ -535,7 +543,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (lane == 0)
                 mbar_arrive(&bars[kBarOFree]);
             if (live && half == 0 && row < R) {
-                p.lse_part[slot] = e_m + log2f(l_tot);
+                p.lse_part[slot] = l_tot > 0.f ? e_m + log2f(l_tot) : -CUDART_INF_F;
                 for (int k = 1; k < ed.nchunks; ++k)   // chunks merged into this run's partial
                     p.lse_part[slot + k] = -CUDART_INF_F;
             }
@@ -544,14 +552,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
         };
 
         uint32_t qw[32];
-        ok = take_desc(bars, base, 0, rd, row / G, b_row, abort_flag, lane);
+        ok = take_desc(bars, base, 0, rd, row / G, b_row, lim_row, abort_flag, lane);
         if (ok && rd.nsub > 0) {
             load_q(p, rd, G, row, b_row, half, qw);
             store_q(qw, half, t_lane + kColQ, &bars[kBarQFull], lane);
         }
         for (int r = 0; ok && rd.nsub > 0; ++r) {
             // the next run's Q rows, loaded while this run's first S is computed
-            if (!(ok = take_desc(bars, base, r + 1, rn, row / G, b_next, abort_flag, lane)))
+            if (!(ok = take_desc(bars, base, r + 1, rn, row / G, b_next, lim_next, abort_flag, lane)))
                 break;
             load_q(p, rn, G, row, b_next, half, qw);
             const int R = rd.n_mem * G;
@@ -567,8 +575,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const uint32_t t_s = t_lane + kColS + (n % kSBufs) * kSub;
                 if (live) {
                     tc::fence_after_sync();
-                    const int valid = (int)min((int64_t)kSub, rd.tok_end - (rd.tok_begin + (int64_t)j * kSub)) -
+                    const int64_t sub_begin = rd.tok_begin + (int64_t)j * kSub;
+                    const int valid = (int)min((int64_t)kSub, rd.tok_end - sub_begin) -
                                       half * 64;       // valid columns of this warp's half
+                    // this row's own end (extend: its causal limit)
+                    const int row_valid = (int)max(min((int64_t)valid, (int64_t)lim_row - sub_begin - half * 64),
+                                                   (int64_t)-1);
                     if (valid + half * 64 < kSub && warp == 0) {
                         // ragged end of a private tail: zero the V rows past it, whose memory may
                         // hold anything (0 * NaN would poison O), once this V copy has landed
@@ -587,7 +599,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     float mx = -CUDART_INF_F;
 #pragma unroll
                     for (int i = 0; i < 64; ++i)
-                        if (i < valid)
+                        if (i < row_valid)
                             mx = fmaxf(mx, v[i]);
                     // the row max over both halves of the sub-tile
                     xmax[((n & 1) * 2 + half) * 128 + row] = mx;
@@ -596,7 +608,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     mx = fmaxf(mx, xmax[((n & 1) * 2 + (half ^ 1)) * 128 + row]) * p.qscale;
                     const bool up = mx > m_ref + kRescaleThreshold;
                     const float m_next = up ? mx : m_ref;   // rows >= R hold garbage and are never stored
-                    const float scale_o = exp2f(m_ref - m_next);   // 1 if the reference stays, 0 at first
+                    // 1 if the reference stays, 0 at first; 1 while a row has seen no key at all
+                    const float scale_o = m_next == -CUDART_INF_F ? 1.f : exp2f(m_ref - m_next);
                     if (__any_sync(kFullMask, up) && j > 0) {
                         // rescale this warp's half of the row's O (P.V of the previous sub-tile landed)
                         if (!(ok = warp_wait(&bars[kBarPvDone + (n - 1) % kSBufs], ((n - 1) / kSBufs) & 1u,
@@ -620,8 +633,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     uint32_t w[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float p0 = 2 * i < valid ? fast_exp2(fmaf(v[2 * i], p.qscale, -m_ref)) : 0.f;
-                        const float p1 = 2 * i + 1 < valid ? fast_exp2(fmaf(v[2 * i + 1], p.qscale, -m_ref)) : 0.f;
+                        const float p0 = 2 * i < row_valid ? fast_exp2(fmaf(v[2 * i], p.qscale, -m_ref)) : 0.f;
+                        const float p1 =
+                            2 * i + 1 < row_valid ? fast_exp2(fmaf(v[2 * i + 1], p.qscale, -m_ref)) : 0.f;
                         lsum += p0 + p1;
                         w[i] = cvt_bf16x2(p0, p1);
                     }
@@ -648,6 +662,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             e_last = n - 1;
             rd = rn;
             b_row = b_next;
+            lim_row = lim_next;
         }
         if (ok && e_last >= 0)
             ok = epilogue();
@@ -887,6 +902,95 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
         row[rlt::kSegWorkBegin] = (int32_t)work_begin[s];
         for (int b : segs[s].mem)
             members[m++] = b;
+    }
+    return RLT_OK;
+}
+
+// ------------------------------------------------------ extend planner
+
+// Work of a causal extend (span) attention for the tensor-core kernel: one
+// segment per request with new tokens, covering its whole key range, whose
+// "members" are its new tokens (rows of the packed q, request by request) with
+// their causal key counts.  Each member block (128 / query_group new tokens)
+// needs keys only up to its last token's limit; its rows' partial slots are
+// the chunks up to there (row_prefix[row] = {limit, slots}, row_len[row] =
+// limit), so the combine merges exactly what the kernel wrote.
+extern "C" RLT_API rlt_status rlt_plan_extend(const int32_t *seq_lens, const int32_t *new_lens,
+                                              int32_t batch, int32_t page_size, int32_t chunk_tiles,
+                                              int32_t query_group, int32_t *segments, int32_t max_segments,
+                                              int32_t *members, int32_t *member_limit,
+                                              int32_t max_member_entries, int32_t *row_prefix,
+                                              int32_t *row_len, int32_t *sizes)
+{
+    using rlt::kPrefixTile;
+    if (batch < 0 || page_size < 1 || chunk_tiles < 1 || chunk_tiles > rlt::kMaxChunkTiles ||
+        query_group < 1 || query_group > 128 || 128 % query_group != 0 || max_segments < 0 ||
+        max_member_entries < 0 || sizes == nullptr ||
+        (batch > 0 && (seq_lens == nullptr || new_lens == nullptr)))
+        return RLT_ERR_INVALID_ARG;
+    if (kPrefixTile % page_size != 0 && page_size % kPrefixTile != 0)
+        return RLT_ERR_UNSUPPORTED;
+    const int per_block = 128 / query_group;
+    const int64_t chunk_tokens = (int64_t)chunk_tiles * kPrefixTile;
+    int64_t nseg = 0, rows = 0, units = 0;
+    int max_chunks = 0, max_members = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int64_t L = seq_lens[b], n = new_lens[b];
+        if (n < 0 || L < n || L > INT32_MAX)
+            return RLT_ERR_INVALID_ARG;
+        if (n == 0)
+            continue;
+        const int tiles = (int)((L + kPrefixTile - 1) / kPrefixTile);
+        const int chunks = (tiles + chunk_tiles - 1) / chunk_tiles;
+        ++nseg;
+        rows += n;
+        units += (int64_t)chunks * ((n + per_block - 1) / per_block);
+        max_chunks = std::max(max_chunks, chunks);
+        max_members = std::max(max_members, (int)n);
+    }
+    if (rows > INT32_MAX || units > INT32_MAX)
+        return RLT_ERR_OUT_OF_RANGE;
+    sizes[0] = (int32_t)nseg;
+    sizes[1] = (int32_t)rows;
+    sizes[2] = max_chunks;
+    sizes[3] = max_chunks;            // partial slots per row: every chunk of the longest key range
+    sizes[4] = max_members;
+    sizes[5] = 0;                     // no split-K rest
+    sizes[6] = (int32_t)units;
+    if (nseg > max_segments || rows > max_member_entries)
+        return RLT_ERR_OUT_OF_RANGE;  // sizes[] tells the caller what is needed
+    if (nseg > 0 && (segments == nullptr || members == nullptr || member_limit == nullptr ||
+                     row_prefix == nullptr || row_len == nullptr))
+        return RLT_ERR_INVALID_ARG;
+    int64_t s = 0, m = 0, work = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int64_t L = seq_lens[b], n = new_lens[b];
+        if (n == 0)
+            continue;
+        const int tiles = (int)((L + kPrefixTile - 1) / kPrefixTile);
+        const int chunks = (tiles + chunk_tiles - 1) / chunk_tiles;
+        int32_t *row = segments + s * rlt::kSegFields;
+        row[rlt::kSegFirstTile] = 0;
+        row[rlt::kSegNumTiles] = tiles;
+        row[rlt::kSegSlotBase] = 0;
+        row[rlt::kSegMemberBegin] = (int32_t)m;
+        row[rlt::kSegMemberCount] = (int32_t)n;
+        row[rlt::kSegPageRow] = b;
+        row[rlt::kSegEndToken] = (int32_t)L;
+        row[rlt::kSegWorkBegin] = (int32_t)work;
+        for (int64_t i = 0; i < n; ++i) {
+            const int64_t limit = L - n + i + 1;
+            const int64_t last = std::min(n, (i / per_block + 1) * per_block) - 1;   // block's last token
+            const int64_t block_end = L - n + last + 1;
+            members[m + i] = (int32_t)(m + i);                 // packed q row of this new token
+            member_limit[m + i] = (int32_t)limit;
+            row_prefix[2 * (m + i)] = (int32_t)limit;
+            row_prefix[2 * (m + i) + 1] = (int32_t)((block_end + chunk_tokens - 1) / chunk_tokens);
+            row_len[m + i] = (int32_t)limit;
+        }
+        work += (int64_t)chunks * ((n + per_block - 1) / per_block);
+        m += n;
+        ++s;
     }
     return RLT_OK;
 }

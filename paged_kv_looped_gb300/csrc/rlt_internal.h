@@ -46,7 +46,9 @@ enum PrefixSegField { kSegFirstTile = 0, kSegNumTiles, kSegSlotBase, kSegMemberB
 
 struct PrefixParams {
     const int32_t *segments;     // [num_segments][kSegFields]
-    const int32_t *members;      // request ids, grouped by segment
+    const int32_t *members;      // query rows (request ids; new-token ids for extend), grouped by segment
+    const int32_t *member_limit; // extend: each member's key count (causal limit); null: every key
+    int32_t num_rows;            // rows of q: members lie in [0, num_rows)
     int32_t num_segments;
     int32_t chunk_tiles;         // 128-token tiles per CTA
     int32_t work_units;          // (segment, member block, chunk) units per kv head

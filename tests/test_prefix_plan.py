@@ -149,3 +149,37 @@ def test_private_tails_cover_every_token(name):
         assert (first + ntiles) * TILE >= end > (first + ntiles - 1) * TILE
         assert base == shared.request_prefix[b, 1]
         assert plan.request_prefix[b, 1] == base + -(-ntiles // 4)
+
+
+@pytest.mark.parametrize("G,chunk_tiles", [(1, 1), (4, 2), (8, 3)])
+def test_extend_plan_by_brute_force(G, chunk_tiles):
+    lens = [300, 50, 1000, 128, 129, 7]
+    new = [40, 50, 0, 128, 1, 7]
+    plan = rlt.rlt_plan_extend(lens, new, 16, chunk_tiles, G)
+    per_block = 128 // G
+    ct = chunk_tiles * TILE
+    assert plan.num_rows == sum(new) and plan.num_segments == sum(1 for n in new if n)
+    row, units, s = 0, 0, 0
+    for b, (L, n) in enumerate(zip(lens, new)):
+        if n == 0:
+            continue
+        first, tiles, base, mb, mc, page_row, end, work = plan.segments[s]
+        assert (first, tiles, base, mc, page_row, end, work) == (0, -(-L // TILE), 0, n, b, L, units)
+        assert mb == row
+        for i in range(n):
+            assert plan.members[row + i] == row + i                     # packed q row of the token
+            assert plan.member_limit[row + i] == L - n + i + 1          # causal key count
+            assert plan.row_len[row + i] == L - n + i + 1
+            block_last = min(n, (i // per_block + 1) * per_block) - 1
+            assert plan.row_prefix[row + i, 0] == L - n + i + 1
+            assert plan.row_prefix[row + i, 1] == -(-(L - n + block_last + 1) // ct)
+        units += -(-tiles // chunk_tiles) * -(-n // per_block)
+        row += n
+        s += 1
+    assert plan.work_units == units
+    assert plan.max_slots == max(-(-(-(-L // TILE)) // chunk_tiles) for L, n in zip(lens, new) if n)
+
+
+def test_extend_plan_rejects_more_new_tokens_than_the_sequence():
+    with pytest.raises(rlt.RltError):
+        rlt.rlt_plan_extend([10], [11], 16)
