@@ -143,6 +143,15 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def bf16_peak() -> float:
+    """Measured dense bf16 TFLOP/s of the GB300s (burst), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return 1900.0
+
+
 def profiled_traffic(workload: str, cascade: bool):
     """Per-launch DRAM bytes of the call's dominant kernel from the committed ncu summary,
     if it was taken on this workload and on the kernel's current source."""
@@ -349,6 +358,36 @@ def run_gpu(args, rank, world):
     attn_timing = "CUDA-graph event nodes" if timed_graph is not None else "eager event pairs"
     assert rlt.rlt_get_device_error() == 0
 
+    # ---- extend (span) attention, when asked: N new tokens per request attend causally over
+    # their request's cached keys (a LOTUS block re-forward / packed prefill chunk), per bank
+    extend = None
+    if args.extend > 0:
+        new = np.minimum(case.seq_lens, args.extend).astype(np.int32)
+        eplan = rlt.rlt_plan_extend(case.seq_lens, new, case.page_size, max(1, args.chunk_tiles or 2),
+                                    case.group).to(dev)
+        qx = torch.randn((int(new.sum()), Hq, D), device=dev).to(torch.bfloat16)
+        ox = torch.empty_like(qx)
+        wsx = torch.empty(max(16, int(rlt.load().rlt_paged_extend_workspace_size(
+            int(new.sum()), Hq, D, max(eplan.max_slots, 1)))), dtype=torch.uint8, device=dev)
+        for i, bank in enumerate(banks[: args.warmup]):
+            rlt.rlt_paged_extend_attn(pool, bank, qx, pt, eplan, out=ox, workspace=wsx, stream=stream)
+        ev = []
+        for i, bank in enumerate(banks):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            rlt.rlt_paged_extend_attn(pool, bank, qx, pt, eplan, out=ox, workspace=wsx, stream=stream)
+            e1.record(stream)
+            ev.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        assert rlt.rlt_get_device_error() == 0
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        keys = sum(int(L) - int(n) + i + 1 for L, n in zip(case.seq_lens, new) for i in range(int(n)))
+        flops = 4.0 * D * Hq * keys                       # QK^T and PV, 2 flops per multiply-add
+        extend = {"new_tokens_per_request": args.extend, "us_per_call": round(ms * 1e3, 2),
+                  "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+                  "frac_of_bf16_peak": round(flops / (ms * 1e-3) / 1e12 / bf16_peak(), 4),
+                  "kv_gbs": round(attn_bytes(case) / (ms * 1e-3) / 1e9, 1)}
+
     # ---- end to end: this step's inputs from pinned host memory, outputs back to the host
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -393,6 +432,7 @@ def run_gpu(args, rank, world):
     combine = ws_bytes > 0
     launches = args.steps * (len(banks) * per_lp + (1 if nz is not None else 0))
     return dict(case=case, banks=banks, cascade=plan is not None, graph=graph is not None, attn_timing=attn_timing,
+                extend=extend,
                 ms_total=ms_total, attn_ms=attn_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                 clocks=clocks.summary(), launches=launches, combine=combine, ws_bytes=ws_bytes)
 
@@ -514,6 +554,8 @@ def main():
                          "tensor-core kernel (auto: when a kv head serves >= 8 query heads)")
     ap.add_argument("--graph", default="on", choices=["on", "off"],
                     help="submit each decode step as one captured CUDA graph (on) or as eager launches")
+    ap.add_argument("--extend", type=int, default=0,
+                    help="also time causal extend attention with this many new tokens per request (0: off)")
     ap.add_argument("--append", default="plain", choices=["plain", "rope"],
                     help="store_kv as given (plain) or with RoPE fused on the keys and written-prefix counters")
     ap.add_argument("--prefix-ctas", type=int, default=0,
@@ -576,6 +618,7 @@ def main():
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"],
+        **({"extend_attention": r["extend"]} if r["extend"] else {}),
         "clocks": r["clocks"],
     }
     print(json.dumps(line))
