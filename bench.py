@@ -245,7 +245,7 @@ def run_gpu(args, rank, world):
         ws_bytes = rlt.rlt_paged_decode_prefix_workspace_size(B, Hq, Hkv, D, plan.max_rest_len,
                                                               plan.max_prefix_slots, args.split_tokens)
         plan_h = [torch.from_numpy(np.ascontiguousarray(a, np.int32).reshape(-1)).pin_memory()
-                  for a in (plan.segments, plan.members, plan.request_prefix)]
+                  for a in (plan.segments, plan.members, plan.member_limit, plan.request_prefix)]
     else:
         ws_bytes = rlt.rlt_paged_decode_workspace_size(B, Hq, Hkv, D, case.max_seq_len, args.split_tokens)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
@@ -400,7 +400,7 @@ def run_gpu(args, rank, world):
             # a captured step stays valid while the plan's shape (grid, slots) is unchanged
             assert graph is None or (p2.num_segments, p2.work_units, p2.max_prefix_slots, p2.max_rest_len) == \
                 (plan.num_segments, plan.work_units, plan.max_prefix_slots, plan.max_rest_len)
-            for host, arr, devt in zip(plan_h, (p2.segments, p2.members, p2.request_prefix), plan.dev):
+            for host, arr, devt in zip(plan_h, (p2.segments, p2.members, p2.member_limit, p2.request_prefix), plan.dev):
                 host.numpy()[:] = np.ascontiguousarray(arr, np.int32).reshape(-1)
                 devt.copy_(host, non_blocking=True)
         q.copy_(q_h, non_blocking=True)

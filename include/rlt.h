@@ -214,8 +214,11 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
  * physical pages).  From host copies of a decode batch's page tables it finds
  * the 128-token tiles that several requests map to identical pages, walking a
  * trie of tiles from position 0, and groups them into segments: runs of tiles
- * shared by one fixed set of requests.  Along each request's path the
- * segments' partial slots are numbered from 0.
+ * shared by one set of requests.  A chain of trie runs whose member set only
+ * shrinks (requests leaving one common prompt one after another) is one
+ * segment when its members fit one member block: each member carries its key
+ * limit, the number of leading tokens it shares, and reads no key past it.
+ * Along each request's path the segments' partial slots are numbered from 0.
  *   chunk_tiles     tiles per CTA of the tensor-core prefix kernel (1..32)
  *   query_group     num_q_heads / num_kv_heads of the attention it plans for
  *                   (a CTA holds 128 query rows, so 128 / query_group members)
@@ -226,10 +229,15 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
  *                   query rows a dense enough contraction
  *   segments        int32 [max_segments][8]: first tile, number of tiles,
  *                   first partial slot, first member entry, member count,
- *                   a member whose page-table row holds the segment's pages,
+ *                   a member whose page-table row holds the segment's pages
+ *                   (the one with the largest limit),
  *                   end token (exclusive; a private tail may end mid-tile),
  *                   first work unit (CTA) of the segment
- *   members         int32 [max_member_entries]: request ids by segment
+ *   members         int32 [max_member_entries]: request ids by segment, in
+ *                   ascending order of their limits
+ *   member_limit    int32 [max_member_entries]: each member's key limit
+ *                   (exclusive end token of what it shares in the segment; the
+ *                   segment's end token for all members of an unmerged one)
  *   request_prefix  int32 [batch][2]: tokens of request b covered by its
  *                   segments (a multiple of 128 unless a private tail
  *                   covers all of it), partial slots they use
@@ -246,8 +254,8 @@ RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t max_pages,
                                    const int32_t *seq_lens, int32_t batch, int32_t page_size,
                                    int32_t chunk_tiles, int32_t query_group, int32_t private_tails,
                                    int32_t *segments, int32_t max_segments, int32_t *members,
-                                   int32_t max_member_entries, int32_t *request_prefix,
-                                   int32_t *sizes);
+                                   int32_t *member_limit, int32_t max_member_entries,
+                                   int32_t *request_prefix, int32_t *sizes);
 
 /* Device workspace bytes of rlt_paged_decode_attn_prefix (sizes[5] and sizes[3]
  * of the plan as max_rest_len and max_prefix_slots). */
@@ -259,7 +267,7 @@ RLT_API size_t rlt_paged_decode_prefix_workspace_size(int32_t batch, int32_t num
 /*
  * Paged decode attention with shared prefixes read once ("cascade"): the same
  * result as rlt_paged_decode_attn, up to fp32 rounding order.  The plan's
- * arrays (segments, members, request_prefix: DEVICE copies of
+ * arrays (segments, members, member_limit, request_prefix: DEVICE copies of
  * rlt_plan_prefix's output) name the tiles several requests share; each is
  * read from HBM once per kv head and applied to every member's queries by a
  * tcgen05 tensor-core kernel (S = Q K^T, O = P V with the members' query rows
@@ -284,7 +292,7 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     const rlt_kv_pool *pool, int32_t bank, const void *q, int32_t num_q_heads,
     const int32_t *page_table, int32_t max_pages, const int32_t *seq_lens, int32_t batch,
     int32_t max_seq_len, const int32_t *segments, const int32_t *members,
-    const int32_t *request_prefix, int32_t num_segments, int32_t work_units,
+    const int32_t *member_limit, const int32_t *request_prefix, int32_t num_segments, int32_t work_units,
     int32_t max_prefix_slots, int32_t chunk_tiles, int32_t max_rest_len, float scale, void *out,
     float *lse_out, void *workspace, size_t workspace_bytes, int32_t split_tokens, int32_t max_ctas,
     void *stream);

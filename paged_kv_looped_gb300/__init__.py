@@ -85,9 +85,9 @@ def load():
         "rlt_paged_decode_attn_noalloc": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, P, i32, i32, f32, P, P,
                                                          i32, P]),
         "rlt_validate_batch": (ctypes.c_int, [P, i32, P, i32, P, i64, i32]),
-        "rlt_plan_prefix": (ctypes.c_int, [P, i32, P, i32, i32, i32, i32, i32, P, i32, P, i32, P, P]),
+        "rlt_plan_prefix": (ctypes.c_int, [P, i32, P, i32, i32, i32, i32, i32, P, i32, P, P, i32, P, P]),
         "rlt_paged_decode_prefix_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, i32]),
-        "rlt_paged_decode_attn_prefix": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, P, i32, i32, P, P, P, i32,
+        "rlt_paged_decode_attn_prefix": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, P, i32, i32, P, P, P, P, i32,
                                                         i32, i32, i32, i32, f32, P, P, P, sz, i32, i32, P]),
         "rlt_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
         "rlt_kv_append_rope": (ctypes.c_int, [pool_p, i32, P, P, P, P, i32, i32, ctypes.c_double, P, P, i32, P]),
@@ -346,9 +346,10 @@ SEG_FIELDS = 8
 class PrefixPlan:
     """Host result of rlt_plan_prefix plus (after ``.to(device)``) its device copies."""
 
-    def __init__(self, segments, members, request_prefix, sizes, chunk_tiles, query_group):
-        self.segments = segments            # int32 [n][6]
-        self.members = members              # int32 [entries]
+    def __init__(self, segments, members, member_limit, request_prefix, sizes, chunk_tiles, query_group):
+        self.segments = segments            # int32 [n][8]
+        self.members = members              # int32 [entries], ascending limits within a segment
+        self.member_limit = member_limit    # int32 [entries]: tokens each member shares in its segment
         self.request_prefix = request_prefix  # int32 [B][2]
         self.num_segments, self.member_entries, self.max_chunks, self.max_prefix_slots, \
             self.max_members, self.max_rest_len, self.work_units = (int(x) for x in sizes)
@@ -361,7 +362,7 @@ class PrefixPlan:
         def t(a):
             a = np.ascontiguousarray(a, np.int32).reshape(-1)
             return torch.from_numpy(a if a.size else np.zeros(1, np.int32)).to(device)
-        self.dev = (t(self.segments), t(self.members), t(self.request_prefix))
+        self.dev = (t(self.segments), t(self.members), t(self.member_limit), t(self.request_prefix))
         return self
 
 
@@ -379,20 +380,22 @@ def rlt_plan_prefix(page_table, seq_lens, page_size: int, chunk_tiles: int = 4,
     null = ctypes.c_void_p(0)
     tails = 1 if private_tails else 0
     st = lib.rlt_plan_prefix(ptp, pt.shape[1], slp, B, page_size, chunk_tiles, query_group, tails, null, 0,
-                             null, 0,
+                             null, null, 0,
                              req.ctypes.data_as(ctypes.c_void_p), sizes.ctypes.data_as(ctypes.c_void_p))
     if st not in (0, 2):
         raise RltError(st, "rlt_plan_prefix")
     seg = np.zeros((max(int(sizes[0]), 1), SEG_FIELDS), np.int32)
     mem = np.zeros(max(int(sizes[1]), 1), np.int32)
+    lim = np.zeros(max(int(sizes[1]), 1), np.int32)
     if st == 2:
         _check(lib.rlt_plan_prefix(ptp, pt.shape[1], slp, B, page_size, chunk_tiles, query_group, tails,
                                    seg.ctypes.data_as(ctypes.c_void_p), seg.shape[0],
-                                   mem.ctypes.data_as(ctypes.c_void_p), mem.size,
+                                   mem.ctypes.data_as(ctypes.c_void_p), lim.ctypes.data_as(ctypes.c_void_p),
+                                   mem.size,
                                    req.ctypes.data_as(ctypes.c_void_p), sizes.ctypes.data_as(ctypes.c_void_p)),
                "rlt_plan_prefix")
     n = int(sizes[0])
-    return PrefixPlan(seg[:n], mem[: int(sizes[1])], req, sizes, chunk_tiles, query_group)
+    return PrefixPlan(seg[:n], mem[: int(sizes[1])], lim[: int(sizes[1])], req, sizes, chunk_tiles, query_group)
 
 
 def rlt_paged_decode_prefix_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_rest_len,
@@ -419,13 +422,13 @@ def rlt_paged_decode_attn_prefix(pool: KVPool, bank: int, q, page_table, seq_len
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     lse_ptr = _dev(lse_out, torch.float32, "lse_out") if lse_out is not None else ctypes.c_void_p(0)
-    seg, mem, req = plan.dev
+    seg, mem, lim, req = plan.dev
     _check(load().rlt_paged_decode_attn_prefix(
         ctypes.byref(pool.struct), bank, _dev(q, torch.bfloat16, "q"), Hq,
         _dev(page_table, torch.int32, "page_table"), page_table.shape[1],
         _dev(seq_lens, torch.int32, "seq_lens"), B, int(max_seq_len),
         _dev(seg, torch.int32, "segments"), _dev(mem, torch.int32, "members"),
-        _dev(req, torch.int32, "request_prefix"), plan.num_segments, plan.work_units,
+        _dev(lim, torch.int32, "member_limit"), _dev(req, torch.int32, "request_prefix"), plan.num_segments, plan.work_units,
         plan.max_prefix_slots, plan.chunk_tiles, rest, float(scale),
         _dev(out, torch.bfloat16, "out"), lse_ptr, ctypes.c_void_p(workspace.data_ptr()),
         workspace.numel() * workspace.element_size(), int(split_tokens), int(max_ctas), _stream(stream)),

@@ -304,7 +304,7 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     const rlt_kv_pool *pool, int32_t bank, const void *q, int32_t num_q_heads,
     const int32_t *page_table, int32_t max_pages, const int32_t *seq_lens, int32_t batch,
     int32_t max_seq_len, const int32_t *segments, const int32_t *members,
-    const int32_t *request_prefix, int32_t num_segments, int32_t work_units,
+    const int32_t *member_limit, const int32_t *request_prefix, int32_t num_segments, int32_t work_units,
     int32_t max_prefix_slots, int32_t chunk_tiles, int32_t max_rest_len, float scale, void *out,
     float *lse_out, void *workspace, size_t workspace_bytes, int32_t split_tokens, int32_t max_ctas,
     void *stream)
@@ -330,7 +330,8 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
         pool->num_kv_heads > 65535)
         return RLT_ERR_UNSUPPORTED;
     if (q == nullptr || page_table == nullptr || seq_lens == nullptr || out == nullptr ||
-        segments == nullptr || members == nullptr || request_prefix == nullptr || workspace == nullptr)
+        segments == nullptr || members == nullptr || member_limit == nullptr || request_prefix == nullptr ||
+        workspace == nullptr)
         return RLT_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || !std::isfinite(scale))
         return RLT_ERR_INVALID_ARG;
@@ -380,7 +381,7 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     rlt::PrefixParams pp{};
     pp.segments = segments;
     pp.members = members;
-    pp.member_limit = nullptr;
+    pp.member_limit = member_limit;
     pp.num_rows = batch;
     pp.num_segments = num_segments;
     pp.chunk_tiles = chunk_tiles;

@@ -452,8 +452,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
         return bh * p.part_stride + (s < n_pre ? s : p.prefix_slots + (s - n_pre));
     };
 
-    float M = -CUDART_INF_F;
-    for (int s = threadIdx.x; s < total; s += kCombineWarps * 32)
+    // Pass 1: the slots' log2-sum-exps; thread t keeps slot t (the common case of at
+    // most 128 slots reads them once) and the block maximum.
+    const float l_own = threadIdx.x < total ? p.lse_part[slot_of(threadIdx.x)] : -CUDART_INF_F;
+    float M = l_own;
+    for (int s = threadIdx.x + kCombineWarps * 32; s < total; s += kCombineWarps * 32)
         M = fmaxf(M, p.lse_part[slot_of(s)]);
     M = warp_max_xor(M, 1);
     if (lane == 0)
@@ -468,45 +471,46 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     for (int d = 0; d < DPL; ++d)
         acc[d] = 0.f;
     float ls = 0.f;
-    auto add = [&](int64_t slot, float lse) {
-        const float w = exp2f(lse - M);
-        ls += w;
-        const float *op = p.o_part + slot * D + lane * DPL;
-        if constexpr (DPL == 4) {
-            const float4 o = *reinterpret_cast<const float4 *>(op);
-            acc[0] = fmaf(w, o.x, acc[0]);
-            acc[1] = fmaf(w, o.y, acc[1]);
-            acc[2] = fmaf(w, o.z, acc[2]);
-            acc[3] = fmaf(w, o.w, acc[3]);
-        } else {
-            const float2 o = *reinterpret_cast<const float2 *>(op);
-            acc[0] = fmaf(w, o.x, acc[0]);
-            acc[1] = fmaf(w, o.y, acc[1]);
-        }
-    };
     if (M != -CUDART_INF_F) {
-        // Warps take 32-slot blocks in turn: one coalesced read of the block's lse values,
-        // then only the slots that hold a partial (finite lse; a tensor-core run marks the
-        // chunk slots it merged with -inf) are read, two at a time.
+        // Pass 2: warps take 32-slot blocks in turn; the live slots of a block (finite
+        // lse; a tensor-core run marks the chunk slots it merged with -inf, and a slot
+        // without a partial may hold anything) are read 8 at a time, all 8 loads in
+        // flight before the first is used.
         for (int s0 = warp * 32; s0 < total; s0 += kCombineWarps * 32) {
             const int s = s0 + lane;
-            const float l = s < total ? p.lse_part[slot_of(s)] : -CUDART_INF_F;
-            unsigned int live = __ballot_sync(kFullMask, l != -CUDART_INF_F);
-            while (live != 0u) {
-                const int k0 = __ffs(live) - 1;
-                live &= live - 1u;
-                const float l0 = __shfl_sync(kFullMask, l, k0);
-                if (live != 0u) {
-                    const int k1 = __ffs(live) - 1;
-                    live &= live - 1u;
-                    const float l1 = __shfl_sync(kFullMask, l, k1);
-                    add(slot_of(s0 + k0), l0);
-                    add(slot_of(s0 + k1), l1);
-                } else {
-                    add(slot_of(s0 + k0), l0);
+            const float l = s0 == warp * 32 ? l_own : (s < total ? p.lse_part[slot_of(s)] : -CUDART_INF_F);
+            const float wgt = l != -CUDART_INF_F ? exp2f(l - M) : 0.f;
+            ls += wgt;
+            const int nblk = min(32, total - s0);
+            for (int k0 = 0; k0 < nblk; k0 += 8) {
+                float wk[8];
+                float o[8][DPL];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    wk[k] = __shfl_sync(kFullMask, wgt, (k0 + k) & 31);
+                    if (k0 + k >= nblk)
+                        wk[k] = 0.f;
+                    const float *op = p.o_part + slot_of(s0 + k0 + k) * D + lane * DPL;
+                    if constexpr (DPL == 4) {
+                        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (wk[k] != 0.f)
+                            v = *reinterpret_cast<const float4 *>(op);
+                        o[k][0] = v.x; o[k][1] = v.y; o[k][2] = v.z; o[k][3] = v.w;
+                    } else {
+                        float2 v = make_float2(0.f, 0.f);
+                        if (wk[k] != 0.f)
+                            v = *reinterpret_cast<const float2 *>(op);
+                        o[k][0] = v.x; o[k][1] = v.y;
+                    }
                 }
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+#pragma unroll
+                    for (int d = 0; d < DPL; ++d)
+                        acc[d] = fmaf(wk[k], o[k][d], acc[d]);
             }
         }
+        ls = warp_sum_xor(ls, 1);
     }
     if (lane == 0)
         red_l[warp] = ls;

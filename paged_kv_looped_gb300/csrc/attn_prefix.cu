@@ -21,6 +21,7 @@
 #include <atomic>
 #include <map>
 #include <mutex>
+#include <type_traits>
 #include <vector>
 
 #include "rlt.h"
@@ -100,11 +101,12 @@ static_assert(kSmemP <= 227 * 1024, "shared memory of one CTA");
 static_assert(kVOff % 1024 == 0, "swizzled operands");
 
 // One run: tokens [tok_begin, tok_end) of a segment for kv head g and n_mem of
-// its members; the partial goes to chunk slot `slot` of each member's (b, h)
-// (the nchunks - 1 following slots are marked empty).
+// its members, their query rows held F times (prefix_replication); copy k of a
+// row writes its partial to slot `slot + k` of the member's (b, h), and marks
+// the slots of the nchunks - 1 following chunks (F each) empty.
 struct RunDesc {
     int64_t tok_begin, tok_end;
-    int32_t g, nsub, page_row, n_mem, slot, nchunks;
+    int32_t g, nsub, page_row, n_mem, slot, nchunks, F;
 };
 static_assert(sizeof(RunDesc) <= 64, "descriptor slot");
 
@@ -138,14 +140,15 @@ __device__ __forceinline__ Run decode_run(const PrefixParams &pp, int G, int ite
     const int per_block = 128 / G;
     const int m0 = mb * per_block;
     r.d.n_mem = min(per_block, sd[kSegMemberCount] - m0);
+    r.d.F = prefix_replication(min(per_block, sd[kSegMemberCount]) * G);
     r.member_begin = sd[kSegMemberBegin] + m0;
     r.d.page_row = sd[kSegPageRow];
-    r.d.slot = sd[kSegSlotBase] + chunk0;
+    r.d.slot = sd[kSegSlotBase] + chunk0 * r.d.F;
     const int t_first = sd[kSegFirstTile] + chunk0 * pp.chunk_tiles;
     const int t_last = sd[kSegFirstTile] + min(num_tiles, (chunk0 + r.d.nchunks) * pp.chunk_tiles);
     r.d.tok_begin = (int64_t)t_first * kPrefixTile;
     r.d.tok_end = min((int64_t)t_last * kPrefixTile, (int64_t)sd[kSegEndToken]);
-    if (pp.member_limit != nullptr && r.d.n_mem > 0)   // extend: no key past the block's last query
+    if (pp.member_limit != nullptr && r.d.n_mem > 0)   // no key past the block's largest limit
         r.d.tok_end = min(r.d.tok_end, (int64_t)pp.member_limit[r.member_begin + r.d.n_mem - 1]);
     r.d.nsub = (r.d.n_mem > 0 && r.d.tok_end > r.d.tok_begin)
                    ? (int)((r.d.tok_end - r.d.tok_begin + kSub - 1) / kSub) : 0;
@@ -171,14 +174,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
     return __all_sync(kFullMask, mbar_wait_or_abort(bar, parity, abort));
 }
 
-// Copy run descriptor r (and, for mrow >= 0, the q row and key count of member mrow) and
-// release its slot.  Warp-collective; false if the wait gave up.
+// Copy run descriptor r (and, for row >= 0, the member and key count behind query row
+// `row` of the run: its copy row % (128 / F), member of that / G) and release its slot.
+// Warp-collective; false if the wait gave up.
 __device__ __forceinline__ bool take_desc(uint64_t *bars, const unsigned char *base, int r, RunDesc &out,
-                                          int mrow, int &member, int &limit, const volatile int *abort, int lane)
+                                          int row, int G, int &member, int &limit, const volatile int *abort,
+                                          int lane)
 {
     if (!warp_wait(&bars[kBarDescFull + r % kDescs], (r / kDescs) & 1u, abort))
         return false;
     out = reinterpret_cast<const RunDesc *>(base + kDescOff)[r % kDescs];
+    const int mrow = row < 0 ? -1 : (row % (128 / max(out.F, 1))) / G;
     if (mrow >= 0 && mrow < out.n_mem) {
         member = reinterpret_cast<const int32_t *>(base + kMemOff)[(r % kDescs) * 128 + mrow];
         limit = reinterpret_cast<const int32_t *>(base + kLimOff)[(r % kDescs) * 128 + mrow];
@@ -189,14 +195,16 @@ __device__ __forceinline__ bool take_desc(uint64_t *bars, const unsigned char *b
     return true;
 }
 
-// Dims 64*half..64*half+63 of this thread's query row (member row / G, head row % G of
-// run d) as 32 words of packed bf16 pairs; zero for rows past the run's members.
+// Dims 64*half..64*half+63 of this thread's query row (copy row lr = row % (128 / F):
+// member lr / G, head lr % G of run d) as 32 words of packed bf16 pairs; zero for rows
+// past the run's members.
 __device__ __forceinline__ void load_q(const DecodeParams &p, const RunDesc &d, int G, int row, int member,
                                        int half, uint32_t (&w)[32])
 {
-    const bool live = d.nsub > 0 && row < d.n_mem * G;
+    const int lr = row % (128 / max(d.F, 1));
+    const bool live = d.nsub > 0 && lr < d.n_mem * G;
     const uint4 *src = reinterpret_cast<const uint4 *>(
-        p.q + ((int64_t)member * p.num_q_heads + d.g * G + row % G) * 128 + half * 64);
+        p.q + ((int64_t)member * p.num_q_heads + d.g * G + lr % G) * 128 + half * 64);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const uint4 v = live ? src[i] : make_uint4(0u, 0u, 0u, 0u);
@@ -347,7 +355,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         };
         int n = 0, r = 0, j = 0;                 // sub-tiles issued; current run and sub-tile
         RunDesc cur;
-        ok = take_desc(bars, base, r, cur, -1, unused, unused, abort_flag, lane);
+        ok = take_desc(bars, base, r, cur, -1, G, unused, unused, abort_flag, lane);
         int row_next = ok && cur.nsub > 0 ? lane_row(cur, 0) : -1;
         while (ok && cur.nsub > 0) {
             const int row = row_next;
@@ -356,7 +364,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 row_next = lane_row(cur, ++j);
             } else {
                 j = 0;
-                if (!(ok = take_desc(bars, base, ++r, cur, -1, unused, unused, abort_flag, lane)))
+                if (!(ok = take_desc(bars, base, ++r, cur, -1, G, unused, unused, abort_flag, lane)))
                     break;
                 if (cur.nsub > 0)
                     row_next = lane_row(cur, 0);
@@ -516,8 +524,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 return false;
             tc::fence_after_sync();
             const int R = ed.n_mem * G;
-            const bool live = quarter * 32 < R;
-            const int64_t slot = ((int64_t)e_b * p.num_q_heads + ed.g * G + row % G) * p.part_stride + ed.slot;
+            const int RB = 128 / ed.F;
+            const int lr = row % RB;              // the row this copy holds
+            const bool live = quarter * 32 % RB < R;
+            const int64_t slot = ((int64_t)e_b * p.num_q_heads + ed.g * G + lr % G) * p.part_stride + ed.slot +
+                                 quarter * 32 / RB;
             float l_tot = e_l;
             if (live) {
                 xsum[half * 128 + row] = e_l;
@@ -529,7 +540,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 for (int c = 0; c < 2; ++c) {
                     float o[32];
                     tc::tmem_ld32(t_lane + kColO + half * 64 + c * 32, o);
-                    if (row < R) {
+                    if (lr < R) {
                         float4 *dst = reinterpret_cast<float4 *>(p.o_part + slot * 128 + half * 64 + c * 32);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
@@ -542,28 +553,30 @@ __global__ void __launch_bounds__(kPThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&bars[kBarOFree]);
-            if (live && half == 0 && row < R) {
+            if (live && half == 0 && lr < R) {
                 p.lse_part[slot] = l_tot > 0.f ? e_m + log2f(l_tot) : -CUDART_INF_F;
                 for (int k = 1; k < ed.nchunks; ++k)   // chunks merged into this run's partial
-                    p.lse_part[slot + k] = -CUDART_INF_F;
+                    p.lse_part[slot + k * ed.F] = -CUDART_INF_F;
             }
             // both warps have read xsum before a later epilogue writes it
             return !live || pair_sync(pair, meets, abort_flag, lane);
         };
 
         uint32_t qw[32];
-        ok = take_desc(bars, base, 0, rd, row / G, b_row, lim_row, abort_flag, lane);
+        ok = take_desc(bars, base, 0, rd, row, G, b_row, lim_row, abort_flag, lane);
         if (ok && rd.nsub > 0) {
             load_q(p, rd, G, row, b_row, half, qw);
             store_q(qw, half, t_lane + kColQ, &bars[kBarQFull], lane);
         }
         for (int r = 0; ok && rd.nsub > 0; ++r) {
             // the next run's Q rows, loaded while this run's first S is computed
-            if (!(ok = take_desc(bars, base, r + 1, rn, row / G, b_next, lim_next, abort_flag, lane)))
+            if (!(ok = take_desc(bars, base, r + 1, rn, row, G, b_next, lim_next, abort_flag, lane)))
                 break;
             load_q(p, rn, G, row, b_next, half, qw);
             const int R = rd.n_mem * G;
-            const bool live = quarter * 32 < R;  // uniform over the quarter's two warps; quarter 0 is live
+            const int RB = 128 / rd.F;           // rows per copy of the run's query rows
+            const int part = quarter * 32 / RB;  // the copy this quarter holds
+            const bool live = quarter * 32 % RB < R;   // uniform over the quarter's two warps
             float m_ref = -CUDART_INF_F, l_run = 0.f;   // l_run: this warp's columns only
             if (!(ok = warp_wait(&bars[kBarSFull + n % kSBufs], (n / kSBufs) & 1u, abort_flag)))
                 break;
@@ -576,12 +589,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 if (live) {
                     tc::fence_after_sync();
                     const int64_t sub_begin = rd.tok_begin + (int64_t)j * kSub;
-                    const int valid = (int)min((int64_t)kSub, rd.tok_end - sub_begin) -
-                                      half * 64;       // valid columns of this warp's half
-                    // this row's own end (extend: its causal limit)
-                    const int row_valid = (int)max(min((int64_t)valid, (int64_t)lim_row - sub_begin - half * 64),
-                                                   (int64_t)-1);
-                    if (valid + half * 64 < kSub && warp == 0) {
+                    const int valid = (int)min((int64_t)kSub, rd.tok_end - sub_begin);   // tokens of the sub-tile
+                    // this row's own end (its key limit: shared prefix length, or causal limit)
+                    const int row_end = (int)max(min((int64_t)valid, (int64_t)lim_row - sub_begin), (int64_t)0);
+                    if (valid < kSub && warp == 0) {
                         // ragged end of a private tail: zero the V rows past it, whose memory may
                         // hold anything (0 * NaN would poison O), once this V copy has landed
                         if (!(ok = warp_wait(&bars[kBarFullV + n % kStagesV], (n / kStagesV) & 1u, abort_flag)))
@@ -594,54 +605,77 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         }
                         fence_proxy_async();     // zeroed rows (generic) -> P.V MMA (async proxy)
                     }
-                    float v[64];
-                    tc::tmem_ld64(t_s + half * 64, v);
-                    float mx = -CUDART_INF_F;
+                    // The copy `part` of a row owns tokens [part * 128/F, +128/F) of the sub-tile;
+                    // the quarter's two warps take one half of them each (WC columns), and each
+                    // warp writes P for its columns and zeros over its share of the other copies'.
+                    auto subtile = [&](auto fc) -> bool {
+                        constexpr int F = decltype(fc)::value;
+                        constexpr int WC = 64 / F;
+                        const int c0 = part * (128 / F) + half * WC;
+                        const int row_valid = min(max(row_end - c0, 0), WC);
+                        float v[WC];
+                        tc::tmem_ld<WC>(t_s + c0, v);
+                        float mx = -CUDART_INF_F;
 #pragma unroll
-                    for (int i = 0; i < 64; ++i)
-                        if (i < row_valid)
-                            mx = fmaxf(mx, v[i]);
-                    // the row max over both halves of the sub-tile
-                    xmax[((n & 1) * 2 + half) * 128 + row] = mx;
-                    if (!(ok = pair_sync(pair, meets, abort_flag, lane)))
-                        break;
-                    mx = fmaxf(mx, xmax[((n & 1) * 2 + (half ^ 1)) * 128 + row]) * p.qscale;
-                    const bool up = mx > m_ref + kRescaleThreshold;
-                    const float m_next = up ? mx : m_ref;   // rows >= R hold garbage and are never stored
-                    // 1 if the reference stays, 0 at first; 1 while a row has seen no key at all
-                    const float scale_o = m_next == -CUDART_INF_F ? 1.f : exp2f(m_ref - m_next);
-                    if (__any_sync(kFullMask, up) && j > 0) {
-                        // rescale this warp's half of the row's O (P.V of the previous sub-tile landed)
-                        if (!(ok = warp_wait(&bars[kBarPvDone + (n - 1) % kSBufs], ((n - 1) / kSBufs) & 1u,
-                                             abort_flag)))
-                            break;
-                        tc::fence_after_sync();
+                        for (int i = 0; i < WC; ++i)
+                            if (i < row_valid)
+                                mx = fmaxf(mx, v[i]);
+                        // the row max over both warps' columns
+                        xmax[((n & 1) * 2 + half) * 128 + row] = mx;
+                        if (!pair_sync(pair, meets, abort_flag, lane))
+                            return false;
+                        mx = fmaxf(mx, xmax[((n & 1) * 2 + (half ^ 1)) * 128 + row]) * p.qscale;
+                        const bool up = mx > m_ref + kRescaleThreshold;
+                        const float m_next = up ? mx : m_ref;   // rows past the members hold garbage, never stored
+                        // 1 if the reference stays, 0 at first; 1 while a row has seen no key at all
+                        const float scale_o = m_next == -CUDART_INF_F ? 1.f : exp2f(m_ref - m_next);
+                        if (__any_sync(kFullMask, up) && j > 0) {
+                            // rescale this warp's half of the row's O (P.V of the previous sub-tile landed)
+                            if (!warp_wait(&bars[kBarPvDone + (n - 1) % kSBufs], ((n - 1) / kSBufs) & 1u, abort_flag))
+                                return false;
+                            tc::fence_after_sync();
 #pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            float o[32];
-                            tc::tmem_ld32(t_lane + kColO + half * 64 + c * 32, o);
+                            for (int c = 0; c < 2; ++c) {
+                                float o[32];
+                                tc::tmem_ld32(t_lane + kColO + half * 64 + c * 32, o);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                o[i] *= scale_o;
-                            tc::tmem_st32(t_lane + kColO + half * 64 + c * 32, o);
+                                for (int i = 0; i < 32; ++i)
+                                    o[i] *= scale_o;
+                                tc::tmem_st32(t_lane + kColO + half * 64 + c * 32, o);
+                            }
                         }
-                    }
-                    l_run *= scale_o;
-                    m_ref = m_next;
-                    // P = 2^(s - m) as bf16 pairs over columns this quarter pair has read
-                    float lsum = 0.f;
-                    uint32_t w[32];
+                        l_run *= scale_o;
+                        m_ref = m_next;
+                        // P = 2^(s - m) as bf16 pairs
+                        float lsum = 0.f;
+                        uint32_t w[WC / 2], zero[WC / 2];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float p0 = 2 * i < row_valid ? fast_exp2(fmaf(v[2 * i], p.qscale, -m_ref)) : 0.f;
-                        const float p1 =
-                            2 * i + 1 < row_valid ? fast_exp2(fmaf(v[2 * i + 1], p.qscale, -m_ref)) : 0.f;
-                        lsum += p0 + p1;
-                        w[i] = cvt_bf16x2(p0, p1);
-                    }
-                    tc::tmem_st32u(t_s + half * 32, w);
-                    l_run += lsum;
-                    tc::fence_before_sync();
+                        for (int i = 0; i < WC / 2; ++i) {
+                            const float p0 = 2 * i < row_valid ? fast_exp2(fmaf(v[2 * i], p.qscale, -m_ref)) : 0.f;
+                            const float p1 =
+                                2 * i + 1 < row_valid ? fast_exp2(fmaf(v[2 * i + 1], p.qscale, -m_ref)) : 0.f;
+                            lsum += p0 + p1;
+                            w[i] = cvt_bf16x2(p0, p1);
+                            zero[i] = 0u;
+                        }
+#pragma unroll
+                        for (int k = 0; k < F; ++k) {
+                            const uint32_t col = t_s + k * (64 / F) + half * (WC / 2);
+                            if (k == part)
+                                tc::tmem_st_nowait<WC / 2>(col, w);
+                            else
+                                tc::tmem_st_nowait<WC / 2>(col, zero);
+                        }
+                        tc::tmem_wait_st();
+                        l_run += lsum;
+                        tc::fence_before_sync();
+                        return true;
+                    };
+                    const bool good = rd.F == 4   ? subtile(std::integral_constant<int, 4>{})
+                                      : rd.F == 2 ? subtile(std::integral_constant<int, 2>{})
+                                                  : subtile(std::integral_constant<int, 1>{});
+                    if (!(ok = good))
+                        break;
                 }
                 __syncwarp();
                 if (lane == 0)
@@ -764,7 +798,8 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
                                               int32_t query_group, int32_t private_tails,
                                               int32_t *segments,
                                               int32_t max_segments, int32_t *members,
-                                              int32_t max_member_entries, int32_t *request_prefix,
+                                              int32_t *member_limit, int32_t max_member_entries,
+                                              int32_t *request_prefix,
                                               int32_t *sizes)
 {
     using rlt::kPrefixTile;
@@ -793,7 +828,8 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
         return (int)(L / kPrefixTile);
     };
 
-    struct Seg { int first, tiles, parent; std::vector<int> mem; int64_t end_token; };
+    // mem: member requests; lim: each member's key count in the segment (its shared tokens)
+    struct Seg { int first, tiles, parent; std::vector<int> mem; int64_t end_token; std::vector<int64_t> lim; };
     std::vector<Seg> segs;
     std::vector<int> deepest(batch, -1);       // segment holding each request's last shared tile
     struct Group { std::vector<int> mem; int seg; };
@@ -833,12 +869,77 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
         level.swap(next);
     }
 
-    for (Seg &sg : segs)
+    for (Seg &sg : segs) {
         sg.end_token = (int64_t)(sg.first + sg.tiles) * kPrefixTile;
+        sg.lim.assign(sg.mem.size(), sg.end_token);
+    }
+
+    // A chain of segments that only shrinks (each the only child of the one before:
+    // requests leaving a common prefix one after another, as in a radix tree over one
+    // prompt) becomes ONE segment whose members carry their own key limits: the tiles
+    // are still read once, and the kernel runs one long accumulation instead of one
+    // short run per link.  Merged only where all members fit one member block of the
+    // kernel (128 / query_group), so that no tile is read more often than before.
+    const int per_block = 128 / query_group;
+    {
+        std::vector<std::vector<int>> kids(segs.size());
+        for (size_t s = 0; s < segs.size(); ++s)
+            if (segs[s].parent >= 0)
+                kids[segs[s].parent].push_back((int)s);
+        std::vector<int> into(segs.size(), -1);
+        std::vector<Seg> out;
+        for (size_t s = 0; s < segs.size(); ++s) {    // parents precede children
+            if (into[s] >= 0)
+                continue;
+            const int idx = (int)out.size();
+            Seg m = segs[s];
+            m.parent = m.parent < 0 ? -1 : into[m.parent];
+            into[s] = idx;
+            std::map<int, size_t> pos;
+            for (size_t i = 0; i < m.mem.size(); ++i)
+                pos[m.mem[i]] = i;
+            int cur = (int)s;
+            if ((int)m.mem.size() <= per_block) {
+                while (kids[cur].size() == 1) {
+                    const int c = kids[cur][0];
+                    m.tiles += segs[c].tiles;
+                    m.end_token = segs[c].end_token;
+                    for (int b : segs[c].mem)
+                        m.lim[pos[b]] = segs[c].end_token;
+                    into[c] = idx;
+                    cur = c;
+                }
+            }
+            // members by ascending limit: a member block then ends at its last member's
+            // limit, and the page row (the longest member) holds every tile's pages
+            std::vector<size_t> order(m.mem.size());
+            for (size_t i = 0; i < order.size(); ++i)
+                order[i] = i;
+            std::stable_sort(order.begin(), order.end(),
+                             [&](size_t a, size_t b) { return m.lim[a] < m.lim[b]; });
+            Seg sorted = m;
+            for (size_t i = 0; i < order.size(); ++i) {
+                sorted.mem[i] = m.mem[order[i]];
+                sorted.lim[i] = m.lim[order[i]];
+            }
+            out.push_back(sorted);
+        }
+        segs.swap(out);
+        for (int b = 0; b < batch; ++b)
+            deepest[b] = -1;
+        for (size_t s = 0; s < segs.size(); ++s)
+            for (int b : segs[s].mem)
+                deepest[b] = (int)s;
+    }
     std::vector<int64_t> covered(batch, 0);
-    for (int b = 0; b < batch; ++b)
-        if (deepest[b] >= 0)
-            covered[b] = segs[deepest[b]].end_token;
+    for (int b = 0; b < batch; ++b) {
+        if (deepest[b] < 0)
+            continue;
+        const Seg &sg = segs[deepest[b]];
+        for (size_t i = 0; i < sg.mem.size(); ++i)
+            if (sg.mem[i] == b)
+                covered[b] = sg.lim[i];
+    }
     if (private_tails) {
         // every request's own remaining tokens become a one-member segment
         for (int b = 0; b < batch; ++b) {
@@ -847,24 +948,26 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
                 continue;
             const int first = (int)(covered[b] / kPrefixTile);
             const int tiles = (int)((L + kPrefixTile - 1) / kPrefixTile) - first;
-            segs.push_back({first, tiles, deepest[b], {b}, L});
+            segs.push_back({first, tiles, deepest[b], {b}, L, {L}});
             deepest[b] = (int)segs.size() - 1;
             covered[b] = L;
         }
     }
     const int nseg = (int)segs.size();
-    std::vector<int> chunks(nseg), slot_base(nseg);
+    // per member, a segment has `chunks` partial slots per copy of its query rows
+    std::vector<int> chunks(nseg), slot_base(nseg), slots(nseg);
     int64_t member_entries = 0;
     int max_chunks = 0, max_members = 0;
     for (int s = 0; s < nseg; ++s) {               // parents precede children
         chunks[s] = (segs[s].tiles + chunk_tiles - 1) / chunk_tiles;
-        slot_base[s] = segs[s].parent < 0 ? 0 : slot_base[segs[s].parent] + chunks[segs[s].parent];
+        slots[s] = chunks[s] *
+                   rlt::prefix_replication(std::min<int>((int)segs[s].mem.size(), per_block) * query_group);
+        slot_base[s] = segs[s].parent < 0 ? 0 : slot_base[segs[s].parent] + slots[segs[s].parent];
         member_entries += (int64_t)segs[s].mem.size();
         max_chunks = std::max(max_chunks, chunks[s]);
         max_members = std::max(max_members, (int)segs[s].mem.size());
     }
     // work units: (segment, chunk, member block); a member block holds 128 / query_group members
-    const int per_block = 128 / query_group;
     std::vector<int64_t> work_begin(nseg + 1, 0);
     for (int s = 0; s < nseg; ++s)
         work_begin[s + 1] = work_begin[s] + (int64_t)chunks[s] *
@@ -880,7 +983,7 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
     for (int b = 0; b < batch; ++b) {
         const int s = deepest[b];
         request_prefix[2 * b] = (int32_t)covered[b];
-        request_prefix[2 * b + 1] = s < 0 ? 0 : slot_base[s] + chunks[s];
+        request_prefix[2 * b + 1] = s < 0 ? 0 : slot_base[s] + slots[s];
         max_slots = std::max(max_slots, request_prefix[2 * b + 1]);
         const int64_t L = std::min<int64_t>(std::max(seq_lens[b], 0), (int64_t)max_pages * page_size);
         max_rest = std::max(max_rest, L - covered[b]);
@@ -889,6 +992,8 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
     sizes[5] = (int32_t)max_rest;
     if (nseg > max_segments || member_entries > max_member_entries)
         return RLT_ERR_OUT_OF_RANGE;               // sizes[] tells the caller what is needed
+    if (nseg > 0 && (segments == nullptr || members == nullptr || member_limit == nullptr))
+        return RLT_ERR_INVALID_ARG;
     int64_t m = 0;
     for (int s = 0; s < nseg; ++s) {
         int32_t *row = segments + (int64_t)s * rlt::kSegFields;
@@ -897,11 +1002,13 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
         row[rlt::kSegSlotBase] = slot_base[s];
         row[rlt::kSegMemberBegin] = (int32_t)m;
         row[rlt::kSegMemberCount] = (int32_t)segs[s].mem.size();
-        row[rlt::kSegPageRow] = segs[s].mem[0];
+        row[rlt::kSegPageRow] = segs[s].mem.back();
         row[rlt::kSegEndToken] = (int32_t)segs[s].end_token;
         row[rlt::kSegWorkBegin] = (int32_t)work_begin[s];
-        for (int b : segs[s].mem)
-            members[m++] = b;
+        for (size_t i = 0; i < segs[s].mem.size(); ++i, ++m) {
+            members[m] = segs[s].mem[i];
+            member_limit[m] = (int32_t)segs[s].lim[i];
+        }
     }
     return RLT_OK;
 }
@@ -933,7 +1040,7 @@ extern "C" RLT_API rlt_status rlt_plan_extend(const int32_t *seq_lens, const int
     const int per_block = 128 / query_group;
     const int64_t chunk_tokens = (int64_t)chunk_tiles * kPrefixTile;
     int64_t nseg = 0, rows = 0, units = 0;
-    int max_chunks = 0, max_members = 0;
+    int max_chunks = 0, max_members = 0, max_slots = 0;
     for (int b = 0; b < batch; ++b) {
         const int64_t L = seq_lens[b], n = new_lens[b];
         if (n < 0 || L < n || L > INT32_MAX)
@@ -947,13 +1054,15 @@ extern "C" RLT_API rlt_status rlt_plan_extend(const int32_t *seq_lens, const int
         units += (int64_t)chunks * ((n + per_block - 1) / per_block);
         max_chunks = std::max(max_chunks, chunks);
         max_members = std::max(max_members, (int)n);
+        max_slots = std::max(max_slots, chunks * rlt::prefix_replication(
+                                                     (int)std::min<int64_t>(n, per_block) * query_group));
     }
     if (rows > INT32_MAX || units > INT32_MAX)
         return RLT_ERR_OUT_OF_RANGE;
     sizes[0] = (int32_t)nseg;
     sizes[1] = (int32_t)rows;
     sizes[2] = max_chunks;
-    sizes[3] = max_chunks;            // partial slots per row: every chunk of the longest key range
+    sizes[3] = max_slots;             // partial slots per row: every chunk of the longest key range, per copy
     sizes[4] = max_members;
     sizes[5] = 0;                     // no split-K rest
     sizes[6] = (int32_t)units;
@@ -969,6 +1078,7 @@ extern "C" RLT_API rlt_status rlt_plan_extend(const int32_t *seq_lens, const int
             continue;
         const int tiles = (int)((L + kPrefixTile - 1) / kPrefixTile);
         const int chunks = (tiles + chunk_tiles - 1) / chunk_tiles;
+        const int F = rlt::prefix_replication((int)std::min<int64_t>(n, per_block) * query_group);
         int32_t *row = segments + s * rlt::kSegFields;
         row[rlt::kSegFirstTile] = 0;
         row[rlt::kSegNumTiles] = tiles;
@@ -985,7 +1095,7 @@ extern "C" RLT_API rlt_status rlt_plan_extend(const int32_t *seq_lens, const int
             members[m + i] = (int32_t)(m + i);                 // packed q row of this new token
             member_limit[m + i] = (int32_t)limit;
             row_prefix[2 * (m + i)] = (int32_t)limit;
-            row_prefix[2 * (m + i) + 1] = (int32_t)((block_end + chunk_tokens - 1) / chunk_tokens);
+            row_prefix[2 * (m + i) + 1] = (int32_t)((block_end + chunk_tokens - 1) / chunk_tokens) * F;
             row_len[m + i] = (int32_t)limit;
         }
         work += (int64_t)chunks * ((n + per_block - 1) / per_block);

@@ -40,6 +40,17 @@ struct DecodeParams {
 // Tokens per tensor-core tile of the shared-prefix kernel.
 constexpr int kPrefixTile = 128;
 
+// Query rows of a tensor-core run are copied into idle TMEM lane quarters: with R
+// live rows (members x query group) a run keeps F = 4, 2 or 1 copies of them,
+// each copy taking 1/F of every 128-token sub-tile's keys and writing its own
+// partial, so that the softmax work of a few rows is spread over all four SM
+// sub-partitions.  F follows from the rows of a segment's first (fullest)
+// member block; planner and kernel must agree on it.
+__host__ __device__ inline int prefix_replication(int rows)
+{
+    return rows <= 32 ? 4 : rows <= 64 ? 2 : 1;
+}
+
 // Fields of one segment of a prefix plan (rlt_plan_prefix).
 enum PrefixSegField { kSegFirstTile = 0, kSegNumTiles, kSegSlotBase, kSegMemberBegin,
                       kSegMemberCount, kSegPageRow, kSegEndToken, kSegWorkBegin, kSegFields };

@@ -16,6 +16,13 @@ import workloads as W
 TILE = 128
 
 
+def copies(members, G):
+    """Copies of a segment's query rows in the tensor-core kernel: its first member block's
+    rows spread over the four TMEM lane quarters (4 copies of <= 32 rows, 2 of <= 64)."""
+    rows = min(members, 128 // G) * G
+    return 4 if rows <= 32 else 2 if rows <= 64 else 1
+
+
 def tile_key(pt, b, t, ps):
     tok = t * TILE
     if ps <= TILE:
@@ -31,9 +38,10 @@ def common_tiles(pt, sl, ps, b, c):
     return t
 
 
-def check_plan(case, chunk_tiles=4):
+def check_plan(case, chunk_tiles=4, G=1):
     pt, sl, ps = case.page_table, case.seq_lens, case.page_size
-    plan = rlt.rlt_plan_prefix(pt, sl, ps, chunk_tiles)
+    plan = rlt.rlt_plan_prefix(pt, sl, ps, chunk_tiles, False, G)
+    per_block = 128 // G
     assert plan.max_rest_len == max(int(sl[b]) - int(plan.request_prefix[b, 0]) for b in range(case.batch))
     B = case.batch
     cp = np.zeros((B, B), int)
@@ -44,17 +52,24 @@ def check_plan(case, chunk_tiles=4):
     # each request's covered prefix = its longest shared run with any other request
     for b in range(B):
         assert plan.request_prefix[b, 0] == TILE * (cp[b].max() if B > 1 else 0), b
-    # segments: members share the segment's tiles page for page, and nobody else does
+    # segments: at tile t the members whose limit lies past t share it page for page
+    # with the page row, and nobody else does
     seg_of_tile = {}
     for s in range(plan.num_segments):
         first, n, base, mb, mc, row, end, work = plan.segments[s]
         assert end == (first + n) * TILE
         mem = plan.members[mb: mb + mc]
-        assert mc >= 2 and row in mem and list(mem) == sorted(mem)
+        lim = plan.member_limit[mb: mb + mc]
+        assert mc >= 2 and row == mem[-1] and lim[-1] == end
+        assert list(lim) == sorted(lim) and len(set(mem)) == mc
+        assert all(first * TILE < x <= end and x % TILE == 0 for x in lim)
+        if len(set(lim)) > 1:
+            assert mc <= per_block                 # a merged chain fits one member block
         for t in range(first, first + n):
-            want = {row} | {c for c in range(B) if c != row and cp[row, c] >= t + 1}
-            assert set(mem) == want, (s, t)
-            for b in mem:
+            live = {int(b) for b, x in zip(mem, lim) if x > t * TILE}
+            want = {int(row)} | {c for c in range(B) if c != row and cp[row, c] >= t + 1}
+            assert live == want, (s, t)
+            for b in live:
                 assert tile_key(pt, b, t, ps) == tile_key(pt, row, t, ps)
                 seg_of_tile.setdefault(b, []).append((t, s))
     # along each request's path: tiles 0..n-1 in order, partial slots contiguous from 0
@@ -64,25 +79,46 @@ def check_plan(case, chunk_tiles=4):
         slots = []
         for s in dict.fromkeys(s for _, s in tiles):
             first, n, base = plan.segments[s][:3]
-            slots += list(range(base, base + -(-n // chunk_tiles)))
+            slots += list(range(base, base + -(-n // chunk_tiles) * copies(int(plan.segments[s][4]), G)))
         assert slots == list(range(len(slots))) and len(slots) == plan.request_prefix[b, 1]
     assert plan.max_prefix_slots == (plan.request_prefix[:, 1].max() if B else 0)
     # work units: chunks x member blocks per segment, numbered in segment order
     units = 0
     for s in range(plan.num_segments):
         assert plan.segments[s][7] == units
-        units += -(-int(plan.segments[s][1]) // chunk_tiles) * -(-int(plan.segments[s][4]) // 128)
+        units += -(-int(plan.segments[s][1]) // chunk_tiles) * -(-int(plan.segments[s][4]) // per_block)
     assert plan.work_units == units
     return plan
 
 
 @pytest.mark.parametrize("name", ["huginn", "longctx", "ouro", "tiny"])
 def test_plan_of_workloads(name):
-    plan = check_plan(W.config(name))
+    case = W.config(name)
+    plan = check_plan(case, G=case.group)
     if name in ("huginn", "longctx"):
-        assert plan.num_segments > 0
+        # one prompt chain that requests leave one by one: a single segment with limits
+        assert plan.num_segments == 1
+        assert plan.segments[0][4] == case.batch
     else:
         assert plan.num_segments == 0              # nothing shared
+
+
+@pytest.mark.parametrize("G", [1, 8, 32, 64])
+def test_chain_merge_respects_member_blocks(G):
+    # 5 requests on one prompt chain, leaving it at different tiles: the chain is merged
+    # from the first link whose members fit one block of 128 / G; links with more
+    # members stay segments of their own, every member reading all their tiles
+    case = W.custom(B=5, Hq=8, Hkv=8, D=128, ps=16, seq_lens=[3000, 2600, 4100, 1700, 2222], shared_frac=0.8,
+                    seed=11)
+    plan = check_plan(case, 2, G)
+    if 5 <= 128 // G:
+        assert plan.num_segments == 1
+    else:
+        assert plan.num_segments > 1
+        for s in range(plan.num_segments):
+            mb, mc = plan.segments[s][3], plan.segments[s][4]
+            if mc > 128 // G:
+                assert len(set(plan.member_limit[mb: mb + mc])) == 1
 
 
 @pytest.mark.parametrize("chunk_tiles", [1, 3, 32])
@@ -148,7 +184,7 @@ def test_private_tails_cover_every_token(name):
         assert first * TILE == shared.request_prefix[b, 0]
         assert (first + ntiles) * TILE >= end > (first + ntiles - 1) * TILE
         assert base == shared.request_prefix[b, 1]
-        assert plan.request_prefix[b, 1] == base + -(-ntiles // 4)
+        assert plan.request_prefix[b, 1] == base + -(-ntiles // 4) * copies(1, 1)
 
 
 @pytest.mark.parametrize("G,chunk_tiles", [(1, 1), (4, 2), (8, 3)])
@@ -172,12 +208,12 @@ def test_extend_plan_by_brute_force(G, chunk_tiles):
             assert plan.row_len[row + i] == L - n + i + 1
             block_last = min(n, (i // per_block + 1) * per_block) - 1
             assert plan.row_prefix[row + i, 0] == L - n + i + 1
-            assert plan.row_prefix[row + i, 1] == -(-(L - n + block_last + 1) // ct)
+            assert plan.row_prefix[row + i, 1] == -(-(L - n + block_last + 1) // ct) * copies(n, G)
         units += -(-tiles // chunk_tiles) * -(-n // per_block)
         row += n
         s += 1
     assert plan.work_units == units
-    assert plan.max_slots == max(-(-(-(-L // TILE)) // chunk_tiles) for L, n in zip(lens, new) if n)
+    assert plan.max_slots == max(-(-(-(-L // TILE)) // chunk_tiles) * copies(n, G) for L, n in zip(lens, new) if n)
 
 
 def test_extend_plan_rejects_more_new_tokens_than_the_sequence():
