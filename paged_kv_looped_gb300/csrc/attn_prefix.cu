@@ -215,6 +215,17 @@ __device__ __forceinline__ void load_q(const DecodeParams &p, const RunDesc &d, 
     }
 }
 
+// Bring the 128 bytes load_q will read into L2 ahead of time (no registers held).
+__device__ __forceinline__ void prefetch_q(const DecodeParams &p, const RunDesc &d, int G, int row, int member,
+                                           int half)
+{
+    const int lr = row % (128 / max(d.F, 1));
+    if (d.nsub > 0 && lr < d.n_mem * G) {
+        const uint16_t *src = p.q + ((int64_t)member * p.num_q_heads + d.g * G + lr % G) * 128 + half * 64;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+    }
+}
+
 // Those words into columns 32*half.. of the TMEM Q buffer at t_q (the A operand
 // layout of S = Q K^T: a row's dims in order, two per column, the lower in the low
 // half), then the warp's arrive on the buffer's barrier.
@@ -537,22 +548,30 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 l_tot = e_l + xsum[(half ^ 1) * 128 + row];
                 const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;   // a row with no key: o = 0
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    float o[32];
-                    tc::tmem_ld32(t_lane + kColO + half * 64 + c * 32, o);
+                for (int c = 0; c < 4; ++c) {
+                    float o[16];
+                    tc::tmem_ld<16>(t_lane + kColO + half * 64 + c * 16, o);
+                    if (c == 3) {
+                        // O has left TMEM: the next run's first P.V may overwrite it now
+                        tc::fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(&bars[kBarOFree]);
+                    }
                     if (lr < R) {
-                        float4 *dst = reinterpret_cast<float4 *>(p.o_part + slot * 128 + half * 64 + c * 32);
+                        float4 *dst = reinterpret_cast<float4 *>(p.o_part + slot * 128 + half * 64 + c * 16);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
+                        for (int i = 0; i < 4; ++i)
                             dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
                                                  o[4 * i + 3] * inv);
                     }
                 }
+            } else {
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars[kBarOFree]);
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&bars[kBarOFree]);
             if (live && half == 0 && lr < R) {
                 p.lse_part[slot] = l_tot > 0.f ? e_m + log2f(l_tot) : -CUDART_INF_F;
                 for (int k = 1; k < ed.nchunks; ++k)   // chunks merged into this run's partial
@@ -572,7 +591,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             // the next run's Q rows, loaded while this run's first S is computed
             if (!(ok = take_desc(bars, base, r + 1, rn, row, G, b_next, lim_next, abort_flag, lane)))
                 break;
-            load_q(p, rn, G, row, b_next, half, qw);
+            prefetch_q(p, rn, G, row, b_next, half);
             const int R = rd.n_mem * G;
             const int RB = 128 / rd.F;           // rows per copy of the run's query rows
             const int part = quarter * 32 / RB;  // the copy this quarter holds
@@ -580,8 +599,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
             float m_ref = -CUDART_INF_F, l_run = 0.f;   // l_run: this warp's columns only
             if (!(ok = warp_wait(&bars[kBarSFull + n % kSBufs], (n / kSBufs) & 1u, abort_flag)))
                 break;
-            if (rn.nsub > 0)   // the previous run's S MMAs are complete: its Q buffer is free
-                store_q(qw, half, t_lane + kColQ + ((r + 1) % kQBufs) * 64, &bars[kBarQFull + (r + 1) % kQBufs], lane);
             for (int j = 0; j < rd.nsub; ++j, ++n) {
                 if (j > 0 && !(ok = warp_wait(&bars[kBarSFull + n % kSBufs], (n / kSBufs) & 1u, abort_flag)))
                     break;
@@ -610,16 +627,23 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     // warp writes P for its columns and zeros over its share of the other copies'.
                     auto subtile = [&](auto fc) -> bool {
                         constexpr int F = decltype(fc)::value;
-                        constexpr int WC = 64 / F;
+                        constexpr int WC = 64 / F;                 // this warp's columns
+                        // all of them stay in registers from the max to the exp pass: once the
+                        // pair has met, the other warp's P stores may overwrite these S columns
+                        constexpr int CW = WC;
+                        constexpr int NCH = 1;
                         const int c0 = part * (128 / F) + half * WC;
-                        const int row_valid = min(max(row_end - c0, 0), WC);
-                        float v[WC];
-                        tc::tmem_ld<WC>(t_s + c0, v);
+                        float v[CW];
                         float mx = -CUDART_INF_F;
 #pragma unroll
-                        for (int i = 0; i < WC; ++i)
-                            if (i < row_valid)
-                                mx = fmaxf(mx, v[i]);
+                        for (int ch = 0; ch < NCH; ++ch) {
+                            const int rv = min(max(row_end - c0 - ch * CW, 0), CW);
+                            tc::tmem_ld<CW>(t_s + c0 + ch * CW, v);
+#pragma unroll
+                            for (int i = 0; i < CW; ++i)
+                                if (i < rv)
+                                    mx = fmaxf(mx, v[i]);
+                        }
                         // the row max over both warps' columns
                         xmax[((n & 1) * 2 + half) * 128 + row] = mx;
                         if (!pair_sync(pair, meets, abort_flag, lane))
@@ -635,36 +659,40 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                 return false;
                             tc::fence_after_sync();
 #pragma unroll
-                            for (int c = 0; c < 2; ++c) {
-                                float o[32];
-                                tc::tmem_ld32(t_lane + kColO + half * 64 + c * 32, o);
+                            for (int c = 0; c < 4; ++c) {
+                                float o[16];
+                                uint32_t ow[16];
+                                tc::tmem_ld<16>(t_lane + kColO + half * 64 + c * 16, o);
 #pragma unroll
-                                for (int i = 0; i < 32; ++i)
-                                    o[i] *= scale_o;
-                                tc::tmem_st32(t_lane + kColO + half * 64 + c * 32, o);
+                                for (int i = 0; i < 16; ++i)
+                                    ow[i] = __float_as_uint(o[i] * scale_o);
+                                tc::tmem_st_nowait<16>(t_lane + kColO + half * 64 + c * 16, ow);
                             }
+                            tc::tmem_wait_st();
                         }
                         l_run *= scale_o;
                         m_ref = m_next;
-                        // P = 2^(s - m) as bf16 pairs
+                        // P = 2^(s - m) as bf16 pairs, stored in pieces of at most 16 words
                         float lsum = 0.f;
-                        uint32_t w[WC / 2], zero[WC / 2];
 #pragma unroll
-                        for (int i = 0; i < WC / 2; ++i) {
-                            const float p0 = 2 * i < row_valid ? fast_exp2(fmaf(v[2 * i], p.qscale, -m_ref)) : 0.f;
-                            const float p1 =
-                                2 * i + 1 < row_valid ? fast_exp2(fmaf(v[2 * i + 1], p.qscale, -m_ref)) : 0.f;
-                            lsum += p0 + p1;
-                            w[i] = cvt_bf16x2(p0, p1);
-                            zero[i] = 0u;
+                        for (int ch = 0; ch < NCH; ++ch) {
+                            const int rv = min(max(row_end - c0 - ch * CW, 0), CW);
+                            uint32_t w[CW / 2];
+#pragma unroll
+                            for (int i = 0; i < CW / 2; ++i) {
+                                const float p0 = 2 * i < rv ? fast_exp2(fmaf(v[2 * i], p.qscale, -m_ref)) : 0.f;
+                                const float p1 = 2 * i + 1 < rv ? fast_exp2(fmaf(v[2 * i + 1], p.qscale, -m_ref)) : 0.f;
+                                lsum += p0 + p1;
+                                w[i] = cvt_bf16x2(p0, p1);
+                            }
+                            tc::tmem_st_nowait<CW / 2>(t_s + (c0 + ch * CW) / 2, w);
                         }
+                        // zeros over this warp's share of the other copies' columns
+                        if constexpr (F > 1) {
 #pragma unroll
-                        for (int k = 0; k < F; ++k) {
-                            const uint32_t col = t_s + k * (64 / F) + half * (WC / 2);
-                            if (k == part)
-                                tc::tmem_st_nowait<WC / 2>(col, w);
-                            else
-                                tc::tmem_st_nowait<WC / 2>(col, zero);
+                            for (int k = 0; k < F; ++k)
+                                if (k != part)
+                                    tc::tmem_zero_nowait<WC / 2>(t_s + k * (64 / F) + half * (WC / 2));
                         }
                         tc::tmem_wait_st();
                         l_run += lsum;
@@ -680,6 +708,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&bars[kBarPFull + n % kSBufs]);
+                // the next run's Q rows (brought into L2 at this run's start) into the Q buffer of
+                // the run before this one, whose S MMAs completed before this run's first S
+                if (j == 0 && rn.nsub > 0) {
+                    load_q(p, rn, G, row, b_next, half, qw);
+                    store_q(qw, half, t_lane + kColQ + ((r + 1) % kQBufs) * 64, &bars[kBarQFull + (r + 1) % kQBufs],
+                            lane);
+                }
                 if (j == 0 && e_last >= 0) {
                     // run r-1's epilogue: its last P.V ran while this P was being made
                     if (!(ok = epilogue()))

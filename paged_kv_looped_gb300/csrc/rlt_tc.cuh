@@ -276,6 +276,22 @@ __device__ __forceinline__ void tmem_st_nowait(uint32_t taddr, const uint32_t *v
     }
 }
 
+// Zero N (8 or 16) consecutive 32-bit columns of this thread's TMEM lane, no wait.
+template <int N>
+__device__ __forceinline__ void tmem_zero_nowait(uint32_t taddr)
+{
+    const uint32_t z = 0u;
+    if constexpr (N == 8) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1};"
+                     ::"r"(taddr), "r"(z) : "memory");
+    } else {
+        static_assert(N == 16, "8 or 16 words");
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                     "{%1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1};"
+                     ::"r"(taddr), "r"(z) : "memory");
+    }
+}
+
 __device__ __forceinline__ void tmem_wait_st()
 {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
