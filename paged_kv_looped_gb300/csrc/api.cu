@@ -295,7 +295,7 @@ RLT_API size_t rlt_paged_decode_prefix_workspace_size(int32_t batch, int32_t num
         max_prefix_slots < 0 || split_tokens < 0)
         return 0;
     const rlt::DecodePlan plan = rlt::plan_decode(batch, num_q_heads, num_kv_heads, head_dim,
-                                                  max_rest_len, split_tokens, current_sms());
+                                                  max_rest_len, split_tokens, current_sms(), rlt::kRestWaves);
     const size_t rows = (size_t)batch * num_q_heads * (size_t)(max_prefix_slots + plan.max_splits);
     return (rows * sizeof(float) + 255) / 256 * 256 + rows * head_dim * sizeof(float);
 }
@@ -345,7 +345,7 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
         return st;
     // the split-K grid covers only what the segments leave: at most max_rest_len tokens
     const rlt::DecodePlan plan = rlt::plan_decode(batch, num_q_heads, pool->num_kv_heads,
-                                                  pool->head_dim, max_rest_len, split_tokens, sms);
+                                                  pool->head_dim, max_rest_len, split_tokens, sms, rlt::kRestWaves);
     const int32_t stride = max_prefix_slots + plan.max_splits;
     const size_t rows = (size_t)batch * num_q_heads * stride;
     const size_t lse_bytes = (rows * sizeof(float) + 255) / 256 * 256;
@@ -392,11 +392,11 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
         ctas = std::min(max_ctas, sms);
     } else if (max_rest_len > 0 && sms > 1) {
         // both kernels at once: SMs in proportion to their tokens (the rest's length is
-        // its longest, 3/4 of it on average), weighted 3:1 for the tensor-core kernel's
+        // its longest, 3/4 of it on average), weighted 9:4 for the tensor-core kernel's
         // lower rate per SM on the short runs a split plan leaves it
         const double pre = (double)work_units * chunk_tiles * rlt::kPrefixTile;
         const double rest = 0.75 * (double)batch * max_rest_len;
-        const double share = std::min(1.0, 3.0 * pre / (pre + rest));
+        const double share = std::min(1.0, 2.25 * pre / (pre + rest));
         ctas = std::max(1, std::min(sms - 1, (int)std::ceil(sms * share)));
     }
     pp.ctas = (int32_t)std::min<int64_t>(ctas, items);

@@ -419,16 +419,25 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
 
 // Merge the partials of one (request, query head): its shared-prefix slots
 // [0, n_pre) and split-K slots [prefix_slots, prefix_slots + n); a slot whose
-// lse is -inf holds no partial and is skipped.  Four warps per pair (lanes over
-// the D dims), then their (max, sum, vector) fold through shared memory.
+// lse is -inf holds no partial (a tensor-core run marks the chunk slots it merged
+// that way).  Four warps per pair.  The slots are taken in windows of
+// kCombineWindow: every thread reads its slots' lse values at once, the live ones
+// are listed in shared memory, and then only those partials are read, each warp
+// with all of its loads in flight; the warps' (sum, vector) fold at the end.
 constexpr int kCombineWarps = 4;
+constexpr int kCombineThreads = kCombineWarps * 32;
+constexpr int kCombineWindow = 1024;
 
 template <int D>
-__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeParams p)
 {
     constexpr int DPL = D / 32;
+    constexpr int kPer = kCombineWindow / kCombineThreads;   // lse values per thread per window
     __shared__ float red_m[kCombineWarps], red_l[kCombineWarps];
     __shared__ __align__(16) float red_o[kCombineWarps][D];
+    __shared__ int live_slot[kCombineWindow];
+    __shared__ float live_w[kCombineWindow];
+    __shared__ int live_off[kPer * kCombineWarps + 1];
     const int64_t bh = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = (int)(bh / p.num_q_heads);
@@ -452,11 +461,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
         return bh * p.part_stride + (s < n_pre ? s : p.prefix_slots + (s - n_pre));
     };
 
-    // Pass 1: the slots' log2-sum-exps; thread t keeps slot t (the common case of at
-    // most 128 slots reads them once) and the block maximum.
-    const float l_own = threadIdx.x < total ? p.lse_part[slot_of(threadIdx.x)] : -CUDART_INF_F;
-    float M = l_own;
-    for (int s = threadIdx.x + kCombineWarps * 32; s < total; s += kCombineWarps * 32)
+    // the largest lse over all slots (independent loads)
+    float M = -CUDART_INF_F;
+    for (int s = threadIdx.x; s < total; s += kCombineThreads)
         M = fmaxf(M, p.lse_part[slot_of(s)]);
     M = warp_max_xor(M, 1);
     if (lane == 0)
@@ -471,46 +478,80 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     for (int d = 0; d < DPL; ++d)
         acc[d] = 0.f;
     float ls = 0.f;
-    if (M != -CUDART_INF_F) {
-        // Pass 2: warps take 32-slot blocks in turn; the live slots of a block (finite
-        // lse; a tensor-core run marks the chunk slots it merged with -inf, and a slot
-        // without a partial may hold anything) are read 8 at a time, all 8 loads in
-        // flight before the first is used.
-        for (int s0 = warp * 32; s0 < total; s0 += kCombineWarps * 32) {
-            const int s = s0 + lane;
-            const float l = s0 == warp * 32 ? l_own : (s < total ? p.lse_part[slot_of(s)] : -CUDART_INF_F);
-            const float wgt = l != -CUDART_INF_F ? exp2f(l - M) : 0.f;
-            ls += wgt;
-            const int nblk = min(32, total - s0);
-            for (int k0 = 0; k0 < nblk; k0 += 8) {
-                float wk[8];
-                float o[8][DPL];
+    for (int w0 = 0; M != -CUDART_INF_F && w0 < total; w0 += kCombineWindow) {
+        // list this window's live slots in slot order with their weights: a ballot per
+        // (value index, warp), one scan of the 32 counts, then each live lane's place
+        float l[kPer];
+        unsigned bal[kPer];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    wk[k] = __shfl_sync(kFullMask, wgt, (k0 + k) & 31);
-                    if (k0 + k >= nblk)
-                        wk[k] = 0.f;
-                    const float *op = p.o_part + slot_of(s0 + k0 + k) * D + lane * DPL;
-                    if constexpr (DPL == 4) {
-                        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (wk[k] != 0.f)
-                            v = *reinterpret_cast<const float4 *>(op);
-                        o[k][0] = v.x; o[k][1] = v.y; o[k][2] = v.z; o[k][3] = v.w;
-                    } else {
-                        float2 v = make_float2(0.f, 0.f);
-                        if (wk[k] != 0.f)
-                            v = *reinterpret_cast<const float2 *>(op);
-                        o[k][0] = v.x; o[k][1] = v.y;
-                    }
-                }
+        for (int i = 0; i < kPer; ++i) {
+            const int s = w0 + i * kCombineThreads + threadIdx.x;
+            l[i] = s < total ? p.lse_part[slot_of(s)] : -CUDART_INF_F;
+        }
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
+        for (int i = 0; i < kPer; ++i) {
+            bal[i] = __ballot_sync(kFullMask, l[i] != -CUDART_INF_F);
+            if (lane == 0)
+                live_off[i * kCombineWarps + warp] = __popc(bal[i]);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            static_assert(kPer * kCombineWarps == 32, "one count per lane");
+            const int c = live_off[lane];
+            int x = c;
 #pragma unroll
-                    for (int d = 0; d < DPL; ++d)
-                        acc[d] = fmaf(wk[k], o[k][d], acc[d]);
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFullMask, x, o);
+                if (lane >= o)
+                    x += y;
+            }
+            __syncwarp();
+            live_off[lane] = x - c;               // exclusive prefix
+            if (lane == 31)
+                live_off[32] = x;                 // live slots in the window
+        }
+        __syncthreads();
+        const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            if (l[i] != -CUDART_INF_F) {
+                const int k = live_off[i * kCombineWarps + warp] + __popc(bal[i] & below);
+                live_slot[k] = w0 + i * kCombineThreads + threadIdx.x;
+                live_w[k] = exp2f(l[i] - M);
             }
         }
-        ls = warp_sum_xor(ls, 1);
+        __syncthreads();
+        // warps take the live partials in turn, eight loads in flight
+        const int nl = live_off[32];
+        for (int k0 = warp * 8; k0 < nl; k0 += kCombineWarps * 8) {
+            float o[8][DPL];
+            float wk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = k0 + i;
+                wk[i] = k < nl ? live_w[k] : 0.f;
+                const float *op = p.o_part + slot_of(k < nl ? live_slot[k] : 0) * D + lane * DPL;
+                if constexpr (DPL == 4) {
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (k < nl)
+                        v = *reinterpret_cast<const float4 *>(op);
+                    o[i][0] = v.x; o[i][1] = v.y; o[i][2] = v.z; o[i][3] = v.w;
+                } else {
+                    float2 v = make_float2(0.f, 0.f);
+                    if (k < nl)
+                        v = *reinterpret_cast<const float2 *>(op);
+                    o[i][0] = v.x; o[i][1] = v.y;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                ls += wk[i];
+#pragma unroll
+                for (int d = 0; d < DPL; ++d)
+                    acc[d] = fmaf(wk[i], o[i][d], acc[d]);
+            }
+        }
+        __syncthreads();                         // the list is rebuilt for the next window
     }
     if (lane == 0)
         red_l[warp] = ls;
@@ -550,7 +591,7 @@ template <int D>
 cudaError_t launch_combine_typed(const DecodeParams &p, cudaStream_t stream)
 {
     const int64_t pairs = (int64_t)p.batch * p.num_q_heads;
-    decode_combine_kernel<D><<<(unsigned)pairs, kCombineWarps * 32, 0, stream>>>(p);
+    decode_combine_kernel<D><<<(unsigned)pairs, kCombineThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -591,7 +632,7 @@ bool decode_supported(int head_dim, int group)
 }
 
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
-                       int32_t head_dim, int32_t max_seq_len, int32_t split_tokens, int num_sms)
+                       int32_t head_dim, int32_t max_seq_len, int32_t split_tokens, int num_sms, int waves)
 {
     DecodePlan plan{};
     const int64_t max_tiles = max_seq_len > 0 ? (max_seq_len + kTileTokens - 1) / kTileTokens : 1;
@@ -599,9 +640,9 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
     if (split_tokens > 0) {
         tiles = (split_tokens + kTileTokens - 1) / kTileTokens;
     } else {
-        // Largest split (fewest partials) that still gives every SM several
+        // Largest split (fewest partials) that still gives every SM `waves`
         // waves of CTAs at 3 resident CTAs per SM.
-        const int64_t target = (int64_t)(num_sms > 0 ? num_sms : 148) * 3 * 8;
+        const int64_t target = (int64_t)(num_sms > 0 ? num_sms : 148) * 3 * waves;
         tiles = 128;
         while (tiles > 8 &&
                (int64_t)batch * num_kv_heads * ((max_tiles + tiles - 1) / tiles) < target)

@@ -79,8 +79,14 @@ struct DecodePlan {
     size_t lse_part_bytes;       // offset of o_part inside the workspace
 };
 
+// waves: the library's split (split_tokens == 0) is the largest that still gives
+// every SM this many waves of 3 CTAs; 8 for plain decode, fewer for the short
+// unshared rests a shared-prefix call leaves, which share the GPU with the
+// tensor-core kernel.
+constexpr int kPlainWaves = 8, kRestWaves = 3;
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
-                       int32_t head_dim, int32_t max_seq_len, int32_t split_tokens, int num_sms);
+                       int32_t head_dim, int32_t max_seq_len, int32_t split_tokens, int num_sms,
+                       int waves = kPlainWaves);
 
 bool decode_supported(int head_dim, int group);
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, cudaStream_t stream);
