@@ -152,22 +152,23 @@ def bf16_peak() -> float:
         return 1900.0
 
 
-def profiled_traffic(workload: str, cascade: bool):
-    """Per-launch DRAM bytes of the call's dominant kernel from the committed ncu summary,
-    if it was taken on this workload and on the kernel's current source."""
+def profiled_traffic(workload: str):
+    """DRAM bytes of one attention call (all its kernels) from the committed ncu summary
+    profiles/traffic_<workload>.txt, if it was taken on the kernels' current sources."""
     import hashlib
-    name, src = (("prefix_traffic.txt", "attn_prefix.cu") if cascade else ("attn_traffic.txt", "attn.cu"))
     try:
-        text = open(os.path.join(ROOT, "profiles", name)).read()
+        text = open(os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")).read()
     except OSError:
         return None
     lines = {k.strip(): v.strip() for k, v in (l.split(":", 1) for l in text.splitlines() if ":" in l)}
-    src_path = os.path.join(ROOT, "paged_kv_looped_gb300", "csrc", src)
-    digest = hashlib.sha256(open(src_path, "rb").read()).hexdigest()[:16]
-    if lines.get("source_sha256_16") != digest or lines.get("workload") != workload:
+    srcs = lines.get("sources", "").split()
+    if not srcs:
+        return None
+    blob = b"".join(open(os.path.join(ROOT, "paged_kv_looped_gb300", "csrc", f), "rb").read() for f in srcs)
+    if lines.get("sources_sha256_16") != hashlib.sha256(blob).hexdigest()[:16] or lines.get("workload") != workload:
         return None
     try:
-        return float(lines["dram_bytes_per_full_launch"])
+        return float(lines["dram_bytes_per_call"])
     except (KeyError, ValueError):
         return None
 
@@ -589,7 +590,7 @@ def main():
     a_bytes = attn_bytes(case)
     peak, peak_kind = hbm_peak()
     achieved = a_bytes / (attn_launch_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(case.name, r["cascade"])
+    traffic = profiled_traffic(case.name)
 
     cpu = None
     if rank == 0 and args.cpu_budget > 0:
