@@ -377,23 +377,23 @@ def rlt_plan_prefix(page_table, seq_lens, page_size: int, chunk_tiles: int = 4,
     req = np.zeros((B, 2), np.int32)
     sizes = np.zeros(7, np.int32)
     lib = load()
-    null = ctypes.c_void_p(0)
     tails = 1 if private_tails else 0
-    st = lib.rlt_plan_prefix(ptp, pt.shape[1], slp, B, page_size, chunk_tiles, query_group, tails, null, 0,
-                             null, null, 0,
-                             req.ctypes.data_as(ctypes.c_void_p), sizes.ctypes.data_as(ctypes.c_void_p))
-    if st not in (0, 2):
-        raise RltError(st, "rlt_plan_prefix")
-    seg = np.zeros((max(int(sizes[0]), 1), SEG_FIELDS), np.int32)
-    mem = np.zeros(max(int(sizes[1]), 1), np.int32)
-    lim = np.zeros(max(int(sizes[1]), 1), np.int32)
-    if st == 2:
-        _check(lib.rlt_plan_prefix(ptp, pt.shape[1], slp, B, page_size, chunk_tiles, query_group, tails,
-                                   seg.ctypes.data_as(ctypes.c_void_p), seg.shape[0],
-                                   mem.ctypes.data_as(ctypes.c_void_p), lim.ctypes.data_as(ctypes.c_void_p),
-                                   mem.size,
-                                   req.ctypes.data_as(ctypes.c_void_p), sizes.ctypes.data_as(ctypes.c_void_p)),
-               "rlt_plan_prefix")
+    # one call with room for the usual plan (segments <= 2B: fewer than B shared member sets
+    # plus B tails); a plan that needs more reports its sizes and is made again
+    seg_cap, mem_cap = 2 * B + 1, 4 * B + 1
+    for _ in range(2):
+        seg = np.zeros((seg_cap, SEG_FIELDS), np.int32)
+        mem = np.zeros(mem_cap, np.int32)
+        lim = np.zeros(mem_cap, np.int32)
+        st = lib.rlt_plan_prefix(ptp, pt.shape[1], slp, B, page_size, chunk_tiles, query_group, tails,
+                                 seg.ctypes.data_as(ctypes.c_void_p), seg_cap,
+                                 mem.ctypes.data_as(ctypes.c_void_p), lim.ctypes.data_as(ctypes.c_void_p),
+                                 mem_cap, req.ctypes.data_as(ctypes.c_void_p),
+                                 sizes.ctypes.data_as(ctypes.c_void_p))
+        if st != 2:
+            break
+        seg_cap, mem_cap = max(int(sizes[0]), 1), max(int(sizes[1]), 1)
+    _check(st, "rlt_plan_prefix")
     n = int(sizes[0])
     return PrefixPlan(seg[:n], mem[: int(sizes[1])], lim[: int(sizes[1])], req, sizes, chunk_tiles, query_group)
 

@@ -848,57 +848,70 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
         return RLT_ERR_UNSUPPORTED;
     const int per_tile = page_size < kPrefixTile ? kPrefixTile / page_size : 1;
 
-    // tile t of request b is keyed by the page ids (and, for big pages, the offset) it covers
-    auto key = [&](int b, int t) {
-        std::vector<int32_t> k;
+    // requests b and c share tile t when they map it to the same pages (for pages larger
+    // than a tile, the same page: the in-page offset is t's in both)
+    auto same_tile = [&](int b, int c, int t) {
         const int64_t tok = (int64_t)t * kPrefixTile;
-        for (int j = 0; j < per_tile; ++j)
-            k.push_back(page_table[(int64_t)b * max_pages + (tok + (int64_t)j * page_size) / page_size]);
-        if (page_size > kPrefixTile)
-            k.push_back((int32_t)(tok % page_size));
-        return k;
+        const int32_t *rb = page_table + (int64_t)b * max_pages, *rc = page_table + (int64_t)c * max_pages;
+        for (int j = 0; j < per_tile; ++j) {
+            const int64_t idx = (tok + (int64_t)j * page_size) / page_size;
+            if (rb[idx] != rc[idx])
+                return false;
+        }
+        return true;
     };
-    auto full_tiles = [&](int b) {
+    std::vector<int> full_tiles(batch);
+    for (int b = 0; b < batch; ++b) {
         const int64_t L = std::min<int64_t>(std::max(seq_lens[b], 0), (int64_t)max_pages * page_size);
-        return (int)(L / kPrefixTile);
-    };
+        full_tiles[b] = (int)(L / kPrefixTile);
+    }
 
     // mem: member requests; lim: each member's key count in the segment (its shared tokens)
     struct Seg { int first, tiles, parent; std::vector<int> mem; int64_t end_token; std::vector<int64_t> lim; };
     std::vector<Seg> segs;
     std::vector<int> deepest(batch, -1);       // segment holding each request's last shared tile
     struct Group { std::vector<int> mem; int seg; };
-    std::vector<Group> level;
+    std::vector<Group> level, next;
     {
         Group root{{}, -1};
         for (int b = 0; b < batch; ++b)
-            if (full_tiles(b) > 0)
+            if (full_tiles[b] > 0)
                 root.mem.push_back(b);
         if (root.mem.size() >= 2)
             level.push_back(root);
     }
+    // walk the trie of tiles from position 0: at tile t each group of requests that agreed
+    // on tiles 0..t-1 splits by tile t's pages (a bucket: the requests whose tile t matches
+    // the first remaining one's); buckets of >= 2 requests go on
+    std::vector<int> rest, bucket, others;
     for (int t = 0; !level.empty(); ++t) {
-        std::vector<Group> next;
+        next.clear();
         for (const Group &grp : level) {
-            std::map<std::vector<int32_t>, std::vector<int>> buckets;
+            rest.clear();
             for (int b : grp.mem)
-                if (full_tiles(b) > t)
-                    buckets[key(b, t)].push_back(b);
-            for (auto &kv : buckets) {
-                if (kv.second.size() < 2)
+                if (full_tiles[b] > t)
+                    rest.push_back(b);
+            while (rest.size() >= 2) {
+                const int rep = rest[0];
+                bucket.clear();
+                others.clear();
+                for (int b : rest)
+                    (b == rep || same_tile(b, rep, t) ? bucket : others).push_back(b);
+                rest.swap(others);
+                if (bucket.size() < 2)
                     continue;                      // not shared: that request's prefix ends here
                 int s;
-                if (grp.seg >= 0 && kv.second == segs[grp.seg].mem &&
+                if (grp.seg >= 0 && bucket == segs[grp.seg].mem &&
                     segs[grp.seg].first + segs[grp.seg].tiles == t) {
                     s = grp.seg;                   // same members: the segment grows
                     segs[s].tiles++;
                 } else {
                     s = (int)segs.size();
-                    segs.push_back({t, 1, grp.seg, kv.second, 0});
+                    segs.push_back({t, 1, grp.seg, bucket, 0, {}});
                 }
-                for (int b : kv.second)
+                for (int b : bucket)
                     deepest[b] = s;
-                next.push_back({kv.second, s});
+                next.push_back({bucket, s});
             }
         }
         level.swap(next);
