@@ -177,13 +177,17 @@ def profiled_traffic(workload: str):
 
 def auto_chunk_tiles(rlt, case, tails, num_sms):
     """Tiles per work item of the persistent tensor-core kernel: the largest power of two
-    (1..16) that still gives every CTA (one per SM) at least 16 items, so that the
-    item-granular split of the work across the CTAs stays within a few percent."""
+    (4..16) that still gives every CTA (one per SM) at least 16 items, so that the
+    item-granular split of the work across the CTAs stays within a few percent; never
+    below 4 tiles (or a segment's length), since every item adds a partial to merge."""
     p1 = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, 1, tails, case.group)
     per_block = 128 // case.group
     tiles = sum(int(s[1]) * -(-int(s[4]) // per_block) for s in p1.segments) * case.num_kv_heads
+    longest = max((int(s[1]) for s in p1.segments), default=1)
     chunk = 16
-    while chunk > 1 and tiles / chunk < 16 * num_sms:
+    while chunk > 4 and tiles / chunk < 16 * num_sms:
+        chunk //= 2
+    while chunk > 1 and chunk > longest:
         chunk //= 2
     return chunk
 
@@ -287,6 +291,17 @@ def run_gpu(args, rank, world):
             if events is not None:
                 events[i][1].record(st)
 
+    def attention_only(st):
+        """Every bank's attention call and nothing else (for the per-call roofline timing)."""
+        for i, bank in enumerate(banks):
+            if plan is not None:
+                rlt.rlt_paged_decode_attn_prefix(pool, bank, q[i], pt, sl, case.max_seq_len, plan, out=out[i],
+                                                 workspace=ws, split_tokens=args.split_tokens,
+                                                 max_ctas=args.prefix_ctas, stream=st)
+            else:
+                rlt.rlt_paged_decode_attn(pool, bank, q[i], pt, sl, case.max_seq_len, out=out[i], workspace=ws,
+                                          split_tokens=args.split_tokens, stream=st)
+
     def new_events(external):
         kw = {"external": True} if external else {}
         return [(torch.cuda.Event(enable_timing=True, **kw), torch.cuda.Event(enable_timing=True, **kw))
@@ -303,19 +318,24 @@ def run_gpu(args, rank, world):
         step(stream)
     assert rlt.rlt_get_device_error() == 0
 
-    # the whole step as one CUDA-graph submission (every call is stream-capturable); a second
-    # capture brackets each attention call with event-record nodes, for the roofline timing
-    graph = timed_graph = graph_events = None
+    # the whole step as one CUDA-graph submission (every call is stream-capturable); a graph of
+    # the attention calls alone gives the roofline's per-call time, and a capture bracketing each
+    # attention call with event-record nodes gives each call's time on its own (reported beside it)
+    graph = timed_graph = graph_events = attn_graph = None
     if args.graph == "on":
-        def capture(events=None):
+        def capture(events=None, fn=None):
             side = torch.cuda.Stream(dev)
             side.wait_stream(stream)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=side):
-                step(side, events)
+                if fn is None:
+                    step(side, events)
+                else:
+                    fn(side)
             stream.wait_stream(side)
             return g
         graph = capture()
+        attn_graph = capture(fn=attention_only)
         try:
             graph_events = new_events(external=True)
             timed_graph = capture(graph_events)
@@ -342,6 +362,18 @@ def run_gpu(args, rank, world):
             run_step()
         t1.record(stream)
         barrier()
+        # the attention calls alone, back to back in one graph as the step submits them: events
+        # around the replays, the average call = elapsed / calls
+        attn_call_ms = None
+        if attn_graph is not None:
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(args.steps):
+                attn_graph.replay()
+            a1.record(stream)
+            torch.cuda.synchronize(dev)
+            attn_call_ms = a0.elapsed_time(a1) / (args.steps * len(banks))
         # each attention call on the device, an event pair around it, step by step
         attn_ms = []
         for _ in range(args.steps):
@@ -356,7 +388,8 @@ def run_gpu(args, rank, world):
                 attn_ms += [a.elapsed_time(b) for a, b in events]
         barrier()
     ms_total = t0.elapsed_time(t1)
-    attn_timing = "CUDA-graph event nodes" if timed_graph is not None else "eager event pairs"
+    attn_timing = ("attention-only CUDA graph (every bank's call back to back), events around the replays"
+                   if attn_call_ms is not None else "eager event pairs")
     assert rlt.rlt_get_device_error() == 0
 
     # ---- extend (span) attention, when asked: N new tokens per request attend causally over
@@ -434,7 +467,7 @@ def run_gpu(args, rank, world):
     launches = args.steps * (len(banks) * per_lp + (1 if nz is not None else 0))
     return dict(case=case, banks=banks, cascade=plan is not None, graph=graph is not None, attn_timing=attn_timing,
                 extend=extend,
-                ms_total=ms_total, attn_ms=attn_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+                ms_total=ms_total, attn_ms=attn_ms, attn_call_ms=attn_call_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                 clocks=clocks.summary(), launches=launches, combine=combine, ws_bytes=ws_bytes)
 
 
@@ -586,7 +619,8 @@ def main():
     value = job_gbs(step_bytes, world, ms_max)
     e2e_value = job_gbs(step_bytes, world, e2e_ms_step)
 
-    attn_launch_ms = statistics.mean(r["attn_ms"])
+    attn_isolated_ms = statistics.mean(r["attn_ms"])
+    attn_launch_ms = r["attn_call_ms"] if r["attn_call_ms"] is not None else attn_isolated_ms
     a_bytes = attn_bytes(case)
     peak, peak_kind = hbm_peak()
     achieved = a_bytes / (attn_launch_ms * 1e-3) / 1e9
@@ -614,7 +648,8 @@ def main():
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": f"{peak_kind} (HBM copy)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": a_bytes, "launch_us": round(attn_launch_ms * 1e3, 2),
-                     "timing": r["attn_timing"]},
+                     "timing": r["attn_timing"],
+                     "launch_us_event_nodes": round(attn_isolated_ms * 1e3, 2)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"]},
