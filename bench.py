@@ -202,6 +202,8 @@ def run_gpu(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     case = W.config(args.workload)
+    if args.batch:      # the first N requests alone, on a compact pool (small case for profilers)
+        case = W.subcase(case, range(min(args.batch, case.batch)))
     lp = layer_planes(case)
     bmap, nbanks = rlt.rlt_bank_map(case.recurrent, case.num_planes)
     assert nbanks == len(lp)
@@ -596,6 +598,8 @@ def main():
                     help="CTAs of the persistent tensor-core kernel (0 = one per SM)")
     ap.add_argument("--banks", type=int, default=0,
                     help="run only the first N layer-plane banks (small-footprint case for profilers); 0 = all")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="run only the first N requests of the workload (small case for profilers); 0 = all")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU time for cpu_baseline")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

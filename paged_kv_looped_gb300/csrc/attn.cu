@@ -100,26 +100,75 @@ __device__ __forceinline__ void load_frag_global(const uint16_t *src, float (&f)
     load_frag<DPL>(reinterpret_cast<const unsigned char *>(src), f);
 }
 
+// Pairs of fp32 in one 64-bit register: Blackwell's packed f32x2 FMA / MUL do two
+// lanes' worth of work per instruction (each half rounded as its own fmaf / fmul).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ float2 f2_unpack(uint64_t v)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return make_float2(lo, hi);
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// A tile row's DPL bf16 dims of this lane as DPL/2 fp32 pairs (bf16 -> fp32 is exact).
+template <int DPL>
+__device__ __forceinline__ void load_frag2(const unsigned char *src, uint64_t (&f)[DPL / 2])
+{
+    if constexpr (DPL == 8) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(src);
+        f[0] = f2_pack(bf16_lo(w.x), bf16_hi(w.x));
+        f[1] = f2_pack(bf16_lo(w.y), bf16_hi(w.y));
+        f[2] = f2_pack(bf16_lo(w.z), bf16_hi(w.z));
+        f[3] = f2_pack(bf16_lo(w.w), bf16_hi(w.w));
+    } else {
+        static_assert(DPL == 4, "head_dim 64 or 128");
+        const uint2 w = *reinterpret_cast<const uint2 *>(src);
+        f[0] = f2_pack(bf16_lo(w.x), bf16_hi(w.x));
+        f[1] = f2_pack(bf16_lo(w.y), bf16_hi(w.y));
+    }
+}
+
 // acc[h] += p[h][t] * V_t for the 8 rows t of this lane's half of a tile.  In
 // the last tile of a request, rows past its end are skipped: that pool memory
 // may hold anything, even NaN patterns, and 0 * NaN would poison the sum.
 template <int D, int G, bool kMasked>
 __device__ __forceinline__ void pv_tile(const unsigned char *vs, const float *pbuf, int half,
-                                        int j, int valid, float (&acc)[G][D / 16])
+                                        int j, int valid, uint64_t (&acc)[G][D / 32])
 {
     constexpr int DPL = D / 16;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
         if (kMasked && half * 8 + r >= valid)
             continue;
-        float vf[DPL];
-        load_frag<DPL>(vs + ((half * 8 + r) * D + j * DPL) * 2, vf);
+        uint64_t vf[DPL / 2];
+        load_frag2<DPL>(vs + ((half * 8 + r) * D + j * DPL) * 2, vf);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             const float pw = pbuf[h * kTileTokens + half * 8 + r];
+            const uint64_t pw2 = f2_pack(pw, pw);
 #pragma unroll
-            for (int d = 0; d < DPL; ++d)
-                acc[h][d] = fmaf(pw, vf[d], acc[h][d]);
+            for (int d = 0; d < DPL / 2; ++d)
+                acc[h][d] = f2_fma(pw2, vf[d], acc[h][d]);
         }
     }
 }
@@ -214,24 +263,27 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
         }
     };
 
-    // Query heads g*G .. g*G+G-1, this lane's dims, pre-scaled into log2 units.
-    float q[G][DPL];
+    // Query heads g*G .. g*G+G-1, this lane's dims, pre-scaled into log2 units, as fp32
+    // pairs; the accumulators are fp32 pairs too.
+    uint64_t q[G][DPL / 2];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-        load_frag_global<DPL>(p.q + ((int64_t)b * p.num_q_heads + g * G + h) * D + j * DPL, q[h]);
+        float qf[DPL];
+        load_frag_global<DPL>(p.q + ((int64_t)b * p.num_q_heads + g * G + h) * D + j * DPL, qf);
 #pragma unroll
-        for (int d = 0; d < DPL; ++d)
-            q[h][d] *= p.qscale;
+        for (int d = 0; d < DPL / 2; ++d)
+            q[h][d] = f2_pack(qf[2 * d] * p.qscale, qf[2 * d + 1] * p.qscale);
     }
 
-    float m[G], l[G], acc[G][DPL];
+    float m[G], l[G];
+    uint64_t acc2[G][DPL / 2];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
         m[h] = -CUDART_INF_F;
         l[h] = 0.f;
 #pragma unroll
-        for (int d = 0; d < DPL; ++d)
-            acc[h][d] = 0.f;
+        for (int d = 0; d < DPL / 2; ++d)
+            acc2[h][d] = f2_pack(0.f, 0.f);
     }
 
     const int n_prologue = my_count < kStages ? my_count : kStages;
@@ -260,15 +312,16 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
             float sc[G][8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
-                float kf[DPL];
-                load_frag<DPL>(ks + ((half * 8 + r) * D + j * DPL) * 2, kf);
+                uint64_t kf[DPL / 2];
+                load_frag2<DPL>(ks + ((half * 8 + r) * D + j * DPL) * 2, kf);
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    float a = 0.f;
+                    uint64_t a = f2_mul(q[h][0], kf[0]);
 #pragma unroll
-                    for (int d = 0; d < DPL; ++d)
-                        a = fmaf(q[h][d], kf[d], a);
-                    sc[h][r] = a;
+                    for (int d = 1; d < DPL / 2; ++d)
+                        a = f2_fma(q[h][d], kf[d], a);
+                    const float2 a2 = f2_unpack(a);
+                    sc[h][r] = a2.x + a2.y;
                 }
             }
             // Transpose butterfly over the 16 lanes of the half: afterwards lane j
@@ -307,9 +360,10 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
                 const float alpha = exp2f(m[h] - m_new);
                 const float pr = exp2f(s_t - m_new);
                 l[h] = l[h] * alpha + ((j & 1) ? 0.f : pr);
+                const uint64_t alpha2 = f2_pack(alpha, alpha);
 #pragma unroll
-                for (int d = 0; d < DPL; ++d)
-                    acc[h][d] *= alpha;
+                for (int d = 0; d < DPL / 2; ++d)
+                    acc2[h][d] = f2_mul(acc2[h][d], alpha2);
                 m[h] = m_new;
                 if ((j & 1) == 0)
                     pbuf[h * kTileTokens + t] = pr;
@@ -318,9 +372,9 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
 
             // acc += p_t * V_t over this half's rows.
             if (valid == kTileTokens)
-                pv_tile<D, G, false>(vs, pbuf, half, j, valid, acc);
+                pv_tile<D, G, false>(vs, pbuf, half, j, valid, acc2);
             else
-                pv_tile<D, G, true>(vs, pbuf, half, j, valid, acc);
+                pv_tile<D, G, true>(vs, pbuf, half, j, valid, acc2);
         }
         __syncwarp();
         fence_proxy_async();                   // our reads of stage s before its next refill
@@ -349,6 +403,15 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
         }
     }
 
+    float acc[G][DPL];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int d = 0; d < DPL / 2; ++d) {
+            const float2 v = f2_unpack(acc2[h][d]);
+            acc[h][2 * d] = v.x;
+            acc[h][2 * d + 1] = v.y;
+        }
     // Fold the two halves (same dims, different rows) and the per-lane sums.
 #pragma unroll
     for (int h = 0; h < G; ++h) {
