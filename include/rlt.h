@@ -5,8 +5,9 @@
  * C++ or framework types cross this boundary.  All array arguments of the
  * compute entry points are DEVICE pointers owned by the caller; the library
  * allocates no device memory and keeps no state besides a per-device error
- * word and, once a shared-prefix call needs it, a per-device side stream with
- * two events (rlt_paged_decode_attn_prefix).
+ * word, the fixed scratch array of rlt_paged_decode_attn_noalloc and, once a
+ * shared-prefix call needs it, a per-device side stream with two events
+ * (rlt_paged_decode_attn_prefix).
  * Every compute call is enqueued on the caller's stream (a cudaStream_t passed
  * as void*; NULL = the legacy default stream), returns without waiting for the
  * GPU, and makes no host/device synchronisation.  Arguments are checked on

@@ -148,6 +148,173 @@ __device__ __forceinline__ void load_frag2(const unsigned char *src, uint64_t (&
     }
 }
 
+// Merge the partials of one (request, query head): its shared-prefix slots
+// [0, n_pre) and split-K slots [prefix_slots, prefix_slots + n); a slot whose
+// lse is -inf holds no partial (a tensor-core run marks the chunk slots it merged
+// that way).  Four warps per pair.  The slots are taken in windows of
+// kCombineWindow: every thread reads its slots' lse values at once, the live ones
+// are listed in shared memory, and then only those partials are read, each warp
+// with all of its loads in flight; the warps' (sum, vector) fold at the end.
+// Partials are read through L2 (they may come from other CTAs of a running grid).
+constexpr int kCombineWarps = 4;
+constexpr int kCombineThreads = kCombineWarps * 32;
+constexpr int kCombineWindow = 1024;
+constexpr int kCombinePer = kCombineWindow / kCombineThreads;   // lse values per thread per window
+
+template <int D>
+struct MergeSmem {
+    float red_m[kCombineWarps], red_l[kCombineWarps];
+    alignas(16) float red_o[kCombineWarps][D];
+    int live_slot[kCombineWindow];
+    float live_w[kCombineWindow];
+    int live_off[kCombinePer * kCombineWarps + 1];
+};
+
+// Merge row bh (total = n_pre + n >= 1 slots) and write out[bh] and lse_out[bh].  Called by
+// all kCombineThreads threads of the CTA; sm may alias other shared memory of the caller.
+template <int D>
+__device__ void merge_row(const DecodeParams &p, int64_t bh, int n_pre, int n, MergeSmem<D> &sm)
+{
+    constexpr int DPL = D / 32;
+    constexpr int kPer = kCombinePer;
+    float *red_m = sm.red_m, *red_l = sm.red_l;
+    auto &red_o = sm.red_o;
+    int *live_slot = sm.live_slot, *live_off = sm.live_off;
+    float *live_w = sm.live_w;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = n_pre + n;
+    __syncthreads();                             // the shared buffers of an earlier merge are free
+    auto slot_of = [&](int s) -> int64_t {
+        return bh * p.part_stride + (s < n_pre ? s : p.prefix_slots + (s - n_pre));
+    };
+
+    // the largest lse over all slots (independent loads)
+    float M = -CUDART_INF_F;
+    for (int s = threadIdx.x; s < total; s += kCombineThreads)
+        M = fmaxf(M, __ldcg(p.lse_part + slot_of(s)));
+    M = warp_max_xor(M, 1);
+    if (lane == 0)
+        red_m[warp] = M;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w)
+        M = fmaxf(M, red_m[w]);
+
+    float acc[DPL];
+#pragma unroll
+    for (int d = 0; d < DPL; ++d)
+        acc[d] = 0.f;
+    float ls = 0.f;
+    for (int w0 = 0; M != -CUDART_INF_F && w0 < total; w0 += kCombineWindow) {
+        // list this window's live slots in slot order with their weights: a ballot per
+        // (value index, warp), one scan of the 32 counts, then each live lane's place
+        float l[kPer];
+        unsigned bal[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int s = w0 + i * kCombineThreads + threadIdx.x;
+            l[i] = s < total ? __ldcg(p.lse_part + slot_of(s)) : -CUDART_INF_F;
+        }
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            bal[i] = __ballot_sync(kFullMask, l[i] != -CUDART_INF_F);
+            if (lane == 0)
+                live_off[i * kCombineWarps + warp] = __popc(bal[i]);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            static_assert(kPer * kCombineWarps == 32, "one count per lane");
+            const int c = live_off[lane];
+            int x = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFullMask, x, o);
+                if (lane >= o)
+                    x += y;
+            }
+            __syncwarp();
+            live_off[lane] = x - c;               // exclusive prefix
+            if (lane == 31)
+                live_off[32] = x;                 // live slots in the window
+        }
+        __syncthreads();
+        const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            if (l[i] != -CUDART_INF_F) {
+                const int k = live_off[i * kCombineWarps + warp] + __popc(bal[i] & below);
+                live_slot[k] = w0 + i * kCombineThreads + threadIdx.x;
+                live_w[k] = exp2f(l[i] - M);
+            }
+        }
+        __syncthreads();
+        // warps take the live partials in turn, eight loads in flight
+        const int nl = live_off[32];
+        for (int k0 = warp * 8; k0 < nl; k0 += kCombineWarps * 8) {
+            float o[8][DPL];
+            float wk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = k0 + i;
+                wk[i] = k < nl ? live_w[k] : 0.f;
+                const float *op = p.o_part + slot_of(k < nl ? live_slot[k] : 0) * D + lane * DPL;
+                if constexpr (DPL == 4) {
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (k < nl)
+                        v = __ldcg(reinterpret_cast<const float4 *>(op));
+                    o[i][0] = v.x; o[i][1] = v.y; o[i][2] = v.z; o[i][3] = v.w;
+                } else {
+                    float2 v = make_float2(0.f, 0.f);
+                    if (k < nl)
+                        v = __ldcg(reinterpret_cast<const float2 *>(op));
+                    o[i][0] = v.x; o[i][1] = v.y;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                ls += wk[i];
+#pragma unroll
+                for (int d = 0; d < DPL; ++d)
+                    acc[d] = fmaf(wk[i], o[i][d], acc[d]);
+            }
+        }
+        __syncthreads();                         // the list is rebuilt for the next window
+    }
+    if (lane == 0)
+        red_l[warp] = ls;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d)
+        red_o[warp][lane * DPL + d] = acc[d];
+    __syncthreads();
+    if (warp != 0)
+        return;
+    ls = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w)
+        ls += red_l[w];
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) {
+        float a = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCombineWarps; ++w)
+            a += red_o[w][lane * DPL + d];
+        acc[d] = a;
+    }
+    const float inv = ls > 0.f ? 1.f / ls : 0.f;
+    uint16_t *o = p.out + bh * D + lane * DPL;
+    if constexpr (DPL == 4) {
+        uint2 w;
+        w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2 *>(o) = w;
+    } else {
+        *reinterpret_cast<uint32_t *>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+    if (lane == 0 && p.lse_out != nullptr)
+        p.lse_out[bh] = ls > 0.f ? (M + log2f(ls)) * kLn2 : -CUDART_INF_F;
+}
+
+
 // acc[h] += p[h][t] * V_t for the 8 rows t of this lane's half of a tile.  In
 // the last tile of a request, rows past its end are skipped: that pool memory
 // may hold anything, even NaN patterns, and 0 * NaN would poison the sum.
@@ -480,27 +647,10 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
     }
 }
 
-// Merge the partials of one (request, query head): its shared-prefix slots
-// [0, n_pre) and split-K slots [prefix_slots, prefix_slots + n); a slot whose
-// lse is -inf holds no partial (a tensor-core run marks the chunk slots it merged
-// that way).  Four warps per pair.  The slots are taken in windows of
-// kCombineWindow: every thread reads its slots' lse values at once, the live ones
-// are listed in shared memory, and then only those partials are read, each warp
-// with all of its loads in flight; the warps' (sum, vector) fold at the end.
-constexpr int kCombineWarps = 4;
-constexpr int kCombineThreads = kCombineWarps * 32;
-constexpr int kCombineWindow = 1024;
-
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeParams p)
 {
-    constexpr int DPL = D / 32;
-    constexpr int kPer = kCombineWindow / kCombineThreads;   // lse values per thread per window
-    __shared__ float red_m[kCombineWarps], red_l[kCombineWarps];
-    __shared__ __align__(16) float red_o[kCombineWarps][D];
-    __shared__ int live_slot[kCombineWindow];
-    __shared__ float live_w[kCombineWindow];
-    __shared__ int live_off[kPer * kCombineWarps + 1];
+    __shared__ MergeSmem<D> sm;
     const int64_t bh = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = (int)(bh / p.num_q_heads);
@@ -510,8 +660,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
     const int n = (n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
     if (n_pre == 0 && n == 1)
         return;                                  // written by the partial kernel
-    const int total = n_pre + n;
-    if (total == 0) {                            // empty request: out = 0, lse = -inf
+    if (n_pre + n == 0) {                        // empty request: out = 0, lse = -inf
         if (warp == 0) {
             for (int d = lane; d < D / 2; d += 32)
                 reinterpret_cast<uint32_t *>(p.out + bh * D)[d] = 0u;
@@ -520,134 +669,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
         }
         return;
     }
-    auto slot_of = [&](int s) -> int64_t {
-        return bh * p.part_stride + (s < n_pre ? s : p.prefix_slots + (s - n_pre));
-    };
-
-    // the largest lse over all slots (independent loads)
-    float M = -CUDART_INF_F;
-    for (int s = threadIdx.x; s < total; s += kCombineThreads)
-        M = fmaxf(M, p.lse_part[slot_of(s)]);
-    M = warp_max_xor(M, 1);
-    if (lane == 0)
-        red_m[warp] = M;
-    __syncthreads();
-#pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w)
-        M = fmaxf(M, red_m[w]);
-
-    float acc[DPL];
-#pragma unroll
-    for (int d = 0; d < DPL; ++d)
-        acc[d] = 0.f;
-    float ls = 0.f;
-    for (int w0 = 0; M != -CUDART_INF_F && w0 < total; w0 += kCombineWindow) {
-        // list this window's live slots in slot order with their weights: a ballot per
-        // (value index, warp), one scan of the 32 counts, then each live lane's place
-        float l[kPer];
-        unsigned bal[kPer];
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-            const int s = w0 + i * kCombineThreads + threadIdx.x;
-            l[i] = s < total ? p.lse_part[slot_of(s)] : -CUDART_INF_F;
-        }
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-            bal[i] = __ballot_sync(kFullMask, l[i] != -CUDART_INF_F);
-            if (lane == 0)
-                live_off[i * kCombineWarps + warp] = __popc(bal[i]);
-        }
-        __syncthreads();
-        if (warp == 0) {
-            static_assert(kPer * kCombineWarps == 32, "one count per lane");
-            const int c = live_off[lane];
-            int x = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(kFullMask, x, o);
-                if (lane >= o)
-                    x += y;
-            }
-            __syncwarp();
-            live_off[lane] = x - c;               // exclusive prefix
-            if (lane == 31)
-                live_off[32] = x;                 // live slots in the window
-        }
-        __syncthreads();
-        const unsigned below = (1u << lane) - 1u;
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-            if (l[i] != -CUDART_INF_F) {
-                const int k = live_off[i * kCombineWarps + warp] + __popc(bal[i] & below);
-                live_slot[k] = w0 + i * kCombineThreads + threadIdx.x;
-                live_w[k] = exp2f(l[i] - M);
-            }
-        }
-        __syncthreads();
-        // warps take the live partials in turn, eight loads in flight
-        const int nl = live_off[32];
-        for (int k0 = warp * 8; k0 < nl; k0 += kCombineWarps * 8) {
-            float o[8][DPL];
-            float wk[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int k = k0 + i;
-                wk[i] = k < nl ? live_w[k] : 0.f;
-                const float *op = p.o_part + slot_of(k < nl ? live_slot[k] : 0) * D + lane * DPL;
-                if constexpr (DPL == 4) {
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (k < nl)
-                        v = *reinterpret_cast<const float4 *>(op);
-                    o[i][0] = v.x; o[i][1] = v.y; o[i][2] = v.z; o[i][3] = v.w;
-                } else {
-                    float2 v = make_float2(0.f, 0.f);
-                    if (k < nl)
-                        v = *reinterpret_cast<const float2 *>(op);
-                    o[i][0] = v.x; o[i][1] = v.y;
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                ls += wk[i];
-#pragma unroll
-                for (int d = 0; d < DPL; ++d)
-                    acc[d] = fmaf(wk[i], o[i][d], acc[d]);
-            }
-        }
-        __syncthreads();                         // the list is rebuilt for the next window
-    }
-    if (lane == 0)
-        red_l[warp] = ls;
-#pragma unroll
-    for (int d = 0; d < DPL; ++d)
-        red_o[warp][lane * DPL + d] = acc[d];
-    __syncthreads();
-    if (warp != 0)
-        return;
-    ls = 0.f;
-#pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w)
-        ls += red_l[w];
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) {
-        float a = 0.f;
-#pragma unroll
-        for (int w = 0; w < kCombineWarps; ++w)
-            a += red_o[w][lane * DPL + d];
-        acc[d] = a;
-    }
-    const float inv = ls > 0.f ? 1.f / ls : 0.f;
-    uint16_t *o = p.out + bh * D + lane * DPL;
-    if constexpr (DPL == 4) {
-        uint2 w;
-        w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-        *reinterpret_cast<uint2 *>(o) = w;
-    } else {
-        *reinterpret_cast<uint32_t *>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    }
-    if (lane == 0 && p.lse_out != nullptr)
-        p.lse_out[bh] = ls > 0.f ? (M + log2f(ls)) * kLn2 : -CUDART_INF_F;
+    merge_row<D>(p, bh, n_pre, n, sm);
 }
 
 template <int D>
@@ -710,6 +732,10 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
         while (tiles > 8 &&
                (int64_t)batch * num_kv_heads * ((max_tiles + tiles - 1) / tiles) < target)
             tiles /= 2;
+        // A call this small is bound by launches and latency: one split per request
+        // writes the output directly and saves the combine launch.
+        if (max_tiles <= 128 && (int64_t)batch * num_kv_heads * max_tiles <= target)
+            tiles = 128;
     }
     if (tiles > 128)
         tiles = 128;                             // one page-table entry per lane per warp
