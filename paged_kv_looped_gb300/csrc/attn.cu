@@ -188,9 +188,17 @@ __device__ void merge_row(const DecodeParams &p, int64_t bh, int n_pre, int n, M
         return bh * p.part_stride + (s < n_pre ? s : p.prefix_slots + (s - n_pre));
     };
 
-    // the largest lse over all slots (independent loads)
+    // the largest lse over all slots (independent loads); the first window's values stay
+    // in registers for the live-slot list below
+    float l0[kPer];
     float M = -CUDART_INF_F;
-    for (int s = threadIdx.x; s < total; s += kCombineThreads)
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int s = i * kCombineThreads + threadIdx.x;
+        l0[i] = s < total ? __ldcg(p.lse_part + slot_of(s)) : -CUDART_INF_F;
+        M = fmaxf(M, l0[i]);
+    }
+    for (int s = kCombineWindow + threadIdx.x; s < total; s += kCombineThreads)
         M = fmaxf(M, __ldcg(p.lse_part + slot_of(s)));
     M = warp_max_xor(M, 1);
     if (lane == 0)
@@ -213,7 +221,7 @@ __device__ void merge_row(const DecodeParams &p, int64_t bh, int n_pre, int n, M
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
             const int s = w0 + i * kCombineThreads + threadIdx.x;
-            l[i] = s < total ? __ldcg(p.lse_part + slot_of(s)) : -CUDART_INF_F;
+            l[i] = w0 == 0 ? l0[i] : s < total ? __ldcg(p.lse_part + slot_of(s)) : -CUDART_INF_F;
         }
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
