@@ -1,10 +1,11 @@
 // Position-keyed latent-state noise for sm_103a.
 //
-// vllm-rlt PR #152, Summary para 2: each token's initial latent state is a
-// function of (request seed, position, channel): a stage-wise SplitMix64-style
-// hash gives a 24-bit uniform, and an inverse normal CDF maps it onto a normal
-// with std = initializer_range truncated at +-3 sigma.  64-bit arithmetic wraps
-// mod 2^64 exactly as on the CPU, so the 24 bits are identical everywhere.
+// vllm-rlt PR #152, Summary para 2: the latent state a token starts from depends
+// on (request seed, position, channel) only.  SplitMix64 steps fold the three in
+// one after another; the top 24 bits of the result pick a uniform cell, and the
+// inverse CDF of a normal (std initializer_range) cut off at +-3 sigma turns it
+// into the value.  The 64-bit arithmetic is exact mod 2^64 on either side, so
+// the 24 bits agree bit for bit with a CPU computation.
 //
 // One stage and one erfinvf per value, written with coalesced 16-byte stores
 // (noise_kernel); the seed and position stages are hashed once per 16 values.

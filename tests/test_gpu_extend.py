@@ -1,7 +1,7 @@
 """GPU parity of causal extend (span) attention on tcgen05 against the fp64 oracle.
 
 "Faster fuzzy minds", LOTUS: a block of positions is re-forwarded several times
-in place, each pass one parallel extend-prefill over the whole block after its
+in place, every pass attending over the whole block at once after its
 K/V were written back to the same slots; packed prefill is the same call over a
 whole prompt.  Bar: the attention tolerance (2e-2 abs or 1e-2 rel), lse within
 1e-3.

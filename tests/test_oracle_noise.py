@@ -1,13 +1,13 @@
 """Pins of the oracle's position-keyed latent noise against things other than itself.
 
-vllm-rlt PR #152 (Summary, para 2; Tests): the initial latent state of each
-token is a function of (request seed, position, channel); a stage-wise
-SplitMix64-style hash gives a 24-bit uniform that an inverse normal CDF maps
-to a normal with std = initializer_range truncated at +-3 sigma.  The PR's
-CPU suite checks batch independence, seed and position keying, no
-seed/channel aliasing, and the truncated-normal moments and tail mass; those
-checks, the published SplitMix64 outputs and library/closed-form values of the
-truncated normal pin the oracle here.
+vllm-rlt PR #152 (Summary, para 2; Tests): the latent state a token starts
+from depends only on (request seed, position, channel), hashed by SplitMix64
+steps down to 24 uniform bits and mapped by the inverse CDF of a normal with
+std = initializer_range, cut off at +-3 sigma.  The PR's CPU suite is said to
+check that the draws do not depend on the batch, follow seed and position, do
+not alias seed and channel, and have the cut-off normal's moments and tail
+mass; those checks, the published SplitMix64 outputs and library/closed-form
+values of the truncated normal pin the oracle here.
 """
 import math
 import os
