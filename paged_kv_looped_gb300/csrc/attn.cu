@@ -17,7 +17,8 @@
 //  * Inside a tile a half-warp holds 8 token rows, each lane D/16 dims:
 //    16-byte (D=128) shared loads without bank conflicts, scores reduced by a
 //    transpose butterfly (8 shuffles for 8 tokens), probabilities broadcast
-//    through shared memory for the P.V accumulation.
+//    through shared memory for the P.V accumulation.  The dot products and the
+//    accumulation run on packed fp32 pairs (f32x2 FMA), half the instructions.
 //  * Splits write (o, log2-sum-exp) partials; the combine kernel merges them.
 //    Requests with one split write their output directly.
 #include <math_constants.h>
