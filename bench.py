@@ -1,8 +1,10 @@
 """Benchmark of the paged-KV decode step of a looped transformer on GB300.
 
 One step = one decode token for every request of the batch through every
-(layer, plane) bank of the model: for each bank, append this step's K/V rows
-(rlt_kv_append) and run split-K paged decode attention (rlt_paged_decode_attn);
+(layer, plane) bank of the model: for each bank, append this step's K/V rows and
+run paged decode attention over them (by default one call does both:
+rlt_paged_decode_attn / _prefix with k_new, v_new; --append plain times
+rlt_kv_append as its own launch);
 workloads whose model draws latent noise (Huginn-shaped) also initialise the new
 tokens' latent state (rlt_latent_noise_init).  All inputs are seeded and
 synthetic; every bank's KV lives in its own region of HBM.
@@ -51,6 +53,12 @@ def attn_bytes(case: W.PagedCase, unique: bool = True) -> int:
 def append_bytes(case: W.PagedCase) -> int:
     n = int((case.new_slots >= 0).sum())
     return n * case.num_kv_heads * case.head_dim * 2 * 2 * 2 + case.batch * 8
+
+
+def fused_append_bytes(case: W.PagedCase) -> int:
+    """The append's bytes when the attention call does it: new rows read, pool rows written
+    (no slot list: the slot comes from the page table the call reads anyway)."""
+    return append_bytes(case) - case.batch * 8
 
 
 def noise_bytes(case: W.PagedCase) -> int:
@@ -152,9 +160,10 @@ def bf16_peak() -> float:
         return 1900.0
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, fused: bool):
     """DRAM bytes of one attention call (all its kernels) from the committed ncu summary
-    profiles/traffic_<workload>.txt, if it was taken on the kernels' current sources."""
+    profiles/traffic_<workload>.txt, if it was taken on the kernels' current sources and
+    with the append in the same form (fused into the call or not)."""
     import hashlib
     try:
         text = open(os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")).read()
@@ -166,6 +175,8 @@ def profiled_traffic(workload: str):
         return None
     blob = b"".join(open(os.path.join(ROOT, "paged_kv_looped_gb300", "csrc", f), "rb").read() for f in srcs)
     if lines.get("sources_sha256_16") != hashlib.sha256(blob).hexdigest()[:16] or lines.get("workload") != workload:
+        return None
+    if (lines.get("append", "plain") == "fused") != fused:
         return None
     try:
         return float(lines["dram_bytes_per_call"])
@@ -279,30 +290,29 @@ def run_gpu(args, rank, world):
             if args.append == "rope":
                 rlt.rlt_kv_append_rope(pool, bank, kn[i], vn[i], new_pos, loc, case.head_dim, 10000.0,
                                        request=req_ids, written=written, stream=st)
-            else:
+            elif args.append == "plain":
                 rlt.rlt_kv_append(pool, bank, kn[i], vn[i], loc, stream=st)
             if events is not None:
                 events[i][0].record(st)
-            if plan is not None:
-                rlt.rlt_paged_decode_attn_prefix(pool, bank, q[i], pt, sl, case.max_seq_len, plan, out=out[i],
-                                                 workspace=ws, split_tokens=args.split_tokens,
-                                                 max_ctas=args.prefix_ctas, stream=st)
-            else:
-                rlt.rlt_paged_decode_attn(pool, bank, q[i], pt, sl, case.max_seq_len, out=out[i], workspace=ws,
-                                          split_tokens=args.split_tokens, stream=st)
+            attend(i, bank, st)
             if events is not None:
                 events[i][1].record(st)
+
+    def attend(i, bank, st):
+        """One bank's attention call (with the append fused into it under --append fused)."""
+        fused = {"k_new": kn[i], "v_new": vn[i]} if args.append == "fused" else {}
+        if plan is not None:
+            rlt.rlt_paged_decode_attn_prefix(pool, bank, q[i], pt, sl, case.max_seq_len, plan, out=out[i],
+                                             workspace=ws, split_tokens=args.split_tokens,
+                                             max_ctas=args.prefix_ctas, stream=st, **fused)
+        else:
+            rlt.rlt_paged_decode_attn(pool, bank, q[i], pt, sl, case.max_seq_len, out=out[i], workspace=ws,
+                                      split_tokens=args.split_tokens, stream=st, **fused)
 
     def attention_only(st):
         """Every bank's attention call and nothing else (for the per-call roofline timing)."""
         for i, bank in enumerate(banks):
-            if plan is not None:
-                rlt.rlt_paged_decode_attn_prefix(pool, bank, q[i], pt, sl, case.max_seq_len, plan, out=out[i],
-                                                 workspace=ws, split_tokens=args.split_tokens,
-                                                 max_ctas=args.prefix_ctas, stream=st)
-            else:
-                rlt.rlt_paged_decode_attn(pool, bank, q[i], pt, sl, case.max_seq_len, out=out[i], workspace=ws,
-                                          split_tokens=args.split_tokens, stream=st)
+            attend(i, bank, st)
 
     def new_events(external):
         kw = {"external": True} if external else {}
@@ -465,6 +475,8 @@ def run_gpu(args, rank, world):
         per_lp = 4 if plan.max_rest_len > 0 else 3    # append, tensor-core segments, [split-K], combine
     else:
         per_lp = 3 if ws_bytes > 0 else 2
+    if args.append == "fused" and (plan is None or plan.max_rest_len > 0):
+        per_lp -= 1                                   # the append rides in the split-K kernel
     combine = ws_bytes > 0
     launches = args.steps * (len(banks) * per_lp + (1 if nz is not None else 0))
     return dict(case=case, banks=banks, cascade=plan is not None, graph=graph is not None, attn_timing=attn_timing,
@@ -592,8 +604,9 @@ def main():
                     help="submit each decode step as one captured CUDA graph (on) or as eager launches")
     ap.add_argument("--extend", type=int, default=0,
                     help="also time causal extend attention with this many new tokens per request (0: off)")
-    ap.add_argument("--append", default="plain", choices=["plain", "rope"],
-                    help="store_kv as given (plain) or with RoPE fused on the keys and written-prefix counters")
+    ap.add_argument("--append", default="fused", choices=["plain", "fused", "rope"],
+                    help="store_kv as its own launch at the given slots (plain), fused into the attention "
+                         "call (fused), or with RoPE on the keys and written-prefix counters (rope)")
     ap.add_argument("--prefix-ctas", type=int, default=0,
                     help="CTAs of the persistent tensor-core kernel (0 = one per SM)")
     ap.add_argument("--banks", type=int, default=0,
@@ -625,10 +638,11 @@ def main():
 
     attn_isolated_ms = statistics.mean(r["attn_ms"])
     attn_launch_ms = r["attn_call_ms"] if r["attn_call_ms"] is not None else attn_isolated_ms
-    a_bytes = attn_bytes(case)
+    fused = args.append == "fused"
+    a_bytes = attn_bytes(case) + (fused_append_bytes(case) if fused else 0)
     peak, peak_kind = hbm_peak()
     achieved = a_bytes / (attn_launch_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(case.name)
+    traffic = profiled_traffic(case.name, fused)
 
     cpu = None
     if rank == 0 and args.cpu_budget > 0:
@@ -648,7 +662,8 @@ def main():
         "kv_tokens_per_s": round(world * case.kv_tokens() * nlp / (ms_max * 1e-3), 1),
         "roofline": {"bound": "hbm",
                      "kernel": ("rlt_paged_decode_attn_prefix (tcgen05 shared-prefix + split-K + combine)"
-                                if r["cascade"] else "rlt_paged_decode_attn (split-K partial + combine)"),
+                                if r["cascade"] else "rlt_paged_decode_attn (split-K partial + combine)")
+                               + (", append fused" if fused else ""),
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": f"{peak_kind} (HBM copy)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": a_bytes, "launch_us": round(attn_launch_ms * 1e3, 2),

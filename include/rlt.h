@@ -183,6 +183,14 @@ RLT_API size_t rlt_paged_decode_workspace_size(int32_t batch, int32_t num_q_head
  * at page page_table[b*max_pages + j/page_size], offset j % page_size, of
  * bank `bank`.
  *   q          bf16 [batch][num_q_heads][head_dim], device
+ *   k_new, v_new  NULL (both), or bf16 [batch][num_kv_heads][head_dim], device:
+ *              the append fused into this call ([FFM] "When scheduler does the
+ *              work": store_kv before attention).  Request b's rows are stored at
+ *              its newest position seq_lens[b] - 1 (slot from the page table, as
+ *              rlt_kv_append would with that slot) and attended to in the same
+ *              call; the split-K CTA that reads that position's tile writes them.
+ *              The slot must belong to request b alone (a shared page is read-
+ *              only).  A request whose seq_len had to be clamped gets no append.
  *   page_table int32 [batch][max_pages], device; entries past a request's
  *              last page are never read
  *   seq_lens   int32 [batch], device, each in [0, max_seq_len]
@@ -203,7 +211,7 @@ RLT_API size_t rlt_paged_decode_workspace_size(int32_t batch, int32_t num_q_head
  * q, out, the pool and workspace must be 16-byte aligned.
  */
 RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, const void *q,
-                                 int32_t num_q_heads, const int32_t *page_table,
+                                 const void *k_new, const void *v_new, int32_t num_q_heads, const int32_t *page_table,
                                  int32_t max_pages, const int32_t *seq_lens, int32_t batch,
                                  int32_t max_seq_len, float scale, void *out, float *lse_out,
                                  void *workspace, size_t workspace_bytes,
@@ -283,14 +291,19 @@ RLT_API size_t rlt_paged_decode_prefix_workspace_size(int32_t batch, int32_t num
  * branches).  The tensor-core kernel is persistent: max_ctas CTAs (0 = the
  * library's choice: one per SM alone, or the SMs split between the two kernels
  * in proportion to their estimated tokens) share the num_kv_heads x work_units
- * work items in contiguous runs.  Other arguments as
+ * work items in contiguous runs.  k_new / v_new (optional) fuse the append as in
+ * rlt_paged_decode_attn: with a split-K rest, its kernel stores each newest row
+ * (a newest position inside a request's shared prefix, whose slot would be a
+ * shared page's, is skipped and sets RLT_DEVERR_BAD_SLOT); with private tails,
+ * one append kernel runs ahead of the tensor-core kernel.  Other arguments as
  * rlt_paged_decode_attn; the workspace (rlt_paged_decode_prefix_workspace_size
  * bytes) is required.  num_segments == 0 runs rlt_paged_decode_attn.
  * Supported: head_dim 128, num_q_heads/num_kv_heads in {1, 2, 4, 8}, page_size
  * a multiple of 16 dividing or divisible by 128.
  */
 RLT_API rlt_status rlt_paged_decode_attn_prefix(
-    const rlt_kv_pool *pool, int32_t bank, const void *q, int32_t num_q_heads,
+    const rlt_kv_pool *pool, int32_t bank, const void *q, const void *k_new, const void *v_new,
+    int32_t num_q_heads,
     const int32_t *page_table, int32_t max_pages, const int32_t *seq_lens, int32_t batch,
     int32_t max_seq_len, const int32_t *segments, const int32_t *members,
     const int32_t *member_limit, const int32_t *request_prefix, int32_t num_segments, int32_t work_units,
@@ -349,7 +362,8 @@ RLT_API rlt_status rlt_paged_extend_attn(
 
 /*
  * rlt_paged_decode_attn without a workspace argument: the same computation,
- * arguments and results as rlt_paged_decode_attn, but the split-K partials go
+ * arguments and results as rlt_paged_decode_attn with k_new = v_new = NULL
+ * (no fused append; those two arguments are absent), but the split-K partials go
  * to a fixed 64 MiB array inside the library, so the call allocates nothing.
  * The paper has no counterpart to this entry point; it exists for callers
  * that cannot allocate device memory at the point of the call, such as

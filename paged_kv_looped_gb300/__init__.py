@@ -77,7 +77,7 @@ def load():
         "rlt_bank_map": (i32, [P, i32, i32, P]),
         "rlt_kv_append": (ctypes.c_int, [pool_p, i32, P, P, P, i32, P]),
         "rlt_paged_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
-        "rlt_paged_decode_attn": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, P, i32, i32, f32, P, P, P,
+        "rlt_paged_decode_attn": (ctypes.c_int, [pool_p, i32, P, P, P, i32, P, i32, P, i32, i32, f32, P, P, P,
                                                  sz, i32, P]),
         "rlt_latent_noise_init": (ctypes.c_int, [P, P, P, i64, i32, f32, P]),
         "rlt_noise_hash24": (ctypes.c_int, [P, P, P, i64, i32, P]),
@@ -87,7 +87,7 @@ def load():
         "rlt_validate_batch": (ctypes.c_int, [P, i32, P, i32, P, i64, i32]),
         "rlt_plan_prefix": (ctypes.c_int, [P, i32, P, i32, i32, i32, i32, i32, P, i32, P, P, i32, P, P]),
         "rlt_paged_decode_prefix_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, i32]),
-        "rlt_paged_decode_attn_prefix": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, P, i32, i32, P, P, P, P, i32,
+        "rlt_paged_decode_attn_prefix": (ctypes.c_int, [pool_p, i32, P, P, P, i32, P, i32, P, i32, i32, P, P, P, P, i32,
                                                         i32, i32, i32, i32, f32, P, P, P, sz, i32, i32, P]),
         "rlt_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
         "rlt_kv_append_rope": (ctypes.c_int, [pool_p, i32, P, P, P, P, i32, i32, ctypes.c_double, P, P, i32, P]),
@@ -234,11 +234,25 @@ def rlt_paged_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, 
                                                       max_seq_len, split_tokens))
 
 
+def _new_rows(k_new, v_new, B, Hkv, D):
+    """Device pointers of the optional fused-append rows (bf16 [B][Hkv][D] each, or both None)."""
+    import torch
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is None:
+        return ctypes.c_void_p(0), ctypes.c_void_p(0)
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        if tuple(t.shape) != (B, Hkv, D):
+            raise ValueError(f"{name} must be [B][Hkv][D] = {(B, Hkv, D)}")
+    return _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new")
+
+
 def rlt_paged_decode_attn(pool: KVPool, bank: int, q, page_table, seq_lens, max_seq_len: int,
                           out=None, lse_out=None, workspace=None, scale: float = 0.0,
-                          split_tokens: int = 0, stream=None):
+                          split_tokens: int = 0, stream=None, k_new=None, v_new=None):
     """Paged decode attention of one bank. q bf16 [B][Hq][D]; page_table int32 [B][max_pages];
-    seq_lens int32 [B].  Returns out (bf16 [B][Hq][D])."""
+    seq_lens int32 [B].  With k_new / v_new (bf16 [B][Hkv][D]) each request's new token is
+    stored at position seq_lens[b] - 1 by the same call (fused append).  Returns out."""
     import torch
     B, Hq, D = q.shape
     if D != pool.head_dim:
@@ -253,8 +267,9 @@ def rlt_paged_decode_attn(pool: KVPool, bank: int, q, page_table, seq_lens, max_
     lse_ptr = _dev(lse_out, torch.float32, "lse_out") if lse_out is not None else ctypes.c_void_p(0)
     if page_table.dim() != 2 or page_table.shape[0] != B or seq_lens.shape != (B,):
         raise ValueError("page_table must be [B][max_pages] and seq_lens [B]")
+    kn, vn = _new_rows(k_new, v_new, B, pool.num_kv_heads, D)
     _check(load().rlt_paged_decode_attn(
-        ctypes.byref(pool.struct), bank, _dev(q, torch.bfloat16, "q"), Hq,
+        ctypes.byref(pool.struct), bank, _dev(q, torch.bfloat16, "q"), kn, vn, Hq,
         _dev(page_table, torch.int32, "page_table"), page_table.shape[1],
         _dev(seq_lens, torch.int32, "seq_lens"), B, int(max_seq_len), float(scale),
         _dev(out, torch.bfloat16, "out"), lse_ptr, ws_ptr, ws_bytes, int(split_tokens),
@@ -406,8 +421,9 @@ def rlt_paged_decode_prefix_workspace_size(batch, num_q_heads, num_kv_heads, hea
 
 def rlt_paged_decode_attn_prefix(pool: KVPool, bank: int, q, page_table, seq_lens, max_seq_len: int,
                                  plan: PrefixPlan, out=None, lse_out=None, workspace=None, scale: float = 0.0,
-                                 split_tokens: int = 0, max_ctas: int = 0, stream=None):
-    """Paged decode attention reading shared-prefix tiles once (plan from rlt_plan_prefix, .to(device))."""
+                                 split_tokens: int = 0, max_ctas: int = 0, stream=None, k_new=None, v_new=None):
+    """Paged decode attention reading shared-prefix tiles once (plan from rlt_plan_prefix, .to(device)).
+    k_new / v_new: the fused append, as in rlt_paged_decode_attn."""
     import torch
     B, Hq, D = q.shape
     if plan.num_segments and plan.query_group != Hq // pool.num_kv_heads:
@@ -423,8 +439,9 @@ def rlt_paged_decode_attn_prefix(pool: KVPool, bank: int, q, page_table, seq_len
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     lse_ptr = _dev(lse_out, torch.float32, "lse_out") if lse_out is not None else ctypes.c_void_p(0)
     seg, mem, lim, req = plan.dev
+    kn, vn = _new_rows(k_new, v_new, B, pool.num_kv_heads, D)
     _check(load().rlt_paged_decode_attn_prefix(
-        ctypes.byref(pool.struct), bank, _dev(q, torch.bfloat16, "q"), Hq,
+        ctypes.byref(pool.struct), bank, _dev(q, torch.bfloat16, "q"), kn, vn, Hq,
         _dev(page_table, torch.int32, "page_table"), page_table.shape[1],
         _dev(seq_lens, torch.int32, "seq_lens"), B, int(max_seq_len),
         _dev(seg, torch.int32, "segments"), _dev(mem, torch.int32, "members"),

@@ -219,7 +219,7 @@ RLT_API size_t rlt_paged_decode_workspace_size(int32_t batch, int32_t num_q_head
 }
 
 RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, const void *q,
-                                         int32_t num_q_heads, const int32_t *page_table,
+                                         const void *k_new, const void *v_new, int32_t num_q_heads, const int32_t *page_table,
                                          int32_t max_pages, const int32_t *seq_lens,
                                          int32_t batch, int32_t max_seq_len, float scale,
                                          void *out, float *lse_out, void *workspace,
@@ -246,7 +246,8 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
         return RLT_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || (workspace != nullptr && !aligned16(workspace)))
         return RLT_ERR_INVALID_ARG;
-    if (!std::isfinite(scale))
+    if (!std::isfinite(scale) || (k_new == nullptr) != (v_new == nullptr) || !aligned16(k_new) ||
+        !aligned16(v_new))
         return RLT_ERR_INVALID_ARG;
 
     unsigned int *err = nullptr;
@@ -263,6 +264,8 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
     p.k_bank = static_cast<const uint16_t *>(pool->k) + off;
     p.v_bank = static_cast<const uint16_t *>(pool->v) + off;
     p.q = static_cast<const uint16_t *>(q);
+    p.k_new = static_cast<const uint16_t *>(k_new);
+    p.v_new = static_cast<const uint16_t *>(v_new);
     p.page_table = page_table;
     p.seq_lens = seq_lens;
     p.out = static_cast<uint16_t *>(out);
@@ -301,7 +304,8 @@ RLT_API size_t rlt_paged_decode_prefix_workspace_size(int32_t batch, int32_t num
 }
 
 RLT_API rlt_status rlt_paged_decode_attn_prefix(
-    const rlt_kv_pool *pool, int32_t bank, const void *q, int32_t num_q_heads,
+    const rlt_kv_pool *pool, int32_t bank, const void *q, const void *k_new, const void *v_new,
+    int32_t num_q_heads,
     const int32_t *page_table, int32_t max_pages, const int32_t *seq_lens, int32_t batch,
     int32_t max_seq_len, const int32_t *segments, const int32_t *members,
     const int32_t *member_limit, const int32_t *request_prefix, int32_t num_segments, int32_t work_units,
@@ -312,7 +316,7 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     if (max_ctas < 0)
         return RLT_ERR_INVALID_ARG;
     if (num_segments == 0)      // nothing shared: the plain kernel computes the same thing
-        return rlt_paged_decode_attn(pool, bank, q, num_q_heads, page_table, max_pages, seq_lens,
+        return rlt_paged_decode_attn(pool, bank, q, k_new, v_new, num_q_heads, page_table, max_pages, seq_lens,
                                      batch, max_seq_len, scale, out, lse_out, workspace,
                                      workspace_bytes, split_tokens, stream);
     rlt_status st = check_pool(pool, bank);
@@ -334,6 +338,8 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
         workspace == nullptr)
         return RLT_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || !std::isfinite(scale))
+        return RLT_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr) || !aligned16(k_new) || !aligned16(v_new))
         return RLT_ERR_INVALID_ARG;
     const int64_t bank_rows = pool->num_pages * pool->num_kv_heads * (int64_t)pool->page_size;
     if (bank_rows >= (int64_t(1) << 31))
@@ -403,6 +409,19 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
+    if (k_new != nullptr && max_rest_len == 0) {
+        // every token on the tensor-core kernel: the new rows go to the pool first
+        e = rlt::launch_append_last(const_cast<uint16_t *>(p.k_bank), const_cast<uint16_t *>(p.v_bank),
+                                    static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),
+                                    page_table, max_pages, seq_lens, batch, pool->num_kv_heads,
+                                    pool->page_size, pool->head_dim, pool->num_pages, err, cs);
+        if (e != cudaSuccess)
+            return from_cuda(e);
+    } else if (k_new != nullptr) {
+        // the split-K kernel covers every request's newest token and stores it on the way
+        p.k_new = static_cast<const uint16_t *>(k_new);
+        p.v_new = static_cast<const uint16_t *>(v_new);
+    }
     if (max_rest_len > 0) {
         SideStream *side = nullptr;
         if ((st = side_stream(&side)) != RLT_OK)

@@ -382,6 +382,10 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
     const int L = sp.L, tok0 = sp.tok0, n_pre = sp.n_pre;
     const int n_tiles = (L - tok0 + kTileTokens - 1) / kTileTokens;
     const int n_splits = (n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    // A fused append needs the new token past the shared prefix: inside it, its slot
+    // would be a shared (read-only) page's.  Flagged, not written.
+    if (p.k_new != nullptr && L > 0 && L - 1 < tok0 && split == 0 && g == 0 && threadIdx.x == 0)
+        record_error(p.err, RLT_DEVERR_BAD_SLOT);
 
     if (n_splits == 0 && n_pre == 0) {          // empty request: out = 0, lse = -inf
         if (split == 0) {
@@ -426,6 +430,19 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
         my_off = tok % p.page_size;
     }
 
+    // Fused append: the new token (position L - 1) falls in tile t_new of [tok0, L); the
+    // warp whose i_new-th tile that is loads row r_new of it from k_new / v_new instead of
+    // the pool (the tile's other rows come from the pool as usual, in one or two pieces)
+    // and, once the tile has landed, stores that row to the pool slot.
+    int i_new = -1, r_new = 0;
+    if (p.k_new != nullptr && L > tok0 && L == p.seq_lens[b]) {      // not on a clamped length
+        const int t_new = (L - 1 - tok0) / kTileTokens;
+        if (t_new >= my_first && t_new < tile_end && (t_new - my_first) % kWarps == 0) {
+            i_new = (t_new - my_first) / kWarps;
+            r_new = (L - 1 - tok0) % kTileTokens;
+        }
+    }
+
     auto issue = [&](int i) {
         const int page = __shfl_sync(kFullMask, my_page, i);
         const int off = __shfl_sync(kFullMask, my_off, i);
@@ -434,8 +451,23 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
             unsigned char *dst = pipe + (i % kStages) * C::kStageBytes;
             const int64_t row = ((int64_t)page * p.num_kv_heads + g) * p.page_size + off;
             mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
-            bulk_load(dst, p.k_bank + row * D, C::kTileBytes, bar);
-            bulk_load(dst + C::kTileBytes, p.v_bank + row * D, C::kTileBytes, bar);
+            if (i != i_new) {
+                bulk_load(dst, p.k_bank + row * D, C::kTileBytes, bar);
+                bulk_load(dst + C::kTileBytes, p.v_bank + row * D, C::kTileBytes, bar);
+            } else {
+                constexpr uint32_t kRow = D * 2;
+                const int64_t nrow = ((int64_t)b * p.num_kv_heads + g) * D;
+                for (int kv = 0; kv < 2; ++kv) {
+                    const uint16_t *bank = kv == 0 ? p.k_bank : p.v_bank;
+                    unsigned char *d = dst + kv * C::kTileBytes;
+                    if (r_new > 0)
+                        bulk_load(d, bank + row * D, r_new * kRow, bar);
+                    bulk_load(d + r_new * kRow, (kv == 0 ? p.k_new : p.v_new) + nrow, kRow, bar);
+                    if (r_new < kTileTokens - 1)
+                        bulk_load(d + (r_new + 1) * kRow, bank + (row + r_new + 1) * D,
+                                  (kTileTokens - 1 - r_new) * kRow, bar);
+                }
+            }
         }
     };
 
@@ -483,6 +515,16 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
             const int valid = min(kTileTokens, L - tok0 - (my_first + i * kWarps) * kTileTokens);
             const unsigned char *ks = pipe + s * C::kStageBytes;
             const unsigned char *vs = ks + C::kTileBytes;
+            if (i == i_new) {                   // warp-uniform: the new row to its pool slot
+                const int off = __shfl_sync(kFullMask, my_off, i);
+                const int vec = lane & 15;
+                if (vec < D / 8) {
+                    const uint4 v = reinterpret_cast<const uint4 *>((lane < 16 ? ks : vs) + r_new * D * 2)[vec];
+                    const int64_t slot_row = ((int64_t)page * p.num_kv_heads + g) * p.page_size + off + r_new;
+                    uint16_t *dst = const_cast<uint16_t *>(lane < 16 ? p.k_bank : p.v_bank) + slot_row * D;
+                    reinterpret_cast<uint4 *>(dst)[vec] = v;
+                }
+            }
 
             // Partial dot products of this lane's dims for its half's 8 rows.
             float sc[G][8];

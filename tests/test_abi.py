@@ -106,7 +106,7 @@ def test_device_entry_points_reject_bad_arguments_before_launch(lib):
     bad = rlt.rlt_kv_pool(8, 16, 10, 1, 2, 16, 128)                                     # misaligned k
     assert lib.rlt_kv_append(ctypes.byref(bad), 0, null, null, null, 1, null) == 1
     attn = lambda p, hq, split=0, ws=0: lib.rlt_paged_decode_attn(                       # noqa: E731
-        ctypes.byref(p), 0, null, hq, null, 1, null, 1, 64, 0.0, null, null, null, ws, split, null)
+        ctypes.byref(p), 0, null, null, null, hq, null, 1, null, 1, 64, 0.0, null, null, null, ws, split, null)
     assert attn(pool, 3) == 1                                # Hq not a multiple of Hkv
     assert attn(pool, 6) == 3                                # group 3: no kernel
     assert attn(pool, 2, split=24) == 1                      # split not a multiple of 16

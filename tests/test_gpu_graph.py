@@ -31,7 +31,9 @@ def capture(fn, device):
     return graph
 
 
-def test_plain_step_replays_and_follows_new_inputs(cuda_device):
+@pytest.mark.parametrize("fused", [False, True])
+def test_plain_step_replays_and_follows_new_inputs(cuda_device, fused):
+    # fused: the append rides in the attention call (k_new / v_new), at position seq_lens[b] - 1
     case = W.config("tiny")
     banks = 3
     h = W.host_tensors(case)
@@ -57,9 +59,11 @@ def test_plain_step_replays_and_follows_new_inputs(cuda_device):
 
     def step(stream):
         for b in range(banks):
-            rlt.rlt_kv_append(pool, b, k_new[b], v_new[b], loc, stream=stream)
+            if not fused:
+                rlt.rlt_kv_append(pool, b, k_new[b], v_new[b], loc, stream=stream)
+            extra = {"k_new": k_new[b], "v_new": v_new[b]} if fused else {}
             rlt.rlt_paged_decode_attn(pool, b, q[b], pt, sl, max_len, out=out[b], lse_out=lse[b],
-                                      workspace=ws, split_tokens=32, stream=stream)
+                                      workspace=ws, split_tokens=32, stream=stream, **extra)
 
     # eager reference of the same step (appends overwrite the same slots: idempotent)
     step(torch.cuda.current_stream(cuda_device))
