@@ -108,7 +108,7 @@ def test_plain_step_replays_and_follows_new_inputs(cuda_device, fused):
 
 
 def test_cascade_step_with_noise_replays_bit_exact(cuda_device):
-    # shared prefix -> tensor-core segments + split-K rest (programmatic launch edges in the graph),
+    # shared prefix -> tensor-core segments + split-K rest (forked onto a side stream and joined),
     # plus the new tokens' latent noise
     case = W.custom(B=6, Hq=16, Hkv=2, D=128, ps=16, seq_lens=[3000, 2900, 3100, 1500, 700, 2333],
                     shared_frac=0.8, seed=21)
