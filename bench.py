@@ -475,8 +475,8 @@ def run_gpu(args, rank, world):
         per_lp = 4 if plan.max_rest_len > 0 else 3    # append, tensor-core segments, [split-K], combine
     else:
         per_lp = 3 if ws_bytes > 0 else 2
-    if args.append == "fused" and (plan is None or plan.max_rest_len > 0):
-        per_lp -= 1                                   # the append rides in the split-K kernel
+    if args.append == "fused":
+        per_lp -= 1                                   # the append rides in an attention kernel
     combine = ws_bytes > 0
     launches = args.steps * (len(banks) * per_lp + (1 if nz is not None else 0))
     return dict(case=case, banks=banks, cascade=plan is not None, graph=graph is not None, attn_timing=attn_timing,

@@ -292,10 +292,11 @@ RLT_API size_t rlt_paged_decode_prefix_workspace_size(int32_t batch, int32_t num
  * library's choice: one per SM alone, or the SMs split between the two kernels
  * in proportion to their estimated tokens) share the num_kv_heads x work_units
  * work items in contiguous runs.  k_new / v_new (optional) fuse the append as in
- * rlt_paged_decode_attn: with a split-K rest, its kernel stores each newest row
- * (a newest position inside a request's shared prefix, whose slot would be a
- * shared page's, is skipped and sets RLT_DEVERR_BAD_SLOT); with private tails,
- * one append kernel runs ahead of the tensor-core kernel.  Other arguments as
+ * rlt_paged_decode_attn: the kernel whose copy covers a request's newest position
+ * stores its rows (the split-K kernel for an unshared rest, the tensor-core
+ * kernel for a private tail); a newest position inside tiles the request shares,
+ * whose slot would be a shared page's, is skipped and sets RLT_DEVERR_BAD_SLOT.
+ * Other arguments as
  * rlt_paged_decode_attn; the workspace (rlt_paged_decode_prefix_workspace_size
  * bytes) is required.  num_segments == 0 runs rlt_paged_decode_attn.
  * Supported: head_dim 128, num_q_heads/num_kv_heads in {1, 2, 4, 8}, page_size

@@ -409,18 +409,14 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
-    if (k_new != nullptr && max_rest_len == 0) {
-        // every token on the tensor-core kernel: the new rows go to the pool first
-        e = rlt::launch_append_last(const_cast<uint16_t *>(p.k_bank), const_cast<uint16_t *>(p.v_bank),
-                                    static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),
-                                    page_table, max_pages, seq_lens, batch, pool->num_kv_heads,
-                                    pool->page_size, pool->head_dim, pool->num_pages, err, cs);
-        if (e != cudaSuccess)
-            return from_cuda(e);
-    } else if (k_new != nullptr) {
-        // the split-K kernel covers every request's newest token and stores it on the way
-        p.k_new = static_cast<const uint16_t *>(k_new);
-        p.v_new = static_cast<const uint16_t *>(v_new);
+    // Fused append: the kernel whose copy covers a request's newest token stores the new
+    // rows on the way -- the split-K kernel for an unshared rest, the tensor-core kernel
+    // for a private tail -- and flags a newest token inside shared tiles.
+    rlt::DecodeParams p_rest = p;
+    if (k_new != nullptr) {
+        rlt::DecodeParams &q = max_rest_len > 0 ? p_rest : p;
+        q.k_new = static_cast<const uint16_t *>(k_new);
+        q.v_new = static_cast<const uint16_t *>(v_new);
     }
     if (max_rest_len > 0) {
         SideStream *side = nullptr;
@@ -432,7 +428,7 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
         if (e == cudaSuccess)
             e = rlt::launch_prefix(p, pp, p.k_bank, p.v_bank, bank_rows, cs);
         if (e == cudaSuccess)
-            e = rlt::launch_decode(p, pool->head_dim, group, side->stream);
+            e = rlt::launch_decode(p_rest, pool->head_dim, group, side->stream);
         if (e == cudaSuccess)
             e = cudaEventRecord(side->join, side->stream);
         if (e == cudaSuccess)

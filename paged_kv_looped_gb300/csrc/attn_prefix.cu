@@ -107,6 +107,7 @@ static_assert(kVOff % 1024 == 0, "swizzled operands");
 struct RunDesc {
     int64_t tok_begin, tok_end;
     int32_t g, nsub, page_row, n_mem, slot, nchunks, F;
+    int32_t tail;                            // a one-member segment: a request's private tail
 };
 static_assert(sizeof(RunDesc) <= 64, "descriptor slot");
 
@@ -143,6 +144,7 @@ __device__ __forceinline__ Run decode_run(const PrefixParams &pp, int G, int ite
     r.d.F = prefix_replication(min(per_block, sd[kSegMemberCount]) * G);
     r.member_begin = sd[kSegMemberBegin] + m0;
     r.d.page_row = sd[kSegPageRow];
+    r.d.tail = sd[kSegMemberCount] == 1;
     r.d.slot = sd[kSegSlotBase] + chunk0 * r.d.F;
     const int t_first = sd[kSegFirstTile] + chunk0 * pp.chunk_tiles;
     const int t_last = sd[kSegFirstTile] + min(num_tiles, (chunk0 + r.d.nchunks) * pp.chunk_tiles);
@@ -250,6 +252,9 @@ __device__ __forceinline__ bool pair_sync(uint64_t *bar, int &k, const volatile 
     return warp_wait(bar, (uint32_t)(k++) & 1u, abort);
 }
 
+// kAppend: the call fuses the append and runs every request's private tail here (no
+// split-K rest), so the producers store each tail's new rows before copying them.
+template <bool kAppend>
 __global__ void __launch_bounds__(kPThreads, 1)
     decode_prefix_kernel(const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const DecodeParams p,
@@ -327,6 +332,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&bars[kBarDescFull + d % kDescs]);
+            // Fused append, checked once the descriptor is out: a member whose newest token
+            // lies in tiles it shares would need a slot of a shared (read-only) page; flagged,
+            // not written.  (The slot stays readable until every consumer has released it.)
+            for (int i = lane; kAppend && has && !r.d.tail && i < r.d.n_mem; i += 32) {
+                const int b = dmem[(d % kDescs) * 128 + i];
+                const int len = p.seq_lens[b];
+                if (len > 0 && dlim[(d % kDescs) * 128 + i] >= len)
+                    record_error(p.err, RLT_DEVERR_BAD_SLOT);
+            }
             if (!has)
                 break;
         }
@@ -364,12 +378,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             return (int)((page * p.num_kv_heads + d.g) * p.page_size + tok % p.page_size);
         };
+        // Fused append (private tails): position of the run's request's new token when the
+        // run ends at that request's length, else -1.
+        auto new_token = [&](const RunDesc &d) -> int64_t {
+            if (!kAppend || !d.tail || d.nsub <= 0 || d.page_row < 0 || d.page_row >= p.batch)
+                return -1;
+            return p.seq_lens[d.page_row] == d.tok_end ? d.tok_end - 1 : -1;
+        };
         int n = 0, r = 0, j = 0;                 // sub-tiles issued; current run and sub-tile
         RunDesc cur;
         ok = take_desc(bars, base, r, cur, -1, G, unused, unused, abort_flag, lane);
         int row_next = ok && cur.nsub > 0 ? lane_row(cur, 0) : -1;
+        int64_t nt_next = ok ? new_token(cur) : -1;
         while (ok && cur.nsub > 0) {
             const int row = row_next;
+            const int64_t nt = nt_next;
+            const int nt_b = cur.page_row, nt_g = cur.g;
             const int64_t sub_begin = cur.tok_begin + (int64_t)j * kSub, tok_end = cur.tok_end;
             if (j + 1 < cur.nsub) {
                 row_next = lane_row(cur, ++j);
@@ -379,6 +403,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     break;
                 if (cur.nsub > 0)
                     row_next = lane_row(cur, 0);
+                nt_next = new_token(cur);
             }
             const int st = n % stages;
             if (n >= stages && !(ok = warp_wait(&freex[st], ((n / stages) - 1) & 1u, abort_flag)))
@@ -387,6 +412,26 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (lane == 0)
                 mbar_arrive_expect_tx(&fullx[st], (uint32_t)(nbox * BR * 128 * 2));
             __syncwarp();
+            if (kAppend && nt >= sub_begin && nt < sub_begin + kSub && lane < 2 * nbox &&
+                (lane >> 1) == (nt - sub_begin) / BR) {
+                // this lane's box holds the new token: its 64 dims go to the pool slot first,
+                // then the copy (same thread, ordered by the proxy fence) reads them back
+                const int64_t dr = (nt - sub_begin) % BR;
+                const int64_t pidx = nt / p.page_size;
+                const int64_t pg = pidx < p.max_pages ? p.page_table[(int64_t)nt_b * p.max_pages + pidx] : -1;
+                const bool page_valid = pg >= 0 && pg < p.num_pages;   // a bad page is flagged, not written
+                const uint4 *src = reinterpret_cast<const uint4 *>((is_v ? p.v_new : p.k_new) +
+                                                                   ((int64_t)nt_b * p.num_kv_heads + nt_g) * 128 +
+                                                                   (lane & 1) * 64);
+                uint4 *dst = reinterpret_cast<uint4 *>(const_cast<uint16_t *>(is_v ? p.v_bank : p.k_bank) +
+                                                       ((int64_t)row + dr) * 128 + (lane & 1) * 64);
+                if (page_valid) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        dst[k] = src[k];
+                }
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
             if (lane < 2 * nbox)
                 tc::tma_load_2d(ring + st * kKVBytes + (lane & 1) * kHalfKV + (lane >> 1) * BR * 128, map,
                                 (lane & 1) * 64, row, &fullx[st]);
@@ -805,21 +850,23 @@ cudaError_t launch_prefix(const DecodeParams &p, const PrefixParams &pp, const v
     CUtensorMap kmap, vmap;
     if (!make_map(&kmap, k_bank, bank_rows, box_rows) || !make_map(&vmap, v_bank, bank_rows, box_rows))
         return cudaErrorInvalidValue;
-    static std::atomic<uint64_t> configured{0};
+    static std::atomic<uint64_t> configured[2]{{0}, {0}};
+    const bool append = p.k_new != nullptr;
+    auto kernel = append ? decode_prefix_kernel<true> : decode_prefix_kernel<false>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
-    if (bit == 0 || (configured.load() & bit) == 0) {
-        e = cudaFuncSetAttribute(decode_prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemP);
+    if (bit == 0 || (configured[append].load() & bit) == 0) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemP);
         if (e != cudaSuccess)
             return e;
-        configured.fetch_or(bit);
+        configured[append].fetch_or(bit);
     }
     if (pp.ctas < 1)
         return cudaErrorInvalidValue;
-    decode_prefix_kernel<<<pp.ctas, kPThreads, kSmemP, stream>>>(kmap, vmap, p, pp);
+    kernel<<<pp.ctas, kPThreads, kSmemP, stream>>>(kmap, vmap, p, pp);
     return cudaGetLastError();
 }
 

@@ -44,43 +44,6 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// The same store for request b's token at position seq_lens[b] - 1, its slot read from
-// the page table.  Requests with seq_lens[b] == 0 have none.
-__global__ void __launch_bounds__(256)
-    append_last_kernel(uint4 *__restrict__ k_bank, uint4 *__restrict__ v_bank,
-                       const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
-                       const int32_t *__restrict__ page_table, int32_t max_pages,
-                       const int32_t *__restrict__ seq_lens, int32_t batch, int32_t num_kv_heads,
-                       int32_t page_size, int32_t vec_per_row, int64_t num_pages, unsigned int *err)
-{
-    const int64_t per_token = (int64_t)num_kv_heads * vec_per_row;
-    const int64_t total = (int64_t)batch * per_token;
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t b = idx / per_token;
-        const int64_t rem = idx - b * per_token;
-        const int64_t L = seq_lens[b];
-        if (L <= 0)
-            continue;
-        if (L > (int64_t)max_pages * page_size) {
-            if (rem == 0)
-                record_error(err, RLT_DEVERR_BAD_LEN);
-            continue;
-        }
-        const int64_t page = page_table[b * max_pages + (L - 1) / page_size];
-        if (page < 0 || page >= num_pages) {
-            if (rem == 0)
-                record_error(err, RLT_DEVERR_BAD_PAGE);
-            continue;
-        }
-        const int64_t g = rem / vec_per_row;
-        const int64_t v = rem - g * vec_per_row;
-        const int64_t dst = ((page * num_kv_heads + g) * page_size + (L - 1) % page_size) * vec_per_row + v;
-        k_bank[dst] = k_new[idx];
-        v_bank[dst] = v_new[idx];
-    }
-}
-
 __global__ void __launch_bounds__(256)
     gather_kernel(const uint4 *__restrict__ k_bank, const uint4 *__restrict__ v_bank,
                   const int32_t *__restrict__ page_table, int32_t max_pages,
@@ -136,21 +99,6 @@ cudaError_t launch_append(uint16_t *k_bank, uint16_t *v_bank, const uint16_t *k_
         reinterpret_cast<uint4 *>(k_bank), reinterpret_cast<uint4 *>(v_bank),
         reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), out_loc,
         n_tokens, num_kv_heads, page_size, vpr, num_pages * page_size, err);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_append_last(uint16_t *k_bank, uint16_t *v_bank, const uint16_t *k_new,
-                               const uint16_t *v_new, const int32_t *page_table, int32_t max_pages,
-                               const int32_t *seq_lens, int32_t batch, int32_t num_kv_heads,
-                               int32_t page_size, int32_t head_dim, int64_t num_pages,
-                               unsigned int *err, cudaStream_t stream)
-{
-    const int32_t vpr = head_dim / 8;
-    const int64_t total = (int64_t)batch * num_kv_heads * vpr;
-    append_last_kernel<<<grid_for(total), 256, 0, stream>>>(
-        reinterpret_cast<uint4 *>(k_bank), reinterpret_cast<uint4 *>(v_bank),
-        reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), page_table,
-        max_pages, seq_lens, batch, num_kv_heads, page_size, vpr, num_pages, err);
     return cudaGetLastError();
 }
 

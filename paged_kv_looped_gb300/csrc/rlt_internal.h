@@ -97,13 +97,6 @@ bool decode_supported(int head_dim, int group);
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, cudaStream_t stream);
 cudaError_t launch_combine(const DecodeParams &p, int head_dim, cudaStream_t stream);
 
-// Store each request's K/V row at its newest position (seq_lens[b] - 1) through the
-// page table: the slot-free form of launch_append a fused decode call falls back to.
-cudaError_t launch_append_last(uint16_t *k_bank, uint16_t *v_bank, const uint16_t *k_new,
-                               const uint16_t *v_new, const int32_t *page_table, int32_t max_pages,
-                               const int32_t *seq_lens, int32_t batch, int32_t num_kv_heads,
-                               int32_t page_size, int32_t head_dim, int64_t num_pages,
-                               unsigned int *err, cudaStream_t stream);
 cudaError_t launch_append(uint16_t *k_bank, uint16_t *v_bank, const uint16_t *k_new,
                           const uint16_t *v_new, const int64_t *out_loc, int32_t n_tokens,
                           int32_t num_kv_heads, int32_t page_size, int32_t head_dim,

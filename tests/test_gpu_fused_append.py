@@ -4,7 +4,9 @@
 layer stores the new token's K/V in its slot (store_kv) and then attends over
 every cached token, the new one included.  With k_new / v_new the attention
 call does both: the split-K CTA reading the tile of position seq_lens[b] - 1
-takes that row from k_new / v_new and writes it to the pool.  Checked against
+takes that row from k_new / v_new and writes it to the pool (for a private
+tail on tensor cores, the producer lane copying that row writes it to the pool
+just before its copy).  Checked against
 the oracle's two steps (kv_append at the slot the page table gives position
 L - 1, then decode attention over the updated pool): the pool bit for bit,
 the output within the attention bar, lse within 1e-3.
@@ -74,7 +76,7 @@ def test_plain_fused_append(cuda_device, G, D, ps, split_tokens):
 @pytest.mark.parametrize("G", [1, 4, 8])
 def test_prefix_fused_append(cuda_device, tails, G):
     # a shared prompt chain (tensor-core segments) and private rests; with private tails the
-    # append runs as its own kernel ahead of the tensor-core kernel
+    # tensor-core kernel stores the new rows (its producer lanes, before their copies)
     Hkv = 2
     lens = [3000, 2900, 3100, 1500, 700, 2333, 2048, 257]
     case = W.custom(B=len(lens), Hq=G * Hkv, Hkv=Hkv, D=128, ps=16, seq_lens=lens, shared_frac=0.8, seed=30 + G)
@@ -120,9 +122,12 @@ def test_fused_equals_append_then_attention_bit_exact(cuda_device):
     assert np.array_equal(outs[0][1], outs[1][1]) and np.array_equal(outs[0][2], outs[1][2])
 
 
-def test_newest_token_inside_a_shared_prefix_is_flagged_not_written(cuda_device):
+@pytest.mark.parametrize("tails", [False, True])
+def test_newest_token_inside_a_shared_prefix_is_flagged_not_written(cuda_device, tails):
     # requests 0 and 1 map the same two pages for 128 tokens: request 0's newest token
-    # (position 127) lies in a tile the plan shares, so its slot is a shared page's
+    # (position 127) lies in a tile the plan shares, so its slot is a shared page's; the
+    # others' rows are written by the split-K kernel (or, with private tails, by the
+    # tensor-core kernel)
     ps = 64
     case = W.custom(B=3, Hq=2, Hkv=2, D=128, ps=ps, seq_lens=[128, 600, 300], seed=17)
     pt = case.page_table.copy()
@@ -131,8 +136,8 @@ def test_newest_token_inside_a_shared_prefix_is_flagged_not_written(cuda_device)
     kn, vn = new_rows(case, 18)
     k, v = bf16_dev(h.k_pool, cuda_device)[None].contiguous(), bf16_dev(h.v_pool, cuda_device)[None].contiguous()
     pool = rlt.KVPool(k, v)
-    plan = rlt.rlt_plan_prefix(pt, case.seq_lens, ps, 1, False, 1).to(cuda_device)
-    assert plan.request_prefix[0, 0] == 128 and plan.max_rest_len > 0
+    plan = rlt.rlt_plan_prefix(pt, case.seq_lens, ps, 1, tails, 1).to(cuda_device)
+    assert plan.num_segments > 0 and (plan.max_rest_len == 0) == tails
     rlt.rlt_get_device_error()
     rlt.rlt_paged_decode_attn_prefix(pool, 0, bf16_dev(h.q, cuda_device), i32_dev(pt, cuda_device),
                                      i32_dev(case.seq_lens, cuda_device), case.max_seq_len, plan,
