@@ -51,7 +51,8 @@ def check(got, ref, lse, ref_lse):
     assert np.abs(lse[fin] - ref_lse[fin]).max(initial=0.0) <= 1e-3
 
 
-@pytest.mark.parametrize("G,D,ps", [(1, 128, 16), (2, 64, 16), (4, 128, 32), (8, 128, 64), (1, 64, 128)])
+@pytest.mark.parametrize("G,D,ps", [(1, 128, 16), (2, 64, 16), (4, 128, 32), (8, 128, 64), (1, 64, 128),
+                                    (2, 128, 256)])
 @pytest.mark.parametrize("split_tokens", [0, 16, 64, 2048])
 def test_plain_fused_append(cuda_device, G, D, ps, split_tokens):
     Hkv = 2
@@ -73,13 +74,13 @@ def test_plain_fused_append(cuda_device, G, D, ps, split_tokens):
 
 
 @pytest.mark.parametrize("tails", [False, True])
-@pytest.mark.parametrize("G", [1, 4, 8])
-def test_prefix_fused_append(cuda_device, tails, G):
+@pytest.mark.parametrize("G,ps", [(1, 16), (4, 16), (8, 16), (2, 64), (1, 256)])
+def test_prefix_fused_append(cuda_device, tails, G, ps):
     # a shared prompt chain (tensor-core segments) and private rests; with private tails the
     # tensor-core kernel stores the new rows (its producer lanes, before their copies)
     Hkv = 2
     lens = [3000, 2900, 3100, 1500, 700, 2333, 2048, 257]
-    case = W.custom(B=len(lens), Hq=G * Hkv, Hkv=Hkv, D=128, ps=16, seq_lens=lens, shared_frac=0.8, seed=30 + G)
+    case = W.custom(B=len(lens), Hq=G * Hkv, Hkv=Hkv, D=128, ps=ps, seq_lens=lens, shared_frac=0.8, seed=30 + G + ps)
     h = W.host_tensors(case)
     kn, vn = new_rows(case, 40 + G)
     k, v = bf16_dev(h.k_pool, cuda_device)[None].contiguous(), bf16_dev(h.v_pool, cuda_device)[None].contiguous()
