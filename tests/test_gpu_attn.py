@@ -222,3 +222,20 @@ def test_full_size_workloads_sampled(cuda_device, name, rows):
         L = W.config(name).seq_lens
         rows = sorted({int(np.argmax(L)), int(np.argmin(L)), 1, 128})
     full_size(name, cuda_device, np.array(rows))
+
+
+def test_many_rows_warp_merge(cuda_device):
+    # >= 2048 (request, query head) rows with a few splits each: the combine takes a warp per
+    # row; ragged lengths with empty, one-split and several-split requests
+    rng = np.random.default_rng(71)
+    lens = rng.integers(1, 700, size=136)
+    lens[[0, 5, 77]] = 0
+    lens[[1, 9]] = [16, 33]
+    case = W.custom(B=len(lens), Hq=16, Hkv=4, D=128, ps=16, seq_lens=lens.tolist(), seed=72)
+    h = W.host_tensors(case)
+    pool, q, pt, sl = dev_case(case, h, cuda_device)
+    got, lse = attend(pool, q, pt, sl, case.max_seq_len, split_tokens=64)
+    ref, ref_lse = oracle.decode_attn(h.q, h.k_pool, h.v_pool, case.page_table, case.seq_lens)
+    assert np.all(got[lens == 0] == 0) and np.all(np.isneginf(lse[lens == 0]))
+    check(got, ref, lse, ref_lse)
+    assert rlt.rlt_get_device_error() == 0
