@@ -723,12 +723,10 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
     merge_row<D>(p, bh, n_pre, n, sm);
 }
 
-constexpr int64_t kWarpCombineRows = 2048;
-
 // The same merge when every row's partial slots fit one warp (prefix slots + splits <= 32):
 // a warp per row, four rows per CTA, no shared memory.  Lane s holds slot s's log2-sum-exp;
-// the live slots' partials are then read in slot order, eight loads in flight per lane.
-template <int D>
+// the live slots' partials are then read in slot order, kLoads loads in flight per lane.
+template <int D, int kLoads>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_warp_kernel(const DecodeParams p)
 {
     constexpr int DPL = D / 32;
@@ -772,15 +770,15 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_warp_kernel(co
     for (int d = 0; d < DPL; ++d)
         acc[d] = 0.f;
     while (live != 0u) {
-        int sl[8];
+        int sl[kLoads];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kLoads; ++i) {
             sl[i] = live != 0u ? __ffs(live) - 1 : -1;
             live &= live - 1u;
         }
-        float v[8][DPL];
+        float v[kLoads][DPL];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kLoads; ++i) {
             const int s = sl[i] >= 0 ? sl[i] : 0;
             const int slot = s < n_pre ? s : p.prefix_slots + (s - n_pre);
             const float *op = p.o_part + (row + slot) * D + lane * DPL;
@@ -797,7 +795,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_warp_kernel(co
             }
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kLoads; ++i) {
             const float wi = __shfl_sync(kFullMask, w, sl[i] >= 0 ? sl[i] : 0);
             if (sl[i] >= 0) {
 #pragma unroll
@@ -823,14 +821,18 @@ template <int D>
 cudaError_t launch_combine_typed(const DecodeParams &p, cudaStream_t stream)
 {
     const int64_t pairs = (int64_t)p.batch * p.num_q_heads;
-    // a warp per row pays off once the rows alone fill the GPU with warps; with fewer rows
-    // the 4-warp merge spreads each row's partial reads wider (measured: gqa's 8192 rows
-    // 521 -> 514 us per call, ouro's 1024 and huginn's 512 rows slower)
-    if ((int64_t)p.prefix_slots + p.max_splits <= 32 && pairs >= kWarpCombineRows)
-        decode_combine_warp_kernel<D><<<(unsigned)((pairs + kCombineWarps - 1) / kCombineWarps), kCombineThreads, 0,
-                                        stream>>>(p);
-    else
+    const unsigned grid = (unsigned)((pairs + kCombineWarps - 1) / kCombineWarps);
+    // A warp per row when the slots fit; with few rows each warp keeps more of its row's
+    // partial reads in flight (measured: huginn's 512 rows 33.8 -> 32.3 us per call with 16,
+    // ouro's 1024 rows 181.2 -> 180.4; gqa's 8192 rows 514 with 8, 515 with 16).
+    if ((int64_t)p.prefix_slots + p.max_splits <= 32) {
+        if (pairs >= 4096)
+            decode_combine_warp_kernel<D, 8><<<grid, kCombineThreads, 0, stream>>>(p);
+        else
+            decode_combine_warp_kernel<D, 16><<<grid, kCombineThreads, 0, stream>>>(p);
+    } else {
         decode_combine_kernel<D><<<(unsigned)pairs, kCombineThreads, 0, stream>>>(p);
+    }
     return cudaGetLastError();
 }
 
