@@ -111,7 +111,8 @@ def test_shared_and_private_requests_mixed_with_empty(cuda_device):
     check(got[:6], ref[:6], lse[:6], ref_lse[:6])
 
 
-def test_longctx_full_size_sampled(cuda_device):
+@pytest.mark.parametrize("chunk_tiles,tails", [(8, False), (6, True)])   # (6, private tails): the bench's launch
+def test_longctx_full_size_sampled(cuda_device, chunk_tiles, tails):
     case = W.config("longctx")
     kd, vd = W.device_pool(case, 1, cuda_device)
     pool = rlt.KVPool(kd, vd)
@@ -120,8 +121,8 @@ def test_longctx_full_size_sampled(cuda_device):
     q = bf16_dev(q_bits, cuda_device)
     pt = i32_dev(case.page_table, cuda_device)
     sl = i32_dev(case.seq_lens, cuda_device)
-    plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, 8,
-                               query_group=case.group).to(cuda_device)
+    plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, chunk_tiles, tails,
+                               case.group).to(cuda_device)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=cuda_device)
     got = rlt.rlt_paged_decode_attn_prefix(pool, 0, q, pt, sl, case.max_seq_len, plan, lse_out=lse)
     got = got.float().cpu().numpy()
