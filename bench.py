@@ -569,6 +569,28 @@ def oracle_sample(case: W.PagedCase, budget_s: float, seed: int = 0):
     return s.bytes * passes / spent / 1e9, s.desc + f"; {passes} passes, {spent:.1f} s", spent
 
 
+def _oracle_worker(args):
+    """One process of the parallel oracle timing: its own sample, timed for budget_s."""
+    name, seed, budget_s = args
+    s = OracleSample(W.config(name), 8, seed)
+    spent, passes = 0.0, 0
+    while spent < budget_s or passes == 0:
+        spent += s.run()
+        passes += 1
+    return s.bytes * passes, spent
+
+
+def oracle_parallel(case: W.PagedCase, procs: int, budget_s: float):
+    """The same single-threaded oracle run as `procs` independent processes at once (spawned:
+    the parent holds a CUDA context), each on its own sample of the workload for about
+    budget_s; returns the summed rate (GB/s) and the process count."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(procs) as pool:
+        res = pool.map(_oracle_worker, [(case.name, 1000 + i, budget_s) for i in range(procs)])
+    return sum(b / t for b, t in res) / 1e9, procs
+
+
 def run_reference(args, rank, world):
     """The oracle as it stands on the host cores, on the bench's workload, metric and unit."""
     if rank != 0:
@@ -658,6 +680,8 @@ def main():
     ap.add_argument("--batch", type=int, default=0,
                     help="run only the first N requests of the workload (small case for profilers); 0 = all")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU time for cpu_baseline")
+    ap.add_argument("--cpu-procs", type=int, default=os.cpu_count() or 1,
+                    help="also time the oracle as this many processes at once (cpu_baseline.all_cores; <= 1: skip)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -692,6 +716,12 @@ def main():
     if rank == 0 and args.cpu_budget > 0:
         v, desc, _ = oracle_sample(case, args.cpu_budget)
         cpu = {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+        if args.cpu_procs > 1:
+            pv, procs = oracle_parallel(case, args.cpu_procs, args.cpu_budget / 2)
+            cpu["all_cores"] = {"value": round(pv, 4), "unit": UNIT, "cores": procs,
+                                "sample": f"{procs} processes of the same single-threaded oracle at once, "
+                                          f"each on its own 8 random requests for about "
+                                          f"{args.cpu_budget / 2:.1f} s; summed rate"}
 
     if rank != 0:
         return
