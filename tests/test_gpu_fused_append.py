@@ -166,9 +166,13 @@ def test_clamped_length_gets_no_append(cuda_device):
     assert np.array_equal(bits_host(k[0]), kp) and np.array_equal(bits_host(v[0]), vp)
 
 
-@pytest.mark.parametrize("name,rows", [("ouro", [0, 17, 33, 63]), ("huginn", list(range(16)))])
+@pytest.mark.parametrize("name,rows", [("ouro", [0, 17, 33, 63]), ("huginn", list(range(16))), ("gqa", None),
+                                       ("longctx", [0, 3, 7]), ("tiny", [0, 1, 2, 3])])
 def test_full_size_fused_sampled(cuda_device, name, rows):
-    # the launch plan the bench times with --append fused
+    # every workload at full size in the launch configuration bench.py times by default: the
+    # append fused into the call, the shared-prefix plan with the bench's private-tails rule and
+    # work-item size, split-K sized by the library
+    import bench
     case = W.config(name)
     kd, vd = W.device_pool(case, 1, cuda_device)
     pool = rlt.KVPool(kd, vd)
@@ -179,9 +183,13 @@ def test_full_size_fused_sampled(cuda_device, name, rows):
     pt, sl = i32_dev(case.page_table, cuda_device), i32_dev(case.seq_lens, cuda_device)
     q = bf16_dev(q_bits, cuda_device)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=cuda_device)
-    plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, 4, False, case.group)
+    tails = case.group >= 8
+    shared = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, 1, False, case.group)
     kw = dict(lse_out=lse, k_new=bf16_dev(kn, cuda_device), v_new=bf16_dev(vn, cuda_device))
-    if plan.num_segments:
+    if shared.num_segments:
+        sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+        chunk = bench.auto_chunk_tiles(rlt, case, tails, sms)
+        plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, chunk, tails, case.group)
         out = rlt.rlt_paged_decode_attn_prefix(pool, 0, q, pt, sl, case.max_seq_len, plan.to(cuda_device), **kw)
     else:
         out = rlt.rlt_paged_decode_attn(pool, 0, q, pt, sl, case.max_seq_len, **kw)
@@ -190,6 +198,8 @@ def test_full_size_fused_sampled(cuda_device, name, rows):
     del kd, vd, pool
     oracle.kv_append(kh0, vh0, kn, vn, case.new_slots)
     assert np.array_equal(kh, kh0) and np.array_equal(vh, vh0)
+    if rows is None:        # gqa: the longest and shortest requests plus two others
+        rows = sorted({int(np.argmax(case.seq_lens)), int(np.argmin(case.seq_lens)), 1, 128})
     rows = np.array(rows)
     ref, ref_lse = oracle.decode_attn_rows(q_bits, kh, vh, case.page_table, case.seq_lens, rows)
     check(out.float().cpu().numpy()[rows], ref, lse.cpu().numpy()[rows], ref_lse)
