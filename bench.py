@@ -186,65 +186,12 @@ def profiled_traffic(workload: str, fused: bool):
 
 # ------------------------------------------------------------ GPU arm
 
-# Per-CTA costs of the tensor-core kernel, measured on GB300 with every SM streaming: one
-# 128-token sub-tile in steady state, and the hand-over from one run (segment member block)
-# to the next (epilogue of one, first P of the other).
-TC_SUBTILE_US = 1.55
-TC_RUN_US = 4.7
-
-
-def tc_cta_costs(rlt, case, chunk, tails, ctas):
-    """Estimated busy time of each tensor-core CTA: the kernel gives CTA c the contiguous work
-    items [c*n/ctas, (c+1)*n/ctas) of (kv head, segment, member block, chunk) and pays one run
-    hand-over per change of (kv head, segment, member block) inside that range."""
-    plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, chunk, tails, case.group)
-    per_block = 128 // case.group
-    units = []
-    for si, seg in enumerate(plan.segments):
-        n, mc = int(seg[1]), int(seg[4])
-        for mb in range(-(-mc // per_block)):
-            for c in range(max(1, -(-n // chunk))):
-                units.append((si, mb, min(chunk, n - c * chunk)))
-    items = [(g,) + u for g in range(case.num_kv_heads) for u in units]
-    n = len(items)
-    ctas = max(1, min(ctas, n))
-    costs = []
-    for c in range(ctas):
-        run, runs, tiles = None, 0, 0
-        for it in items[c * n // ctas:(c + 1) * n // ctas]:
-            tiles += it[3]
-            if it[:3] != run:
-                run, runs = it[:3], runs + 1
-        costs.append(tiles * TC_SUBTILE_US + runs * TC_RUN_US)
-    return costs
-
-
 def auto_chunk_tiles(rlt, case, tails, num_sms):
-    """Tiles per work item of the persistent tensor-core kernel.
-
-    With private tails the tensor-core kernel does the whole call on one CTA per SM, so the
-    call ends with its busiest CTA: take the chunk (4..16 tiles) whose contiguous item split
-    gives the smallest estimated maximum (tc_cta_costs), the larger chunk on a tie.
-    Otherwise the split-K kernel runs beside it on the other SMs: the largest power of two
-    (4..16) that still gives every CTA at least 16 items; never below 4 tiles (or a segment's
-    length), since every item adds a partial to merge."""
-    p1 = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, 1, tails, case.group)
-    longest = max((int(s[1]) for s in p1.segments), default=1)
-    if tails:
-        best = None
-        for chunk in range(4, 17):
-            cost = max(tc_cta_costs(rlt, case, chunk, tails, num_sms))
-            if best is None or cost <= best[0] + 1e-9:
-                best = (cost, chunk)
-        return min(best[1], max(1, longest))
-    per_block = 128 // case.group
-    tiles = sum(int(s[1]) * -(-int(s[4]) // per_block) for s in p1.segments) * case.num_kv_heads
-    chunk = 16
-    while chunk > 4 and tiles / chunk < 16 * num_sms:
-        chunk //= 2
-    while chunk > 1 and chunk > longest:
-        chunk //= 2
-    return chunk
+    """Tiles per work item of the persistent tensor-core kernel: the library's choice for this
+    batch (rlt_choose_chunk_tiles: with private tails the chunk whose contiguous item split has
+    the least-loaded busiest CTA, otherwise at least 16 items per CTA)."""
+    return rlt.rlt_choose_chunk_tiles(case.page_table, case.seq_lens, case.page_size, case.group, tails,
+                                      case.num_kv_heads, num_sms)
 
 
 def run_gpu(args, rank, world):

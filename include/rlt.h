@@ -266,6 +266,25 @@ RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t max_pages,
                                    int32_t *member_limit, int32_t max_member_entries,
                                    int32_t *request_prefix, int32_t *sizes);
 
+/*
+ * Work-item size (chunk_tiles) for rlt_plan_prefix / rlt_paged_decode_attn_prefix, HOST
+ * function, from the same host page tables and lengths the plan is built from.  The
+ * tensor-core kernel gives each of its CTAs a contiguous run of (kv head, segment, member
+ * block, chunk) items.  With private_tails it does the whole call, so the call ends with its
+ * busiest CTA: the function builds the plan for every chunk of 4..16 tiles, estimates each
+ * CTA's busy time (1.55 us per 128-token sub-tile plus 4.7 us per change of run, both measured
+ * on GB300) over num_ctas CTAs, and returns the chunk with the smallest maximum (the larger on
+ * a tie).  Without private tails a split-K kernel shares the SMs: it returns the largest
+ * power of two in 4..16 that still gives every CTA at least 16 items.  Either result is
+ * capped at the longest segment.  num_ctas: the tensor-core CTAs (the SM count when the
+ * kernel has the GPU to itself).  Returns the chunk (>= 1), or -RLT_ERR_INVALID_ARG /
+ * -RLT_ERR_UNSUPPORTED as rlt_plan_prefix would fail.
+ */
+RLT_API int32_t rlt_choose_chunk_tiles(const int32_t *page_table, int32_t max_pages,
+                                       const int32_t *seq_lens, int32_t batch, int32_t page_size,
+                                       int32_t query_group, int32_t private_tails,
+                                       int32_t num_kv_heads, int32_t num_ctas);
+
 /* Device workspace bytes of rlt_paged_decode_attn_prefix (sizes[5] and sizes[3]
  * of the plan as max_rest_len and max_prefix_slots). */
 RLT_API size_t rlt_paged_decode_prefix_workspace_size(int32_t batch, int32_t num_q_heads,

@@ -28,7 +28,7 @@ __all__ = [
     "rlt_paged_decode_workspace_size", "rlt_paged_decode_attn", "rlt_paged_decode_attn_noalloc",
     "rlt_latent_noise_init",
     "rlt_noise_hash24", "rlt_paged_gather", "rlt_validate_batch", "rlt_get_device_error",
-    "rlt_version", "PrefixPlan", "rlt_plan_prefix", "rlt_paged_decode_attn_prefix",
+    "rlt_version", "PrefixPlan", "rlt_plan_prefix", "rlt_choose_chunk_tiles", "rlt_paged_decode_attn_prefix",
     "rlt_paged_decode_prefix_workspace_size", "rlt_kv_append_rope", "rlt_publishable_prefix",
     "ExtendPlan", "rlt_plan_extend", "rlt_paged_extend_attn", "DEVERR_BAD_PAGE", "DEVERR_BAD_SLOT", "DEVERR_TIMEOUT", "DEVERR_BAD_LEN",
 ]
@@ -87,6 +87,7 @@ def load():
         "rlt_validate_batch": (ctypes.c_int, [P, i32, P, i32, P, i64, i32]),
         "rlt_plan_prefix": (ctypes.c_int, [P, i32, P, i32, i32, i32, i32, i32, P, i32, P, P, i32, P, P]),
         "rlt_paged_decode_prefix_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, i32]),
+        "rlt_choose_chunk_tiles": (i32, [P, i32, P, i32, i32, i32, i32, i32, i32]),
         "rlt_paged_decode_attn_prefix": (ctypes.c_int, [pool_p, i32, P, P, P, i32, P, i32, P, i32, i32, P, P, P, P, i32,
                                                         i32, i32, i32, i32, f32, P, P, P, sz, i32, i32, P]),
         "rlt_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
@@ -411,6 +412,18 @@ def rlt_plan_prefix(page_table, seq_lens, page_size: int, chunk_tiles: int = 4,
     _check(st, "rlt_plan_prefix")
     n = int(sizes[0])
     return PrefixPlan(seg[:n], mem[: int(sizes[1])], lim[: int(sizes[1])], req, sizes, chunk_tiles, query_group)
+
+
+def rlt_choose_chunk_tiles(page_table, seq_lens, page_size: int, query_group: int, private_tails: bool,
+                           num_kv_heads: int, num_ctas: int) -> int:
+    """Tiles per work item for rlt_plan_prefix (host arrays in): see the C declaration."""
+    pt, ptp = _host(page_table, np.int32)
+    sl, slp = _host(seq_lens, np.int32)
+    r = int(load().rlt_choose_chunk_tiles(ptp, pt.shape[1], slp, sl.size, int(page_size), int(query_group),
+                                          1 if private_tails else 0, int(num_kv_heads), int(num_ctas)))
+    if r < 1:
+        raise RltError(-r, "rlt_choose_chunk_tiles")
+    return r
 
 
 def rlt_paged_decode_prefix_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_rest_len,

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <mutex>
 #include <unordered_set>
+#include <vector>
 
 #include "rlt.h"
 #include "rlt_internal.h"
@@ -287,6 +288,108 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
     const double s = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)pool->head_dim);
     p.qscale = (float)(s * 1.4426950408889634);   // log2(e): softmax in base 2
     return from_cuda(rlt::launch_decode(p, pool->head_dim, group, static_cast<cudaStream_t>(stream)));
+}
+
+// Per-CTA costs of the tensor-core kernel measured on GB300 with every SM streaming: one
+// 128-token sub-tile in steady state, and the hand-over from one run (kv head, segment,
+// member block) to the next.
+constexpr double kTcSubTileUs = 1.55;
+constexpr double kTcRunUs = 4.7;
+
+RLT_API int32_t rlt_choose_chunk_tiles(const int32_t *page_table, int32_t max_pages,
+                                                  const int32_t *seq_lens, int32_t batch,
+                                                  int32_t page_size, int32_t query_group,
+                                                  int32_t private_tails, int32_t num_kv_heads,
+                                                  int32_t num_ctas)
+{
+    if (batch < 0 || num_kv_heads < 1 || num_ctas < 1 || query_group < 1 || query_group > 128)
+        return -RLT_ERR_INVALID_ARG;
+    std::vector<int32_t> seg, mem, lim, req(2 * (size_t)std::max(batch, 1));
+    int32_t sizes[7] = {0, 0, 0, 0, 0, 0, 0};
+    auto plan = [&](int chunk) -> rlt_status {
+        size_t seg_cap = 2 * (size_t)batch + 1, mem_cap = 4 * (size_t)batch + 1;
+        for (int attempt = 0; attempt < 2; ++attempt) {
+            seg.assign(seg_cap * rlt::kSegFields, 0);
+            mem.assign(mem_cap, 0);
+            lim.assign(mem_cap, 0);
+            const rlt_status st = rlt_plan_prefix(page_table, max_pages, seq_lens, batch, page_size, chunk,
+                                                  query_group, private_tails, seg.data(), (int32_t)seg_cap,
+                                                  mem.data(), lim.data(), (int32_t)mem_cap, req.data(), sizes);
+            if (st != RLT_ERR_OUT_OF_RANGE)
+                return st;
+            seg_cap = std::max(sizes[0], 1);
+            mem_cap = std::max(sizes[1], 1);
+        }
+        return RLT_ERR_OUT_OF_RANGE;
+    };
+    rlt_status st = plan(1);
+    if (st != RLT_OK)
+        return -st;
+    const int per_block = 128 / query_group;
+    int longest = 1;
+    int64_t tiles = 0;
+    for (int s = 0; s < sizes[0]; ++s) {
+        const int32_t *sd = &seg[(size_t)s * rlt::kSegFields];
+        longest = std::max(longest, (int)sd[rlt::kSegNumTiles]);
+        tiles += (int64_t)sd[rlt::kSegNumTiles] * ((sd[rlt::kSegMemberCount] + per_block - 1) / per_block);
+    }
+    tiles *= num_kv_heads;
+    if (!private_tails) {
+        // a split-K kernel shares the SMs: the largest power of two (4..16) that still gives
+        // every CTA at least 16 items, never below 4 tiles (each item adds a partial), nor
+        // above the longest segment
+        int chunk = 16;
+        while (chunk > 4 && tiles < (int64_t)chunk * 16 * num_ctas)
+            chunk /= 2;
+        while (chunk > 1 && chunk > longest)
+            chunk /= 2;
+        return chunk;
+    }
+    // The tensor-core kernel does the whole call, one CTA per SM, each taking a contiguous
+    // run of items: the call ends with the busiest CTA.  Estimate each CTA's busy time from
+    // the plan and take the chunk (4..16) with the smallest maximum, the larger on a tie.
+    struct Unit {
+        int s, mb, tiles;
+    };
+    int best_chunk = 4;
+    double best_cost = -1.0;
+    for (int chunk = 4; chunk <= 16; ++chunk) {
+        if ((st = plan(chunk)) != RLT_OK)
+            return -st;
+        std::vector<Unit> units;
+        for (int s = 0; s < sizes[0]; ++s) {
+            const int32_t *sd = &seg[(size_t)s * rlt::kSegFields];
+            const int n = sd[rlt::kSegNumTiles], mc = sd[rlt::kSegMemberCount];
+            const int nch = std::max(1, (n + chunk - 1) / chunk);
+            for (int mb = 0; mb < (mc + per_block - 1) / per_block; ++mb)
+                for (int c = 0; c < nch; ++c)
+                    units.push_back({s, mb, std::min(chunk, n - c * chunk)});
+        }
+        const int64_t n_items = (int64_t)units.size() * num_kv_heads;
+        if (n_items == 0)
+            continue;
+        const int64_t ctas = std::min<int64_t>(num_ctas, n_items);
+        double worst = 0.0;
+        for (int64_t c = 0; c < ctas; ++c) {
+            const int64_t i0 = c * n_items / ctas, i1 = (c + 1) * n_items / ctas;
+            int64_t run_key = -1, runs = 0, t = 0;
+            for (int64_t i = i0; i < i1; ++i) {
+                const Unit &u = units[(size_t)(i % (int64_t)units.size())];
+                const int64_t key = ((i / (int64_t)units.size()) * (sizes[0] + 1) + u.s) * 4096 + u.mb;
+                t += u.tiles;
+                if (key != run_key) {
+                    run_key = key;
+                    ++runs;
+                }
+            }
+            worst = std::max(worst, t * kTcSubTileUs + runs * kTcRunUs);
+        }
+        if (best_cost < 0.0 || worst <= best_cost + 1e-9) {
+            best_cost = worst;
+            best_chunk = chunk;
+        }
+    }
+    return std::min(best_chunk, longest);
 }
 
 RLT_API size_t rlt_paged_decode_prefix_workspace_size(int32_t batch, int32_t num_q_heads,

@@ -219,3 +219,76 @@ def test_extend_plan_by_brute_force(G, chunk_tiles):
 def test_extend_plan_rejects_more_new_tokens_than_the_sequence():
     with pytest.raises(rlt.RltError):
         rlt.rlt_plan_extend([10], [11], 16)
+
+
+# ---------------------------------------------------------------- work-item size
+
+def busiest_cta(case, chunk, tails, ctas, sub_us=1.55, run_us=4.7):
+    """Brute-force estimate of the tensor-core kernel's busiest CTA for one chunk size: items
+    (kv head, segment, member block, chunk) in the kernel's order, contiguous equal-count runs of
+    them per CTA, each CTA paying its tiles and one hand-over per change of (head, segment, block)."""
+    plan = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, chunk, tails, case.group)
+    per_block = 128 // case.group
+    units = []
+    for si, seg in enumerate(plan.segments):
+        n, mc = int(seg[1]), int(seg[4])
+        for mb in range(-(-mc // per_block)):
+            for c in range(max(1, -(-n // chunk))):
+                units.append((si, mb, min(chunk, n - c * chunk)))
+    items = [(g,) + u for g in range(case.num_kv_heads) for u in units]
+    n = len(items)
+    ctas = min(ctas, n)
+    worst = 0.0
+    for c in range(ctas):
+        run, runs, tiles = None, 0, 0
+        for it in items[c * n // ctas:(c + 1) * n // ctas]:
+            tiles += it[3]
+            if it[:3] != run:
+                run, runs = it[:3], runs + 1
+        worst = max(worst, tiles * sub_us + runs * run_us)
+    return worst
+
+
+@pytest.mark.parametrize("name,ctas", [("longctx", 152), ("longctx", 100), ("huginn", 152), ("huginn", 37)])
+def test_choose_chunk_tiles_private_tails_minimises_the_busiest_cta(name, ctas):
+    case = W.config(name)
+    got = rlt.rlt_choose_chunk_tiles(case.page_table, case.seq_lens, case.page_size, case.group, True,
+                                     case.num_kv_heads, ctas)
+    costs = {c: busiest_cta(case, c, True, ctas) for c in range(4, 17)}
+    best = min(costs.values())
+    assert costs[got] <= best + 1e-6
+    # the larger on a tie, no larger than the longest segment
+    longest = max(int(s[1]) for s in rlt.rlt_plan_prefix(case.page_table, case.seq_lens, case.page_size, 1, True,
+                                                         case.group).segments)
+    assert got == min(max(c for c, v in costs.items() if v <= best + 1e-6), longest)
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_choose_chunk_tiles_custom_batches(G):
+    case = W.custom(B=7, Hq=8 * G, Hkv=8, D=128, ps=16, seq_lens=[3000, 2600, 4100, 1700, 2222, 900, 5000],
+                    shared_frac=0.8, seed=40 + G)
+    for ctas in (19, 152):
+        got = rlt.rlt_choose_chunk_tiles(case.page_table, case.seq_lens, case.page_size, G, True, 8, ctas)
+        costs = {c: busiest_cta(case, c, True, ctas) for c in range(4, 17)}
+        longest = max(int(s[1]) for s in rlt.rlt_plan_prefix(case.page_table, case.seq_lens, 16, 1, True, G).segments)
+        best = min(costs.values())
+        want = min(max(c for c, v in costs.items() if v <= best + 1e-6), longest)
+        assert got == want
+        # without private tails: the count rule (16 items per CTA, 4..16 tiles, power of two)
+        got2 = rlt.rlt_choose_chunk_tiles(case.page_table, case.seq_lens, case.page_size, G, False, 8, ctas)
+        p1 = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, 16, 1, False, G)
+        tiles = sum(int(s[1]) * -(-int(s[4]) // (128 // G)) for s in p1.segments) * 8
+        chunk = 16
+        while chunk > 4 and tiles < chunk * 16 * ctas:
+            chunk //= 2
+        while chunk > 1 and chunk > max([int(s[1]) for s in p1.segments] + [1]):
+            chunk //= 2
+        assert got2 == chunk
+
+
+def test_choose_chunk_tiles_rejects_bad_arguments():
+    case = W.config("tiny")
+    with pytest.raises(rlt.RltError):
+        rlt.rlt_choose_chunk_tiles(case.page_table, case.seq_lens, case.page_size, 1, True, 0, 152)
+    with pytest.raises(rlt.RltError):
+        rlt.rlt_choose_chunk_tiles(case.page_table, case.seq_lens, 48, 1, True, 2, 152)
