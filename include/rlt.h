@@ -16,6 +16,16 @@
  * time is skipped and recorded in the device error word
  * (rlt_get_device_error).
  *
+ * Debug mode: with RLT_VALIDATE=1 in the environment (read at each call),
+ * rlt_kv_append, rlt_paged_decode_attn and rlt_paged_decode_attn_prefix first
+ * synchronise the stream, copy the batch's device arrays to the host and check
+ * them: append slots inside the pool and distinct; page-table entries in use
+ * and lengths in range, and, with a fused append, each request's newest slot
+ * on a page no other request maps (rlt_validate_batch's rules).  A violation
+ * returns RLT_ERR_OUT_OF_RANGE / RLT_ERR_INVALID_ARG and launches nothing.
+ * While the stream is being captured the check is skipped (a capture cannot
+ * synchronise).
+ *
  * CUDA graphs: every compute call may be recorded by stream capture, so that a
  * whole decode step (every layer-plane bank's append and attention, the noise)
  * is one graph submission, as the pages' engines run decode ([FFM] "Recurrent

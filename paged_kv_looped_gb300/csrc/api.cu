@@ -4,6 +4,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 #include <unordered_set>
 #include <vector>
@@ -107,6 +108,72 @@ rlt_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RLT_OK : RLT_ERR
 
 }  // namespace
 
+namespace {
+
+// Debug mode: with RLT_VALIDATE=1 in the environment (read at each call) the compute calls
+// synchronise the stream, copy the batch's device arrays to the host and check them
+// before launching; a violation fails the call.  Not while the stream is being captured
+// (a capture cannot synchronise): there the calls run unchecked.
+bool validate_enabled()
+{
+    const char *v = std::getenv("RLT_VALIDATE");
+    return v != nullptr && v[0] == '1' && v[1] == '\0';
+}
+
+// Host copies of a batch for validation; false (status set) if the stream is capturing or
+// a CUDA call failed.
+bool fetch_for_validation(cudaStream_t stream, rlt_status *st)
+{
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        *st = RLT_ERR_CUDA;
+        return false;
+    }
+    *st = RLT_OK;
+    if (cap != cudaStreamCaptureStatusNone)
+        return false;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        *st = RLT_ERR_CUDA;
+        return false;
+    }
+    return true;
+}
+
+template <typename T>
+bool copy_to_host(std::vector<T> &h, const T *d, size_t n)
+{
+    h.resize(n);
+    return n == 0 || cudaMemcpy(h.data(), d, n * sizeof(T), cudaMemcpyDeviceToHost) == cudaSuccess;
+}
+
+// The attention calls' check: page-table entries in use and lengths in range; with a fused
+// append, each request's newest slot is derived from its page table and must lie on a page
+// no other request maps (shared pages are read-only).
+rlt_status validate_attention_batch(const int32_t *page_table, int32_t max_pages, const int32_t *seq_lens,
+                                    int32_t batch, int64_t num_pages, int32_t page_size, bool fused,
+                                    cudaStream_t stream)
+{
+    rlt_status st = RLT_OK;
+    if (!fetch_for_validation(stream, &st))
+        return st;
+    std::vector<int32_t> pt, sl;
+    if (!copy_to_host(pt, page_table, (size_t)batch * max_pages) || !copy_to_host(sl, seq_lens, (size_t)batch))
+        return RLT_ERR_CUDA;
+    std::vector<int64_t> slots;
+    if (fused) {
+        slots.assign((size_t)batch, -1);
+        for (int32_t b = 0; b < batch; ++b) {
+            const int64_t L = sl[b];
+            if (L >= 1 && L <= (int64_t)max_pages * page_size)
+                slots[b] = (int64_t)pt[(size_t)b * max_pages + (L - 1) / page_size] * page_size + (L - 1) % page_size;
+        }
+    }
+    return rlt_validate_batch(pt.data(), max_pages, sl.data(), batch, fused ? slots.data() : nullptr, num_pages,
+                              page_size);
+}
+
+}  // namespace
+
 extern "C" {
 
 RLT_API const char *rlt_status_string(rlt_status status)
@@ -151,6 +218,24 @@ RLT_API rlt_status rlt_kv_append(const rlt_kv_pool *pool, int32_t bank, const vo
         return RLT_ERR_INVALID_ARG;
     if (!aligned16(k_new) || !aligned16(v_new) || reinterpret_cast<uintptr_t>(out_loc) % 8 != 0)
         return RLT_ERR_INVALID_ARG;
+    if (validate_enabled()) {
+        std::vector<int64_t> loc;
+        if (fetch_for_validation(static_cast<cudaStream_t>(stream), &st)) {
+            if (!copy_to_host(loc, out_loc, (size_t)n_tokens))
+                return RLT_ERR_CUDA;
+            std::unordered_set<int64_t> seen;
+            for (const int64_t slot : loc) {
+                if (slot < 0)
+                    continue;
+                if (slot >= pool->num_pages * pool->page_size)
+                    return RLT_ERR_OUT_OF_RANGE;
+                if (!seen.insert(slot).second)
+                    return RLT_ERR_INVALID_ARG;   // two tokens written to one slot
+            }
+        } else if (st != RLT_OK) {
+            return st;
+        }
+    }
     unsigned int *err = nullptr;
     if ((st = device_info(&err, nullptr)) != RLT_OK)
         return st;
@@ -250,6 +335,10 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
     if (!std::isfinite(scale) || (k_new == nullptr) != (v_new == nullptr) || !aligned16(k_new) ||
         !aligned16(v_new))
         return RLT_ERR_INVALID_ARG;
+    if (validate_enabled() &&
+        (st = validate_attention_batch(page_table, max_pages, seq_lens, batch, pool->num_pages, pool->page_size,
+                                       k_new != nullptr, static_cast<cudaStream_t>(stream))) != RLT_OK)
+        return st;
 
     unsigned int *err = nullptr;
     int sms = 0;
@@ -444,6 +533,10 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
         return RLT_ERR_INVALID_ARG;
     if ((k_new == nullptr) != (v_new == nullptr) || !aligned16(k_new) || !aligned16(v_new))
         return RLT_ERR_INVALID_ARG;
+    if (validate_enabled() &&
+        (st = validate_attention_batch(page_table, max_pages, seq_lens, batch, pool->num_pages, pool->page_size,
+                                       k_new != nullptr, static_cast<cudaStream_t>(stream))) != RLT_OK)
+        return st;
     const int64_t bank_rows = pool->num_pages * pool->num_kv_heads * (int64_t)pool->page_size;
     if (bank_rows >= (int64_t(1) << 31))
         return RLT_ERR_UNSUPPORTED;
