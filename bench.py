@@ -685,7 +685,10 @@ def main():
                      "kernel": ("rlt_paged_decode_attn_prefix (tcgen05 shared-prefix + split-K + combine)"
                                 if r["cascade"] else "rlt_paged_decode_attn (split-K partial + combine)")
                                + (", append fused" if fused else ""),
-                     "achieved": round(achieved, 2), "peak": peak, "peak_kind": f"{peak_kind} (HBM copy)",
+                     "achieved": round(achieved, 2),
+                     "achieved_logical": round((attn_bytes(case, unique=False) + (a_bytes - attn_bytes(case)))
+                                               / (attn_launch_ms * 1e-3) / 1e9, 2),
+                     "peak": peak, "peak_kind": f"{peak_kind} (HBM copy)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": a_bytes, "launch_us": round(attn_launch_ms * 1e3, 2),
                      "timing": r["attn_timing"],
