@@ -85,10 +85,12 @@ struct DecodePlan {
 };
 
 // waves: the library's split (split_tokens == 0) is the largest that still gives
-// every SM this many waves of 3 CTAs; 8 for plain decode, fewer for the short
+// every SM this many waves of 3 CTAs; 8 for plain decode, one for the short
 // unshared rests a shared-prefix call leaves, which share the GPU with the
-// tensor-core kernel.
-constexpr int kPlainWaves = 8, kRestWaves = 3;
+// tensor-core kernel: there each CTA's start-up round trips weigh most, so a
+// rest is split only when one wave would leave SMs idle (measured on the huginn
+// shape: 30.3 us per call with one wave, 32.3 with three).
+constexpr int kPlainWaves = 8, kRestWaves = 1;
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                        int32_t head_dim, int32_t max_seq_len, int32_t split_tokens, int num_sms,
                        int waves = kPlainWaves);
