@@ -93,15 +93,20 @@ typedef enum rlt_status {
 #define RLT_DEVERR_BAD_LEN 8u         /* a seq_len outside [0, min(max_pages*page_size,
                                          max_seq_len rounded to the split grid)] was clamped */
 
+/* Element type of a KV pool.  The pages' engines keep K/V in bf16, and so does
+ * every kernel here: any other value is refused with RLT_ERR_UNSUPPORTED. */
+typedef enum rlt_dtype { RLT_BF16 = 0 } rlt_dtype;
+
 /* A paged KV pool (device memory owned by the caller). */
 typedef struct rlt_kv_pool {
-    void *k;                /* bf16 [num_banks][num_pages][num_kv_heads][page_size][head_dim] */
+    void *k;                /* dtype [num_banks][num_pages][num_kv_heads][page_size][head_dim] */
     void *v;                /* same shape as k */
     int64_t num_pages;      /* physical pages per bank */
     int32_t num_banks;      /* one bank per (layer, plane) the model holds */
     int32_t num_kv_heads;
     int32_t page_size;      /* tokens per page, >= 1 */
     int32_t head_dim;       /* 64 or 128 */
+    int32_t dtype;          /* rlt_dtype: RLT_BF16 */
 } rlt_kv_pool;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -121,6 +126,16 @@ RLT_API int32_t rlt_version(void);
  */
 RLT_API int32_t rlt_bank_map(const uint8_t *recurrent, int32_t num_layers, int32_t num_planes,
                      int32_t *map_out);
+
+/*
+ * One entry of that map, HOST function (same passages): the bank that holds
+ * (layer, plane), looked up in map (int32 [num_layers][num_planes], as
+ * rlt_bank_map writes it).  Returns -1 where the plane does not hold the layer
+ * (a prelude or coda layer at plane >= 1) and for a null map or a layer or
+ * plane outside the map.
+ */
+RLT_API int32_t rlt_bank_index(const int32_t *map, int32_t num_layers, int32_t num_planes, int32_t layer,
+                               int32_t plane);
 
 /*
  * KV append = store_kv ([FFM] "LOTUS"): for i < n_tokens with out_loc[i] >= 0,
@@ -402,7 +417,13 @@ RLT_API rlt_status rlt_paged_extend_attn(
  *   - Each device that loads the library holds the array until the process
  *     exits.  The first call on a device looks up the array's device address
  *     (with that device current); make that first call before any stream
- *     capture.
+ *     capture.  The address is kept for the life of the process, so this entry
+ *     point supports only the device's primary context (the runtime's): after a
+ *     cudaDeviceReset, or from another driver context on the same device, it
+ *     would hand the kernels a stale address.
+ *   - Arguments are checked as rlt_paged_decode_attn checks them, in the same
+ *     order, before the scratch size: a bad pool, bank, split or pointer gets
+ *     the status rlt_paged_decode_attn would return.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; nothing in it needs to start at zero.  Calls that overlap on the
  *     GPU (other streams, other host threads) race on it: serialise them.

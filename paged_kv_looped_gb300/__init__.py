@@ -8,6 +8,7 @@ has not been built, every call raises.
 Functions keep the C names:
 
 * ``rlt_bank_map``          (layer, plane) -> KV bank map (host).
+* ``rlt_bank_index``        one (layer, plane) entry of that map (host).
 * ``rlt_kv_append``         store_kv: scatter this step's K/V rows to their slots.
 * ``rlt_paged_decode_attn`` split-K paged GQA decode attention (+ combine).
 * ``rlt_latent_noise_init`` position-keyed truncated-normal latent noise.
@@ -24,7 +25,7 @@ import os
 import numpy as np
 
 __all__ = [
-    "RltError", "KVPool", "library_path", "load", "rlt_bank_map", "rlt_kv_append",
+    "RltError", "KVPool", "library_path", "load", "rlt_bank_map", "rlt_bank_index", "rlt_kv_append",
     "rlt_paged_decode_workspace_size", "rlt_paged_decode_attn", "rlt_paged_decode_attn_noalloc",
     "rlt_latent_noise_init",
     "rlt_noise_hash24", "rlt_paged_gather", "rlt_validate_batch", "rlt_get_device_error",
@@ -50,7 +51,10 @@ class RltError(RuntimeError):
 class rlt_kv_pool(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_pages", ctypes.c_int64),
                 ("num_banks", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
-                ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+                ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+RLT_BF16 = 0
 
 
 _lib = None
@@ -75,6 +79,7 @@ def load():
         "rlt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "rlt_version": (i32, []),
         "rlt_bank_map": (i32, [P, i32, i32, P]),
+        "rlt_bank_index": (i32, [P, i32, i32, i32, i32]),
         "rlt_kv_append": (ctypes.c_int, [pool_p, i32, P, P, P, i32, P]),
         "rlt_paged_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
         "rlt_paged_decode_attn": (ctypes.c_int, [pool_p, i32, P, P, P, i32, P, i32, P, i32, i32, f32, P, P, P,
@@ -148,7 +153,7 @@ class KVPool:
         self.k, self.v = k, v
         nb, P, Hkv, ps, D = k.shape
         self.num_banks, self.num_pages, self.num_kv_heads, self.page_size, self.head_dim = nb, P, Hkv, ps, D
-        self.struct = rlt_kv_pool(k.data_ptr(), v.data_ptr(), P, nb, Hkv, ps, D)
+        self.struct = rlt_kv_pool(k.data_ptr(), v.data_ptr(), P, nb, Hkv, ps, D, RLT_BF16)
 
     @classmethod
     def empty(cls, num_banks, num_pages, num_kv_heads, page_size, head_dim, device="cuda"):
@@ -172,6 +177,14 @@ def rlt_bank_map(recurrent, num_planes: int):
     if n < 0:
         raise RltError(-n, "rlt_bank_map")
     return out, int(n)
+
+
+def rlt_bank_index(bank_map, layer: int, plane: int) -> int:
+    """The bank holding (layer, plane) in a map from rlt_bank_map, or -1 where the plane does not hold it."""
+    m, mp = _host(bank_map, np.int32)
+    if m.ndim != 2:
+        raise ValueError("bank_map must be int32 [num_layers][num_planes]")
+    return int(load().rlt_bank_index(mp, m.shape[0], m.shape[1], int(layer), int(plane)))
 
 
 def rlt_validate_batch(page_table, seq_lens, new_slots, num_pages: int, page_size: int) -> int:
@@ -235,6 +248,20 @@ def rlt_paged_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, 
                                                       max_seq_len, split_tokens))
 
 
+def _check_q_out(pool, q, out, lse_out):
+    """q [B][Hq][D] against the pool's head_dim; out (if given) shaped like q, lse_out [B][Hq].
+    The C ABI takes no head_dim for q: a mismatch here would read and write past the arrays."""
+    if q.dim() != 3:
+        raise ValueError("q must be [B][Hq][head_dim]")
+    B, Hq, D = q.shape
+    if D != pool.head_dim:
+        raise ValueError(f"q head_dim {D} does not match the pool's {pool.head_dim}")
+    if out is not None and tuple(out.shape) != (B, Hq, D):
+        raise ValueError(f"out must be [B][Hq][D] = {(B, Hq, D)}")
+    if lse_out is not None and tuple(lse_out.shape) != (B, Hq):
+        raise ValueError(f"lse_out must be [B][Hq] = {(B, Hq)}")
+
+
 def _new_rows(k_new, v_new, B, Hkv, D):
     """Device pointers of the optional fused-append rows (bf16 [B][Hkv][D] each, or both None)."""
     import torch
@@ -255,9 +282,8 @@ def rlt_paged_decode_attn(pool: KVPool, bank: int, q, page_table, seq_lens, max_
     seq_lens int32 [B].  With k_new / v_new (bf16 [B][Hkv][D]) each request's new token is
     stored at position seq_lens[b] - 1 by the same call (fused append).  Returns out."""
     import torch
+    _check_q_out(pool, q, out, lse_out)
     B, Hq, D = q.shape
-    if D != pool.head_dim:
-        raise ValueError("q head_dim does not match the pool")
     if out is None:
         out = torch.empty_like(q)
     ws_need = rlt_paged_decode_workspace_size(B, Hq, pool.num_kv_heads, D, max_seq_len, split_tokens)
@@ -289,6 +315,7 @@ def rlt_paged_decode_attn_noalloc(pool: KVPool, bank: int, q, page_table, seq_le
     Calls on one device share the scratch array: calls that overlap on the GPU race.
     """
     import torch
+    _check_q_out(pool, q, out, lse_out)
     B, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)
@@ -438,7 +465,10 @@ def rlt_paged_decode_attn_prefix(pool: KVPool, bank: int, q, page_table, seq_len
     """Paged decode attention reading shared-prefix tiles once (plan from rlt_plan_prefix, .to(device)).
     k_new / v_new: the fused append, as in rlt_paged_decode_attn."""
     import torch
+    _check_q_out(pool, q, out, lse_out)
     B, Hq, D = q.shape
+    if page_table.dim() != 2 or page_table.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("page_table must be [B][max_pages] and seq_lens [B]")
     if plan.num_segments and plan.query_group != Hq // pool.num_kv_heads:
         raise ValueError("the plan was built for another query group")
     if plan.dev is None:
@@ -515,6 +545,7 @@ def rlt_paged_extend_attn(pool: KVPool, bank: int, q, page_table, plan: ExtendPl
                           workspace=None, scale: float = 0.0, max_ctas: int = 0, stream=None):
     """Causal extend attention: q/out bf16 [new tokens][Hq][D] packed request by request."""
     import torch
+    _check_q_out(pool, q, out, lse_out)
     N, Hq, D = q.shape
     if plan.num_rows != N:
         raise ValueError("the plan was built for another number of new tokens")

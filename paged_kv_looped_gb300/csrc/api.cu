@@ -94,6 +94,8 @@ rlt_status check_pool(const rlt_kv_pool *pool, int32_t bank)
         return RLT_ERR_INVALID_ARG;
     if (!aligned16(pool->k) || !aligned16(pool->v))
         return RLT_ERR_INVALID_ARG;
+    if (pool->dtype != RLT_BF16)
+        return RLT_ERR_UNSUPPORTED;
     if (bank < 0 || bank >= pool->num_banks)
         return RLT_ERR_OUT_OF_RANGE;
     return RLT_OK;
@@ -174,6 +176,43 @@ rlt_status validate_attention_batch(const int32_t *page_table, int32_t max_pages
 
 }  // namespace
 
+namespace rlt {
+
+rlt_status check_decode_args(const rlt_kv_pool *pool, int32_t bank, const void *q, const void *k_new,
+                             const void *v_new, int32_t num_q_heads, const int32_t *page_table, int32_t max_pages,
+                             const int32_t *seq_lens, int32_t batch, int32_t max_seq_len, float scale,
+                             const void *out, int32_t split_tokens, bool *empty)
+{
+    *empty = false;
+    rlt_status st = check_pool(pool, bank);
+    if (st != RLT_OK)
+        return st;
+    if (batch < 0 || max_seq_len < 0 || max_pages < 0 || num_q_heads < 1 || split_tokens < 0 ||
+        split_tokens % kTileTokens != 0 || split_tokens > 128 * kTileTokens)
+        return RLT_ERR_INVALID_ARG;
+    if (num_q_heads % pool->num_kv_heads != 0)
+        return RLT_ERR_INVALID_ARG;
+    const int group = num_q_heads / pool->num_kv_heads;
+    if (!decode_supported(pool->head_dim, group) || pool->page_size % kTileTokens != 0)
+        return RLT_ERR_UNSUPPORTED;
+    if (batch > 65535 || pool->num_kv_heads > 65535)
+        return RLT_ERR_UNSUPPORTED;
+    if (batch == 0) {
+        *empty = true;
+        return RLT_OK;
+    }
+    if (q == nullptr || page_table == nullptr || seq_lens == nullptr || out == nullptr || max_pages < 1)
+        return RLT_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out))
+        return RLT_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || (k_new == nullptr) != (v_new == nullptr) || !aligned16(k_new) ||
+        !aligned16(v_new))
+        return RLT_ERR_INVALID_ARG;
+    return RLT_OK;
+}
+
+}  // namespace rlt
+
 extern "C" {
 
 RLT_API const char *rlt_status_string(rlt_status status)
@@ -201,6 +240,15 @@ RLT_API int32_t rlt_bank_map(const uint8_t *recurrent, int32_t num_layers, int32
         for (int32_t l = 0; l < num_layers; ++l)
             map_out[l * num_planes + t] = (t == 0 || recurrent[l] != 0) ? next++ : -1;
     return next;
+}
+
+RLT_API int32_t rlt_bank_index(const int32_t *map, int32_t num_layers, int32_t num_planes, int32_t layer,
+                               int32_t plane)
+{
+    if (map == nullptr || layer < 0 || layer >= num_layers || plane < 0 || plane >= num_planes)
+        return -1;
+    const int32_t bank = map[(int64_t)layer * num_planes + plane];
+    return bank >= 0 ? bank : -1;
 }
 
 RLT_API rlt_status rlt_kv_append(const rlt_kv_pool *pool, int32_t bank, const void *k_new,
@@ -312,29 +360,14 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
                                          size_t workspace_bytes, int32_t split_tokens,
                                          void *stream)
 {
-    rlt_status st = check_pool(pool, bank);
-    if (st != RLT_OK)
+    bool empty = false;
+    rlt_status st = rlt::check_decode_args(pool, bank, q, k_new, v_new, num_q_heads, page_table, max_pages,
+                                           seq_lens, batch, max_seq_len, scale, out, split_tokens, &empty);
+    if (st != RLT_OK || empty)
         return st;
-    if (batch < 0 || max_seq_len < 0 || max_pages < 0 || num_q_heads < 1 || split_tokens < 0 ||
-        split_tokens % rlt::kTileTokens != 0 || split_tokens > 128 * rlt::kTileTokens)
-        return RLT_ERR_INVALID_ARG;
-    if (num_q_heads % pool->num_kv_heads != 0)
+    if (workspace != nullptr && !aligned16(workspace))
         return RLT_ERR_INVALID_ARG;
     const int group = num_q_heads / pool->num_kv_heads;
-    if (!rlt::decode_supported(pool->head_dim, group) || pool->page_size % rlt::kTileTokens != 0)
-        return RLT_ERR_UNSUPPORTED;
-    if (batch > 65535 || pool->num_kv_heads > 65535)
-        return RLT_ERR_UNSUPPORTED;
-    if (batch == 0)
-        return RLT_OK;
-    if (q == nullptr || page_table == nullptr || seq_lens == nullptr || out == nullptr ||
-        max_pages < 1)
-        return RLT_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(out) || (workspace != nullptr && !aligned16(workspace)))
-        return RLT_ERR_INVALID_ARG;
-    if (!std::isfinite(scale) || (k_new == nullptr) != (v_new == nullptr) || !aligned16(k_new) ||
-        !aligned16(v_new))
-        return RLT_ERR_INVALID_ARG;
     if (validate_enabled() &&
         (st = validate_attention_batch(page_table, max_pages, seq_lens, batch, pool->num_pages, pool->page_size,
                                        k_new != nullptr, static_cast<cudaStream_t>(stream))) != RLT_OK)

@@ -54,9 +54,13 @@ extern "C" RLT_API rlt_status rlt_paged_decode_attn_noalloc(
     const int32_t *page_table, int32_t max_pages, const int32_t *seq_lens, int32_t batch,
     int32_t max_seq_len, float scale, void *out, float *lse_out, int32_t split_tokens, void *stream)
 {
-    if (batch < 0 || num_q_heads < 1 || max_seq_len < 0 || split_tokens < 0 || pool == nullptr ||
-        pool->num_kv_heads < 1 || pool->head_dim < 1)
-        return RLT_ERR_INVALID_ARG;
+    // the same checks, in the same order, as rlt_paged_decode_attn before the scratch size
+    bool empty = false;
+    const rlt_status arg = rlt::check_decode_args(pool, bank, q, nullptr, nullptr, num_q_heads, page_table,
+                                                  max_pages, seq_lens, batch, max_seq_len, scale, out,
+                                                  split_tokens, &empty);
+    if (arg != RLT_OK || empty)
+        return arg;
     const size_t need = rlt_paged_decode_workspace_size(batch, num_q_heads, pool->num_kv_heads,
                                                         pool->head_dim, max_seq_len, split_tokens);
     if (need > (size_t)RLT_NOALLOC_SCRATCH_BYTES)

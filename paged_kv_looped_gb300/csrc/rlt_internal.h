@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "rlt.h"
+
 namespace rlt {
 
 // Tokens per attention tile: one bulk copy of K and one of V per tile.
@@ -96,6 +98,14 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                        int waves = kPlainWaves);
 
 bool decode_supported(int head_dim, int group);
+
+// The argument checks of rlt_paged_decode_attn that come before its workspace check, in
+// its order (pool and bank, sizes and split, supported shape, pointers and alignment);
+// *empty: a batch of 0 requests, nothing to launch.
+rlt_status check_decode_args(const rlt_kv_pool *pool, int32_t bank, const void *q, const void *k_new,
+                             const void *v_new, int32_t num_q_heads, const int32_t *page_table, int32_t max_pages,
+                             const int32_t *seq_lens, int32_t batch, int32_t max_seq_len, float scale,
+                             const void *out, int32_t split_tokens, bool *empty);
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, cudaStream_t stream);
 cudaError_t launch_combine(const DecodeParams &p, int head_dim, cudaStream_t stream);
 

@@ -58,6 +58,32 @@ def test_bank_map_matches_oracle(lib, rec, planes):
     assert n == no and np.array_equal(m, mo)
 
 
+@pytest.mark.parametrize("rec,planes", [([1] * 24, 4), ([0, 0, 1, 1, 1, 1, 0, 0], 32), ([1, 0, 1], 5)])
+def test_bank_index_matches_oracle_map(lib, rec, planes):
+    """rlt_bank_index, one (layer, plane) lookup through the C ABI, against the oracle's whole map."""
+    mo, _ = oracle.bank_map(np.array(rec, np.uint8), planes)
+    m, _ = rlt.rlt_bank_map(np.array(rec, np.uint8), planes)
+    for layer in range(len(rec)):
+        for plane in range(planes):
+            assert rlt.rlt_bank_index(m, layer, plane) == mo[layer, plane]
+    # prelude / coda layers exist on plane 0 only; lookups outside the map give -1
+    assert rlt.rlt_bank_index(m, -1, 0) == -1 and rlt.rlt_bank_index(m, len(rec), 0) == -1
+    assert rlt.rlt_bank_index(m, 0, planes) == -1 and rlt.rlt_bank_index(m, 0, -1) == -1
+    assert lib.rlt_bank_index(None, len(rec), planes, 0, 0) == -1
+
+
+def test_bank_index_huginn_planes(lib):
+    """Huginn: layers 0-1 and 6-7 (prelude, coda) only on plane 0; 2-5 on all 32 planes."""
+    m, n = rlt.rlt_bank_map(np.array([0, 0, 1, 1, 1, 1, 0, 0], np.uint8), 32)
+    assert n == 132
+    for layer in (0, 1, 6, 7):
+        assert rlt.rlt_bank_index(m, layer, 0) >= 0
+        assert all(rlt.rlt_bank_index(m, layer, t) == -1 for t in range(1, 32))
+    held = sorted(rlt.rlt_bank_index(m, l, t) for l in range(8) for t in range(32)
+                  if rlt.rlt_bank_index(m, l, t) >= 0)
+    assert held == list(range(132))
+
+
 def test_bank_map_rejects_bad_sizes(lib):
     with pytest.raises(rlt.RltError):
         rlt.rlt_bank_map(np.zeros(0, np.uint8), 4)
@@ -121,6 +147,58 @@ def test_device_entry_points_reject_bad_arguments_before_launch(lib):
     assert lib.rlt_paged_gather(ctypes.byref(pool), 0, null, 1, null, 2, 10, null, null, null) == 1
     assert lib.rlt_validate_batch(null, 1, null, 1, null, 10, 0) == 1
     assert lib.rlt_paged_decode_workspace_size(-1, 1, 1, 128, 10, 0) == 0
+
+
+def test_pool_dtype_other_than_bf16_is_refused(lib):
+    null = ctypes.c_void_p(0)
+    fp16 = rlt.rlt_kv_pool(16, 16, 10, 1, 2, 16, 128, 1)
+    assert lib.rlt_kv_append(ctypes.byref(fp16), 0, null, null, null, 1, null) == 3
+    assert lib.rlt_paged_decode_attn(ctypes.byref(fp16), 0, null, null, null, 2, null, 1, null, 1, 64, 0.0, null,
+                                     null, null, 0, 0, null) == 3
+    assert lib.rlt_paged_gather(ctypes.byref(fp16), 0, null, 1, null, 2, 10, null, null, null) == 3
+
+
+def test_noalloc_checks_arguments_before_the_scratch_size(lib):
+    """The no-allocation entry point reports what rlt_paged_decode_attn would for a bad pool, bank,
+    split or pointer, even for a shape whose partials would not fit its scratch array; only a
+    well-formed call too large for the array gets RLT_ERR_WORKSPACE_TOO_SMALL.  Nothing launches:
+    the pointers are aligned stand-ins that no kernel ever sees."""
+    fake = ctypes.c_void_p(4096)
+    pool = rlt.rlt_kv_pool(4096, 8192, 10, 1, 8, 16, 128)
+    big = dict(Hq=64, batch=65535, max_len=1 << 20, split=16)
+    call = lambda p, bank=0, split=16, q=fake, Hq=64: lib.rlt_paged_decode_attn_noalloc(  # noqa: E731
+        ctypes.byref(p), bank, q, Hq, fake, 1 << 16, fake, big["batch"], big["max_len"], 0.0, fake, None, split, None)
+    assert rlt.rlt_paged_decode_workspace_size(big["batch"], 64, 8, 128, big["max_len"], 16) > \
+        rlt.NOALLOC_SCRATCH_BYTES
+    assert call(pool) == 4                                   # well formed, too large: scratch size
+    assert call(pool, bank=1) == 2                           # bank outside the pool
+    assert call(pool, split=24) == 1                         # split not a multiple of 16
+    assert call(pool, Hq=24) == 3                            # group 3: no kernel
+    assert call(pool, Hq=12) == 1                            # Hq not a multiple of Hkv
+    assert call(pool, q=ctypes.c_void_p(0)) == 1             # null q
+    assert call(pool, q=ctypes.c_void_p(4100)) == 1          # misaligned q
+    bad = rlt.rlt_kv_pool(4104, 8192, 10, 1, 8, 16, 128)     # misaligned k
+    assert call(bad) == 1
+    assert lib.rlt_paged_decode_attn_noalloc(None, 0, fake, 64, fake, 1, fake, 1, 16, 0.0, fake, None, 0,
+                                             None) == 1
+
+
+def test_wrappers_check_q_out_and_lse_shapes():
+    """The binding checks what the C ABI cannot (it takes no head_dim for q): a q, out or lse_out
+    of the wrong shape is refused before any pointer is passed on."""
+    import types
+
+    import torch
+    pool = types.SimpleNamespace(head_dim=128)
+    q = torch.zeros((4, 8, 128), dtype=torch.bfloat16)
+    rlt._check_q_out(pool, q, None, None)
+    rlt._check_q_out(pool, q, torch.zeros_like(q), torch.zeros((4, 8)))
+    with pytest.raises(ValueError, match="head_dim"):
+        rlt._check_q_out(pool, torch.zeros((4, 8, 64), dtype=torch.bfloat16), None, None)
+    with pytest.raises(ValueError, match="out"):
+        rlt._check_q_out(pool, q, torch.zeros((4, 8, 64), dtype=torch.bfloat16), None)
+    with pytest.raises(ValueError, match="lse_out"):
+        rlt._check_q_out(pool, q, None, torch.zeros((4, 9)))
 
 
 def test_workspace_size_grows_with_splits(lib):

@@ -218,10 +218,12 @@ def full_size(name, device, rows):
     ("longctx", [0, 5]),
 ])
 def test_full_size_workloads_sampled(cuda_device, name, rows):
-    if rows is None:        # gqa: the longest and shortest requests plus two others
-        L = W.config(name).seq_lens
-        rows = sorted({int(np.argmax(L)), int(np.argmin(L)), 1, 128})
-    full_size(name, cuda_device, np.array(rows))
+    # every sample includes the workload's longest request (the deepest split, the largest
+    # combine fan-in) and its shortest
+    L = W.config(name).seq_lens
+    rows = set(rows) if rows is not None else {1, 128}
+    rows |= {int(np.argmax(L)), int(np.argmin(L))}
+    full_size(name, cuda_device, np.array(sorted(rows)))
 
 
 def test_many_rows_warp_merge(cuda_device):

@@ -198,8 +198,9 @@ def test_full_size_fused_sampled(cuda_device, name, rows):
     del kd, vd, pool
     oracle.kv_append(kh0, vh0, kn, vn, case.new_slots)
     assert np.array_equal(kh, kh0) and np.array_equal(vh, vh0)
-    if rows is None:        # gqa: the longest and shortest requests plus two others
-        rows = sorted({int(np.argmax(case.seq_lens)), int(np.argmin(case.seq_lens)), 1, 128})
-    rows = np.array(rows)
+    # the sample always holds the longest request (deepest split, largest combine fan-in) and the
+    # shortest
+    rows = set(rows) if rows is not None else {1, 128}
+    rows = np.array(sorted(rows | {int(np.argmax(case.seq_lens)), int(np.argmin(case.seq_lens))}))
     ref, ref_lse = oracle.decode_attn_rows(q_bits, kh, vh, case.page_table, case.seq_lens, rows)
     check(out.float().cpu().numpy()[rows], ref, lse.cpu().numpy()[rows], ref_lse)

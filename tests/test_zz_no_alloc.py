@@ -68,7 +68,8 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(cuda_device):
     pool = rlt.KVPool.empty(1, 4, 8, 16, 128, device=cuda_device)
     need = rlt.rlt_paged_decode_workspace_size(65535, 64, 8, 128, 1 << 20, 16)
     assert need > rlt.NOALLOC_SCRATCH_BYTES
-    null = ctypes.c_void_p(0)
-    status = lib.rlt_paged_decode_attn_noalloc(ctypes.byref(pool.struct), 0, null, 64, null, 1, null, 65535,
-                                               1 << 20, 0.0, null, null, 16, null)
+    # aligned stand-ins for q, tables and out: the call is refused before any launch
+    fake = ctypes.c_void_p(4096)
+    status = lib.rlt_paged_decode_attn_noalloc(ctypes.byref(pool.struct), 0, fake, 64, fake, 1 << 16, fake, 65535,
+                                               1 << 20, 0.0, fake, None, 16, None)
     assert status == 4                                   # RLT_ERR_WORKSPACE_TOO_SMALL, nothing launched
