@@ -271,6 +271,9 @@ def run_gpu(args, rank, world):
     new_pos = torch.from_numpy(np.maximum(case.seq_lens.astype(np.int64) - 1, 0)).to(dev)
     req_ids = torch.arange(B, dtype=torch.int32, device=dev)
     written = torch.zeros((nbanks, B), dtype=torch.int32, device=dev)
+    # early start (programmatic dependent launch of each call behind the kernel ahead of it) is
+    # valid when nothing ahead of a call writes its bank: the append fused into the call
+    early = args.early_start == "on" and args.append == "fused"
 
 
     def step(st, events=None):
@@ -295,10 +298,10 @@ def run_gpu(args, rank, world):
         if plan is not None:
             rlt.rlt_paged_decode_attn_prefix(pool, bank, q[i], pt, sl, case.max_seq_len, plan, out=out[i],
                                              workspace=ws, split_tokens=args.split_tokens,
-                                             max_ctas=args.prefix_ctas, stream=st, **fused)
+                                             max_ctas=args.prefix_ctas, stream=st, early_start=early, **fused)
         else:
             rlt.rlt_paged_decode_attn(pool, bank, q[i], pt, sl, case.max_seq_len, out=out[i], workspace=ws,
-                                      split_tokens=args.split_tokens, stream=st, **fused)
+                                      split_tokens=args.split_tokens, stream=st, early_start=early, **fused)
 
     def attention_only(st):
         """Every bank's attention call and nothing else (for the per-call roofline timing)."""
@@ -678,6 +681,7 @@ def config_dict(case, args, gpu=True):
             "cascade": args.cascade, "chunk_tiles": args.chunk_tiles, "tails": args.tails,
             "prefix_ctas": args.prefix_ctas or "one per SM",
             "banks_run": args.banks or "all", "cuda_graph": args.graph, "append": args.append,
+            "early_start": "on" if (args.early_start == "on" and args.append == "fused") else "off",
             "l2": "inputs larger than L2: every bank's KV exceeds the 129 MB L2 and each is read once per step"}
 
 
@@ -724,6 +728,9 @@ def main():
     ap.add_argument("--append", default="fused", choices=["plain", "fused", "rope"],
                     help="store_kv as its own launch at the given slots (plain), fused into the attention "
                          "call (fused), or with RoPE on the keys and written-prefix counters (rope)")
+    ap.add_argument("--early-start", default="on", choices=["on", "off"],
+                    help="launch each attention call as a programmatic dependent of the kernel ahead of it "
+                         "(RLT_ATTN_EARLY_START; only with the append fused into the call)")
     ap.add_argument("--prefix-ctas", type=int, default=0,
                     help="CTAs of the persistent tensor-core kernel (0 = one per SM)")
     ap.add_argument("--banks", type=int, default=0,

@@ -93,6 +93,30 @@ typedef enum rlt_status {
 #define RLT_DEVERR_BAD_LEN 8u         /* a seq_len outside [0, min(max_pages*page_size,
                                          max_seq_len rounded to the split grid)] was clamped */
 
+/*
+ * Flags of the attention calls (rlt_paged_decode_attn, rlt_paged_decode_attn_prefix,
+ * rlt_paged_extend_attn).
+ *
+ * RLT_ATTN_EARLY_START: the call's first kernels are launched as programmatic
+ * dependents of the kernel ahead of them in the stream (Hopper/Blackwell
+ * programmatic dependent launch; under stream capture, programmatic graph edges),
+ * so they may be scheduled while that kernel still runs -- as soon as it lets its
+ * dependents start, which every kernel of this library does at its start.  Before
+ * the work ahead of them has completed they only read the page table, the lengths,
+ * the shared-prefix plan and the cached K/V rows of `bank`, and issue the copies of
+ * those rows; they read q, k_new and v_new, and write out, lse_out, the workspace
+ * and the pool, only after it completed.  So a caller may set the flag when no
+ * kernel still running ahead of the call writes the page table, the lengths, the
+ * plan or that bank of the pool -- as in a decode step whose page tables are
+ * copied in before the step and whose KV append is fused into the attention call
+ * (k_new, v_new), where the kernels ahead (projections, an earlier layer's
+ * attention) write only q, k_new, v_new.  Not with a separate rlt_kv_append into
+ * the same bank right before the call.  Without the flag the first kernels start
+ * after all earlier work in the stream; inside a call the combine always starts
+ * behind the partial kernels this way (it is this library's own kernel).
+ */
+#define RLT_ATTN_EARLY_START 1u
+
 /* Element type of a KV pool.  The pages' engines keep K/V in bf16, and so does
  * every kernel here: any other value is refused with RLT_ERR_UNSUPPORTED. */
 typedef enum rlt_dtype { RLT_BF16 = 0 } rlt_dtype;
@@ -229,6 +253,7 @@ RLT_API size_t rlt_paged_decode_workspace_size(int32_t batch, int32_t num_q_head
  *              share one workspace.
  *   split_tokens tokens per split-K chunk, a multiple of 16 up to 2048;
  *              0 = the library's choice for the current device
+ *   flags      0 or RLT_ATTN_EARLY_START (any other bit: RLT_ERR_INVALID_ARG)
  * A request with seq_lens[b] == 0 gets out = 0 and lse = -inf.  Supported:
  * head_dim 64 or 128; num_q_heads/num_kv_heads in {1, 2, 4, 8}; page_size a
  * multiple of 16 up to 256.  Page-table entries outside [0, num_pages) are
@@ -240,7 +265,7 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
                                  int32_t max_pages, const int32_t *seq_lens, int32_t batch,
                                  int32_t max_seq_len, float scale, void *out, float *lse_out,
                                  void *workspace, size_t workspace_bytes,
-                                 int32_t split_tokens, void *stream);
+                                 int32_t split_tokens, uint32_t flags, void *stream);
 
 /*
  * Shared-prefix plan, HOST function ([FFM] "When scheduler does the work":
@@ -340,7 +365,7 @@ RLT_API size_t rlt_paged_decode_prefix_workspace_size(int32_t batch, int32_t num
  * stores its rows (the split-K kernel for an unshared rest, the tensor-core
  * kernel for a private tail); a newest position inside tiles the request shares,
  * whose slot would be a shared page's, is skipped and sets RLT_DEVERR_BAD_SLOT.
- * Other arguments as
+ * Other arguments (flags included) as
  * rlt_paged_decode_attn; the workspace (rlt_paged_decode_prefix_workspace_size
  * bytes) is required.  num_segments == 0 runs rlt_paged_decode_attn.
  * Supported: head_dim 128, num_q_heads/num_kv_heads in {1, 2, 4, 8}, page_size
@@ -354,7 +379,7 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     const int32_t *member_limit, const int32_t *request_prefix, int32_t num_segments, int32_t work_units,
     int32_t max_prefix_slots, int32_t chunk_tiles, int32_t max_rest_len, float scale, void *out,
     float *lse_out, void *workspace, size_t workspace_bytes, int32_t split_tokens, int32_t max_ctas,
-    void *stream);
+    uint32_t flags, void *stream);
 
 /*
  * Causal extend (span) attention over the paged pool ([FFM] "LOTUS":
@@ -383,7 +408,9 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
  * sizes[0], [6], [3] as num_segments, work_units, max_slots and the
  * chunk_tiles the plan was built with) and a workspace of
  * rlt_paged_extend_workspace_size bytes; page_table is int32 [batch][max_pages]
- * of the requests.  max_ctas as rlt_paged_decode_attn_prefix.  Supported:
+ * of the requests.  max_ctas as rlt_paged_decode_attn_prefix; flags as
+ * rlt_paged_decode_attn (with RLT_ATTN_EARLY_START no kernel still running
+ * ahead may write the plan, the page table or the bank).  Supported:
  * head_dim 128, num_q_heads/num_kv_heads in {1, 2, 4, 8}.
  */
 RLT_API rlt_status rlt_plan_extend(const int32_t *seq_lens, const int32_t *new_lens, int32_t batch,
@@ -400,7 +427,7 @@ RLT_API rlt_status rlt_paged_extend_attn(
     const int32_t *page_table, int32_t max_pages, int32_t batch, const int32_t *segments,
     const int32_t *members, const int32_t *member_limit, const int32_t *row_prefix, const int32_t *row_len,
     int32_t num_segments, int32_t work_units, int32_t max_slots, int32_t chunk_tiles, float scale, void *out,
-    float *lse_out, void *workspace, size_t workspace_bytes, int32_t max_ctas, void *stream);
+    float *lse_out, void *workspace, size_t workspace_bytes, int32_t max_ctas, uint32_t flags, void *stream);
 
 /* Size of the scratch array rlt_paged_decode_attn_noalloc uses (64 MiB). */
 #define RLT_NOALLOC_SCRATCH_BYTES (64u << 20)
@@ -485,6 +512,20 @@ RLT_API rlt_status rlt_paged_gather(const rlt_kv_pool *pool, int32_t bank, const
 RLT_API rlt_status rlt_validate_batch(const int32_t *page_table, int32_t max_pages,
                               const int32_t *seq_lens, int32_t batch, const int64_t *new_slots,
                               int64_t num_pages, int32_t page_size);
+
+/*
+ * Fault injection for tests of the bounded copy waits; the pages have no
+ * counterpart (it exists so that the give-up path can be exercised without a
+ * GPU fault).  Arms the next rlt_paged_decode_attn call made by this host
+ * thread, once: its split-K kernel gives every copy wait wait_limit_ns (1 ns ..
+ * 1 s; the ordinary limit is 1 s) and never issues the first tile copy of warp 0
+ * of the CTA for (split 0, kv head 0, request 0), so that wait runs out.  The
+ * kernel then records RLT_DEVERR_TIMEOUT, waits (bounded by the same limit) for
+ * that warp's copies still in flight, leaves the warp's tiles out of request 0's
+ * result for kv head 0's query heads, and returns: nothing faults or hangs, and
+ * later calls are unaffected.  RLT_ERR_INVALID_ARG for a limit outside that range.
+ */
+RLT_API rlt_status rlt_debug_fault_next_decode(uint64_t wait_limit_ns);
 
 /*
  * Read and clear the device error word (RLT_DEVERR_* bits) of the current

@@ -28,10 +28,10 @@ __all__ = [
     "RltError", "KVPool", "library_path", "load", "rlt_bank_map", "rlt_bank_index", "rlt_kv_append",
     "rlt_paged_decode_workspace_size", "rlt_paged_decode_attn", "rlt_paged_decode_attn_noalloc",
     "rlt_latent_noise_init",
-    "rlt_noise_hash24", "rlt_paged_gather", "rlt_validate_batch", "rlt_get_device_error",
+    "rlt_noise_hash24", "rlt_paged_gather", "rlt_validate_batch", "rlt_get_device_error", "rlt_debug_fault_next_decode",
     "rlt_version", "PrefixPlan", "rlt_plan_prefix", "rlt_choose_chunk_tiles", "rlt_paged_decode_attn_prefix",
     "rlt_paged_decode_prefix_workspace_size", "rlt_kv_append_rope", "rlt_publishable_prefix",
-    "ExtendPlan", "rlt_plan_extend", "rlt_paged_extend_attn", "DEVERR_BAD_PAGE", "DEVERR_BAD_SLOT", "DEVERR_TIMEOUT", "DEVERR_BAD_LEN",
+    "ExtendPlan", "rlt_plan_extend", "rlt_paged_extend_attn", "ATTN_EARLY_START", "DEVERR_BAD_PAGE", "DEVERR_BAD_SLOT", "DEVERR_TIMEOUT", "DEVERR_BAD_LEN",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -40,6 +40,7 @@ _LIB_PATH = os.path.join(_HERE, "librlt.so")
 STATUS = {0: "RLT_OK", 1: "RLT_ERR_INVALID_ARG", 2: "RLT_ERR_OUT_OF_RANGE", 3: "RLT_ERR_UNSUPPORTED",
           4: "RLT_ERR_WORKSPACE_TOO_SMALL", 5: "RLT_ERR_CUDA"}
 DEVERR_BAD_PAGE, DEVERR_BAD_SLOT, DEVERR_TIMEOUT, DEVERR_BAD_LEN = 1, 2, 4, 8
+ATTN_EARLY_START = 1     # RLT_ATTN_EARLY_START: see include/rlt.h
 
 
 class RltError(RuntimeError):
@@ -74,6 +75,7 @@ def load():
                            "(nvcc, sm_103a); this package has no CPU fallback")
     lib = ctypes.CDLL(_LIB_PATH)
     P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    u32 = ctypes.c_uint32
     pool_p = ctypes.POINTER(rlt_kv_pool)
     sigs = {
         "rlt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -83,7 +85,7 @@ def load():
         "rlt_kv_append": (ctypes.c_int, [pool_p, i32, P, P, P, i32, P]),
         "rlt_paged_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
         "rlt_paged_decode_attn": (ctypes.c_int, [pool_p, i32, P, P, P, i32, P, i32, P, i32, i32, f32, P, P, P,
-                                                 sz, i32, P]),
+                                                 sz, i32, u32, P]),
         "rlt_latent_noise_init": (ctypes.c_int, [P, P, P, i64, i32, f32, P]),
         "rlt_noise_hash24": (ctypes.c_int, [P, P, P, i64, i32, P]),
         "rlt_paged_gather": (ctypes.c_int, [pool_p, i32, P, i32, P, i32, i32, P, P, P]),
@@ -94,14 +96,15 @@ def load():
         "rlt_paged_decode_prefix_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, i32]),
         "rlt_choose_chunk_tiles": (i32, [P, i32, P, i32, i32, i32, i32, i32, i32]),
         "rlt_paged_decode_attn_prefix": (ctypes.c_int, [pool_p, i32, P, P, P, i32, P, i32, P, i32, i32, P, P, P, P, i32,
-                                                        i32, i32, i32, i32, f32, P, P, P, sz, i32, i32, P]),
+                                                        i32, i32, i32, i32, f32, P, P, P, sz, i32, i32, u32, P]),
         "rlt_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
+        "rlt_debug_fault_next_decode": (ctypes.c_int, [ctypes.c_uint64]),
         "rlt_kv_append_rope": (ctypes.c_int, [pool_p, i32, P, P, P, P, i32, i32, ctypes.c_double, P, P, i32, P]),
         "rlt_publishable_prefix": (ctypes.c_int, [P, i32, i32, i32, P, P]),
         "rlt_plan_extend": (ctypes.c_int, [P, P, i32, i32, i32, i32, P, i32, P, P, i32, P, P, P]),
         "rlt_paged_extend_workspace_size": (sz, [i32, i32, i32, i32]),
         "rlt_paged_extend_attn": (ctypes.c_int, [pool_p, i32, P, i32, i32, P, i32, i32, P, P, P, P, P, i32, i32,
-                                                 i32, i32, f32, P, P, P, sz, i32, P]),
+                                                 i32, i32, f32, P, P, P, sz, i32, u32, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -203,6 +206,12 @@ def rlt_get_device_error() -> int:
     return int(v.value)
 
 
+def rlt_debug_fault_next_decode(wait_limit_ns: int):
+    """Test hook: the next rlt_paged_decode_attn of this thread runs with this copy-wait limit and
+    one tile copy left unissued, so that a wait runs out (see include/rlt.h)."""
+    _check(load().rlt_debug_fault_next_decode(int(wait_limit_ns)), "rlt_debug_fault_next_decode")
+
+
 # ------------------------------------------------------------- device calls
 
 def rlt_kv_append(pool: KVPool, bank: int, k_new, v_new, out_loc, stream=None):
@@ -277,10 +286,12 @@ def _new_rows(k_new, v_new, B, Hkv, D):
 
 def rlt_paged_decode_attn(pool: KVPool, bank: int, q, page_table, seq_lens, max_seq_len: int,
                           out=None, lse_out=None, workspace=None, scale: float = 0.0,
-                          split_tokens: int = 0, stream=None, k_new=None, v_new=None):
+                          split_tokens: int = 0, stream=None, k_new=None, v_new=None, early_start: bool = False):
     """Paged decode attention of one bank. q bf16 [B][Hq][D]; page_table int32 [B][max_pages];
     seq_lens int32 [B].  With k_new / v_new (bf16 [B][Hkv][D]) each request's new token is
-    stored at position seq_lens[b] - 1 by the same call (fused append).  Returns out."""
+    stored at position seq_lens[b] - 1 by the same call (fused append).  early_start sets
+    RLT_ATTN_EARLY_START (the call may start while the kernel ahead of it runs; see rlt.h for
+    what that kernel must not write).  Returns out."""
     import torch
     _check_q_out(pool, q, out, lse_out)
     B, Hq, D = q.shape
@@ -300,7 +311,7 @@ def rlt_paged_decode_attn(pool: KVPool, bank: int, q, page_table, seq_lens, max_
         _dev(page_table, torch.int32, "page_table"), page_table.shape[1],
         _dev(seq_lens, torch.int32, "seq_lens"), B, int(max_seq_len), float(scale),
         _dev(out, torch.bfloat16, "out"), lse_ptr, ws_ptr, ws_bytes, int(split_tokens),
-        _stream(stream)), "rlt_paged_decode_attn")
+        ATTN_EARLY_START if early_start else 0, _stream(stream)), "rlt_paged_decode_attn")
     return out
 
 
@@ -461,9 +472,10 @@ def rlt_paged_decode_prefix_workspace_size(batch, num_q_heads, num_kv_heads, hea
 
 def rlt_paged_decode_attn_prefix(pool: KVPool, bank: int, q, page_table, seq_lens, max_seq_len: int,
                                  plan: PrefixPlan, out=None, lse_out=None, workspace=None, scale: float = 0.0,
-                                 split_tokens: int = 0, max_ctas: int = 0, stream=None, k_new=None, v_new=None):
+                                 split_tokens: int = 0, max_ctas: int = 0, stream=None, k_new=None, v_new=None,
+                                 early_start: bool = False):
     """Paged decode attention reading shared-prefix tiles once (plan from rlt_plan_prefix, .to(device)).
-    k_new / v_new: the fused append, as in rlt_paged_decode_attn."""
+    k_new / v_new: the fused append, and early_start, as in rlt_paged_decode_attn."""
     import torch
     _check_q_out(pool, q, out, lse_out)
     B, Hq, D = q.shape
@@ -491,8 +503,8 @@ def rlt_paged_decode_attn_prefix(pool: KVPool, bank: int, q, page_table, seq_len
         _dev(lim, torch.int32, "member_limit"), _dev(req, torch.int32, "request_prefix"), plan.num_segments, plan.work_units,
         plan.max_prefix_slots, plan.chunk_tiles, rest, float(scale),
         _dev(out, torch.bfloat16, "out"), lse_ptr, ctypes.c_void_p(workspace.data_ptr()),
-        workspace.numel() * workspace.element_size(), int(split_tokens), int(max_ctas), _stream(stream)),
-        "rlt_paged_decode_attn_prefix")
+        workspace.numel() * workspace.element_size(), int(split_tokens), int(max_ctas),
+        ATTN_EARLY_START if early_start else 0, _stream(stream)), "rlt_paged_decode_attn_prefix")
     return out
 
 
@@ -542,8 +554,10 @@ def rlt_plan_extend(seq_lens, new_lens, page_size: int, chunk_tiles: int = 4, qu
 
 
 def rlt_paged_extend_attn(pool: KVPool, bank: int, q, page_table, plan: ExtendPlan, out=None, lse_out=None,
-                          workspace=None, scale: float = 0.0, max_ctas: int = 0, stream=None):
-    """Causal extend attention: q/out bf16 [new tokens][Hq][D] packed request by request."""
+                          workspace=None, scale: float = 0.0, max_ctas: int = 0, stream=None,
+                          early_start: bool = False):
+    """Causal extend attention: q/out bf16 [new tokens][Hq][D] packed request by request.
+    early_start as in rlt_paged_decode_attn."""
     import torch
     _check_q_out(pool, q, out, lse_out)
     N, Hq, D = q.shape
@@ -567,5 +581,5 @@ def rlt_paged_extend_attn(pool: KVPool, bank: int, q, page_table, plan: ExtendPl
         _dev(rp, torch.int32, "row_prefix"), _dev(rl, torch.int32, "row_len"), plan.num_segments, plan.work_units,
         max(plan.max_slots, 1), plan.chunk_tiles, float(scale), _dev(out, torch.bfloat16, "out"), lse_ptr,
         ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(), int(max_ctas),
-        _stream(stream)), "rlt_paged_extend_attn")
+        ATTN_EARLY_START if early_start else 0, _stream(stream)), "rlt_paged_extend_attn")
     return out

@@ -108,6 +108,10 @@ int64_t bank_elems(const rlt_kv_pool *pool)
 
 rlt_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RLT_OK : RLT_ERR_CUDA; }
 
+// rlt_debug_fault_next_decode: copy-wait limit (ns) for the next rlt_paged_decode_attn call of
+// this host thread, which also leaves one tile copy unissued; 0 = not armed.
+thread_local uint64_t t_fault_wait_ns = 0;
+
 }  // namespace
 
 namespace {
@@ -358,8 +362,10 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
                                          int32_t batch, int32_t max_seq_len, float scale,
                                          void *out, float *lse_out, void *workspace,
                                          size_t workspace_bytes, int32_t split_tokens,
-                                         void *stream)
+                                         uint32_t flags, void *stream)
 {
+    if ((flags & ~RLT_ATTN_EARLY_START) != 0)
+        return RLT_ERR_INVALID_ARG;
     bool empty = false;
     rlt_status st = rlt::check_decode_args(pool, bank, q, k_new, v_new, num_q_heads, page_table, max_pages,
                                            seq_lens, batch, max_seq_len, scale, out, split_tokens, &empty);
@@ -409,7 +415,13 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
     p.part_stride = plan.max_splits;
     const double s = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)pool->head_dim);
     p.qscale = (float)(s * 1.4426950408889634);   // log2(e): softmax in base 2
-    return from_cuda(rlt::launch_decode(p, pool->head_dim, group, static_cast<cudaStream_t>(stream)));
+    if (t_fault_wait_ns != 0) {                   // armed by rlt_debug_fault_next_decode
+        p.wait_limit_ns = t_fault_wait_ns;
+        p.debug_drop_copy = 1;
+        t_fault_wait_ns = 0;
+    }
+    return from_cuda(rlt::launch_decode(p, pool->head_dim, group, static_cast<cudaStream_t>(stream),
+                                        (flags & RLT_ATTN_EARLY_START) != 0));
 }
 
 // Per-CTA costs of the tensor-core kernel measured on GB300 with every SM streaming: one
@@ -536,14 +548,14 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     const int32_t *member_limit, const int32_t *request_prefix, int32_t num_segments, int32_t work_units,
     int32_t max_prefix_slots, int32_t chunk_tiles, int32_t max_rest_len, float scale, void *out,
     float *lse_out, void *workspace, size_t workspace_bytes, int32_t split_tokens, int32_t max_ctas,
-    void *stream)
+    uint32_t flags, void *stream)
 {
-    if (max_ctas < 0)
+    if (max_ctas < 0 || (flags & ~RLT_ATTN_EARLY_START) != 0)
         return RLT_ERR_INVALID_ARG;
     if (num_segments == 0)      // nothing shared: the plain kernel computes the same thing
         return rlt_paged_decode_attn(pool, bank, q, k_new, v_new, num_q_heads, page_table, max_pages, seq_lens,
                                      batch, max_seq_len, scale, out, lse_out, workspace,
-                                     workspace_bytes, split_tokens, stream);
+                                     workspace_bytes, split_tokens, flags, stream);
     rlt_status st = check_pool(pool, bank);
     if (st != RLT_OK)
         return st;
@@ -638,6 +650,10 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
+    // Early start: both partial kernels are programmatic dependents of what precedes the call
+    // (under stream capture the fork and the join become programmatic graph edges), and the
+    // combine of what they leave.
+    const bool early = (flags & RLT_ATTN_EARLY_START) != 0;
     // Fused append: the kernel whose copy covers a request's newest token stores the new
     // rows on the way -- the split-K kernel for an unshared rest, the tensor-core kernel
     // for a private tail -- and flags a newest token inside shared tiles.
@@ -655,15 +671,15 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
         if (e == cudaSuccess)
             e = cudaStreamWaitEvent(side->stream, side->fork, 0);
         if (e == cudaSuccess)
-            e = rlt::launch_prefix(p, pp, p.k_bank, p.v_bank, bank_rows, cs);
+            e = rlt::launch_prefix(p, pp, p.k_bank, p.v_bank, bank_rows, cs, early);
         if (e == cudaSuccess)
-            e = rlt::launch_decode(p_rest, pool->head_dim, group, side->stream);
+            e = rlt::launch_decode(p_rest, pool->head_dim, group, side->stream, early);
         if (e == cudaSuccess)
             e = cudaEventRecord(side->join, side->stream);
         if (e == cudaSuccess)
             e = cudaStreamWaitEvent(cs, side->join, 0);
     } else {
-        e = rlt::launch_prefix(p, pp, p.k_bank, p.v_bank, bank_rows, cs);
+        e = rlt::launch_prefix(p, pp, p.k_bank, p.v_bank, bank_rows, cs, early);
     }
     if (e == cudaSuccess)
         e = rlt::launch_combine(p, pool->head_dim, cs);
@@ -684,14 +700,14 @@ RLT_API rlt_status rlt_paged_extend_attn(
     const int32_t *page_table, int32_t max_pages, int32_t batch, const int32_t *segments,
     const int32_t *members, const int32_t *member_limit, const int32_t *row_prefix, const int32_t *row_len,
     int32_t num_segments, int32_t work_units, int32_t max_slots, int32_t chunk_tiles, float scale, void *out,
-    float *lse_out, void *workspace, size_t workspace_bytes, int32_t max_ctas, void *stream)
+    float *lse_out, void *workspace, size_t workspace_bytes, int32_t max_ctas, uint32_t flags, void *stream)
 {
     rlt_status st = check_pool(pool, bank);
     if (st != RLT_OK)
         return st;
     if (num_rows < 0 || batch < 0 || max_pages < 1 || num_q_heads < 1 || num_segments < 0 || work_units < 0 ||
         max_slots < 0 || chunk_tiles < 1 || max_ctas < 0 || num_q_heads % pool->num_kv_heads != 0 ||
-        !std::isfinite(scale))
+        !std::isfinite(scale) || (flags & ~RLT_ATTN_EARLY_START) != 0)
         return RLT_ERR_INVALID_ARG;
     if (num_rows == 0 || num_segments == 0)
         return RLT_OK;
@@ -749,7 +765,8 @@ RLT_API rlt_status rlt_paged_extend_attn(
     pp.ctas = (int32_t)std::min<int64_t>(max_ctas > 0 ? std::min(max_ctas, sms) : sms,
                                          (int64_t)pool->num_kv_heads * work_units);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    cudaError_t e = rlt::launch_prefix(p, pp, p.k_bank, p.v_bank, bank_rows, cs);
+    cudaError_t e = rlt::launch_prefix(p, pp, p.k_bank, p.v_bank, bank_rows, cs,
+                                       (flags & RLT_ATTN_EARLY_START) != 0);
     if (e == cudaSuccess) {
         // the merge runs over the new tokens: each row's "request" is its causal prefix
         rlt::DecodeParams pc = p;
@@ -875,6 +892,14 @@ RLT_API rlt_status rlt_validate_batch(const int32_t *page_table, int32_t max_pag
                 return RLT_ERR_INVALID_ARG;        // append into a shared (read-only) page
         }
     }
+    return RLT_OK;
+}
+
+RLT_API rlt_status rlt_debug_fault_next_decode(uint64_t wait_limit_ns)
+{
+    if (wait_limit_ns == 0 || wait_limit_ns > rlt::kMaxFaultWaitNs)
+        return RLT_ERR_INVALID_ARG;
+    t_fault_wait_ns = wait_limit_ns;
     return RLT_OK;
 }
 

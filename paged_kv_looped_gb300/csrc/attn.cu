@@ -368,6 +368,8 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
     constexpr int DPL = C::kDpl;
     extern __shared__ __align__(128) unsigned char smem[];
 
+    // The kernel behind this one (the combine, or the next call) may be scheduled now.
+    pdl_launch_dependents();
     const int split = blockIdx.x;
     const int g = blockIdx.y;
     const int b = blockIdx.z;
@@ -387,8 +389,12 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
     if (p.k_new != nullptr && L > 0 && L - 1 < tok0 && split == 0 && g == 0 && threadIdx.x == 0)
         record_error(p.err, RLT_DEVERR_BAD_SLOT);
 
+    // Until pdl_wait this CTA reads only what no kernel still running may write: the
+    // lengths, page table, prefix plan and cached K/V rows of the bank.  q, k_new and
+    // v_new are read, and out, the partials and the pool written, only after it.
     if (n_splits == 0 && n_pre == 0) {          // empty request: out = 0, lse = -inf
         if (split == 0) {
+            pdl_wait();
             for (int i = threadIdx.x; i < G * D / 2; i += kThreads) {
                 const int h = i / (D / 2), d2 = i % (D / 2);
                 reinterpret_cast<uint32_t *>(
@@ -399,8 +405,11 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
         }
         return;
     }
-    if (split >= n_splits)
+    if (split >= n_splits) {
+        if (split == 0)
+            pdl_wait();                         // every grid waits in at least one CTA
         return;
+    }
 
     const int tile_begin = split * p.tiles_per_split;
     const int tile_end = min(tile_begin + p.tiles_per_split, n_tiles);
@@ -451,7 +460,9 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
             unsigned char *dst = pipe + (i % kStages) * C::kStageBytes;
             const int64_t row = ((int64_t)page * p.num_kv_heads + g) * p.page_size + off;
             mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
-            if (i != i_new) {
+            if (p.debug_drop_copy != 0 && i == 0 && warp == 0 && split == 0 && g == 0 && b == 0) {
+                // fault injection (timeout test only): this stage's bytes never arrive
+            } else if (i != i_new) {
                 bulk_load(dst, p.k_bank + row * D, C::kTileBytes, bar);
                 bulk_load(dst + C::kTileBytes, p.v_bank + row * D, C::kTileBytes, bar);
             } else {
@@ -470,6 +481,18 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
             }
         }
     };
+
+    // The first ring stages go out before the wait for the kernels ahead (their K/V rows
+    // are already in the pool); the tile that takes the fused append's new row from
+    // k_new / v_new goes out after it.
+    const int n_prologue = my_count < kStages ? my_count : kStages;
+    const int n_early = (i_new >= 0 && i_new < n_prologue) ? i_new : n_prologue;
+    int issued = 0;
+    for (; issued < n_early; ++issued)
+        issue(issued);
+    pdl_wait();
+    for (; issued < n_prologue; ++issued)
+        issue(issued);
 
     // Query heads g*G .. g*G+G-1, this lane's dims, pre-scaled into log2 units, as fp32
     // pairs; the accumulators are fp32 pairs too.
@@ -494,18 +517,15 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
             acc2[h][d] = f2_pack(0.f, 0.f);
     }
 
-    const int n_prologue = my_count < kStages ? my_count : kStages;
-    for (int i = 0; i < n_prologue; ++i)
-        issue(i);
-    int issued = n_prologue;
     uint32_t phase = 0;                        // bit s: parity of stage s's next phase
+    const uint64_t wait_ns = p.wait_limit_ns != 0 ? p.wait_limit_ns : kWaitLimitNs;
     int failed_at = -1;
 
     for (int i = 0; i < my_count; ++i) {
         const int s = i % kStages;
         const int page = __shfl_sync(kFullMask, my_page, i);
         if (page >= 0) {
-            const bool arrived = __all_sync(kFullMask, mbar_wait(&bars[s], (phase >> s) & 1u));
+            const bool arrived = __all_sync(kFullMask, mbar_wait(&bars[s], (phase >> s) & 1u, wait_ns));
             if (!arrived) {
                 failed_at = i;
                 break;
@@ -610,7 +630,7 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
         for (int k = failed_at; k < issued; ++k) {
             const int s = k % kStages;
             if (__shfl_sync(kFullMask, my_page, k) >= 0) {
-                mbar_wait(&bars[s], (phase >> s) & 1u);
+                mbar_wait(&bars[s], (phase >> s) & 1u, wait_ns);
                 phase ^= 1u << s;
             }
         }
@@ -702,6 +722,8 @@ template <int D>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeParams p)
 {
     __shared__ MergeSmem<D> sm;
+    pdl_launch_dependents();
+    pdl_wait();                                  // the partial kernels of this call are done
     const int64_t bh = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = (int)(bh / p.num_q_heads);
@@ -730,6 +752,8 @@ template <int D, int kLoads>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_warp_kernel(const DecodeParams p)
 {
     constexpr int DPL = D / 32;
+    pdl_launch_dependents();
+    pdl_wait();                                  // the partial kernels of this call are done
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t bh = (int64_t)blockIdx.x * kCombineWarps + warp;
     if (bh >= (int64_t)p.batch * p.num_q_heads)
@@ -825,19 +849,21 @@ cudaError_t launch_combine_typed(const DecodeParams &p, cudaStream_t stream)
     // A warp per row when the slots fit; with few rows each warp keeps more of its row's
     // partial reads in flight (measured: huginn's 512 rows 33.8 -> 32.3 us per call with 16,
     // ouro's 1024 rows 181.2 -> 180.4; gqa's 8192 rows 514 with 8, 515 with 16).
+    // Launched as a programmatic dependent of the call's partial kernels: it is resident
+    // while they finish and waits for them in pdl_wait.
     if ((int64_t)p.prefix_slots + p.max_splits <= 32) {
         if (pairs >= 4096)
-            decode_combine_warp_kernel<D, 8><<<grid, kCombineThreads, 0, stream>>>(p);
-        else
-            decode_combine_warp_kernel<D, 16><<<grid, kCombineThreads, 0, stream>>>(p);
-    } else {
-        decode_combine_kernel<D><<<(unsigned)pairs, kCombineThreads, 0, stream>>>(p);
+            return launch_kernel(decode_combine_warp_kernel<D, 8>, dim3(grid), dim3(kCombineThreads), 0, stream,
+                                 true, p);
+        return launch_kernel(decode_combine_warp_kernel<D, 16>, dim3(grid), dim3(kCombineThreads), 0, stream, true,
+                             p);
     }
-    return cudaGetLastError();
+    return launch_kernel(decode_combine_kernel<D>, dim3((unsigned)pairs), dim3(kCombineThreads), 0, stream, true,
+                         p);
 }
 
 template <int D, int G>
-cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream)
+cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream, bool early)
 {
     using C = Cfg<D, G>;
     static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -856,8 +882,7 @@ cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream)
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     const dim3 grid(p.max_splits, p.num_kv_heads, p.batch);
-    kernel<<<grid, kThreads, C::kSmemBytes, stream>>>(p);
-    e = cudaGetLastError();
+    e = launch_kernel(kernel, grid, dim3(kThreads), C::kSmemBytes, stream, early, p);
     // plain decode merges here; shared-prefix mode merges after the prefix kernel
     if (e != cudaSuccess || p.max_splits <= 1 || p.request_prefix != nullptr)
         return e;
@@ -916,21 +941,21 @@ cudaError_t launch_combine(const DecodeParams &p, int head_dim, cudaStream_t str
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, cudaStream_t stream)
+cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, cudaStream_t stream, bool early)
 {
     if (head_dim == 128) {
         switch (group) {
-        case 1: return launch_typed<128, 1>(p, stream);
-        case 2: return launch_typed<128, 2>(p, stream);
-        case 4: return launch_typed<128, 4>(p, stream);
-        case 8: return launch_typed<128, 8>(p, stream);
+        case 1: return launch_typed<128, 1>(p, stream, early);
+        case 2: return launch_typed<128, 2>(p, stream, early);
+        case 4: return launch_typed<128, 4>(p, stream, early);
+        case 8: return launch_typed<128, 8>(p, stream, early);
         }
     } else if (head_dim == 64) {
         switch (group) {
-        case 1: return launch_typed<64, 1>(p, stream);
-        case 2: return launch_typed<64, 2>(p, stream);
-        case 4: return launch_typed<64, 4>(p, stream);
-        case 8: return launch_typed<64, 8>(p, stream);
+        case 1: return launch_typed<64, 1>(p, stream, early);
+        case 2: return launch_typed<64, 2>(p, stream, early);
+        case 4: return launch_typed<64, 4>(p, stream, early);
+        case 8: return launch_typed<64, 8>(p, stream, early);
         }
     }
     return cudaErrorInvalidValue;

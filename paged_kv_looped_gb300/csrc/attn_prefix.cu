@@ -267,6 +267,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + kFlagOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + kFlagOff + 4);
 
+    // The kernel behind this one (the combine) may be scheduled now.  Until pdl_wait a thread
+    // reads only what no kernel still running may write: the plan, lengths, page table and
+    // cached K/V rows.  q and k_new / v_new are read, and partials and pool rows written, only
+    // by threads that have passed it.
+    pdl_launch_dependents();
     const int G = p.num_q_heads / p.num_kv_heads;
     const int64_t n_items = (int64_t)p.num_kv_heads * pp.work_units;
     const int item_begin = (int)((int64_t)blockIdx.x * n_items / gridDim.x);
@@ -420,6 +425,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const int64_t pidx = nt / p.page_size;
                 const int64_t pg = pidx < p.max_pages ? p.page_table[(int64_t)nt_b * p.max_pages + pidx] : -1;
                 const bool page_valid = pg >= 0 && pg < p.num_pages;   // a bad page is flagged, not written
+                pdl_wait();
                 const uint4 *src = reinterpret_cast<const uint4 *>((is_v ? p.v_new : p.k_new) +
                                                                    ((int64_t)nt_b * p.num_kv_heads + nt_g) * 128 +
                                                                    (lane & 1) * 64);
@@ -628,6 +634,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
         uint32_t qw[32];
         ok = take_desc(bars, base, 0, rd, row, G, b_row, lim_row, abort_flag, lane);
+        pdl_wait();                              // q, and the partials this warp writes
         if (ok && rd.nsub > 0) {
             load_q(p, rd, G, row, b_row, half, qw);
             store_q(qw, half, t_lane + kColQ, &bars[kBarQFull], lane);
@@ -790,6 +797,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         record_error(p.err, RLT_DEVERR_TIMEOUT);
     if (warp == 0)
         tc::tmem_dealloc(tmem, kTmemCols);
+    if (tid == 0)
+        pdl_wait();                              // no CTA ends before the grids it depends on
 }
 
 // ---------------------------------------------------------- tensor maps
@@ -840,7 +849,7 @@ bool prefix_supported(int head_dim, int group, int page_size)
 size_t prefix_smem_bytes(int, int) { return kSmemP; }
 
 cudaError_t launch_prefix(const DecodeParams &p, const PrefixParams &pp, const void *k_bank,
-                          const void *v_bank, int64_t bank_rows, cudaStream_t stream)
+                          const void *v_bank, int64_t bank_rows, cudaStream_t stream, bool early)
 {
     if (pp.num_segments == 0 || pp.work_units == 0)
         return cudaSuccess;
@@ -866,8 +875,7 @@ cudaError_t launch_prefix(const DecodeParams &p, const PrefixParams &pp, const v
     }
     if (pp.ctas < 1)
         return cudaErrorInvalidValue;
-    kernel<<<pp.ctas, kPThreads, kSmemP, stream>>>(kmap, vmap, p, pp);
-    return cudaGetLastError();
+    return launch_kernel(kernel, dim3(pp.ctas), dim3(kPThreads), kSmemP, stream, early, kmap, vmap, p, pp);
 }
 
 }  // namespace rlt

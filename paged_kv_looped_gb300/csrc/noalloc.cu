@@ -73,6 +73,6 @@ extern "C" RLT_API rlt_status rlt_paged_decode_attn_noalloc(
     }
     return rlt_paged_decode_attn(pool, bank, q, nullptr, nullptr, num_q_heads, page_table, max_pages, seq_lens, batch,
                                  max_seq_len, scale, out, lse_out, scratch,
-                                 need > 0 ? (size_t)RLT_NOALLOC_SCRATCH_BYTES : 0, split_tokens,
+                                 need > 0 ? (size_t)RLT_NOALLOC_SCRATCH_BYTES : 0, split_tokens, 0u,
                                  stream);
 }

@@ -119,16 +119,17 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
     return done != 0;
 }
 
-// Wait for the phase with the given parity to complete; false after the time limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+// Wait for the phase with the given parity to complete; false after the time limit
+// (limit_ns of %globaltimer, and at most 2^32 - 1 tries).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = global_ns();
-    for (uint32_t it = 1; it != 0; ++it) {       // at most 2^32 - 1 tries
+    for (uint32_t it = 1; it != 0; ++it) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if ((it & 255u) == 0u && global_ns() - t0 > kWaitLimitNs)
+        if ((it & 255u) == 0u && global_ns() - t0 > limit_ns)
             return false;
     }
     return false;
@@ -172,6 +173,23 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
             "r"(smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// ------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start before the
+// kernel ahead of it in the stream has finished.  launch_dependents lets the
+// kernel behind this one start (once every CTA has issued it or exited);
+// pdl_wait blocks the calling thread until every grid this one depends on has
+// completed and its memory writes are visible.  Without such a launch both are
+// no-ops.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------------- warp helpers

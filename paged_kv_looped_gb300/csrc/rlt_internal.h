@@ -13,6 +13,9 @@ namespace rlt {
 // Tokens per attention tile: one bulk copy of K and one of V per tile.
 constexpr int kTileTokens = 16;
 
+// Longest copy-wait limit the timeout test may ask for (rlt_debug_fault_next_decode).
+constexpr uint64_t kMaxFaultWaitNs = 1000000000ull;
+
 struct DecodeParams {
     const uint16_t *k_bank;      // bank base of the K pool: [num_pages][Hkv][ps][D]
     const uint16_t *v_bank;
@@ -42,6 +45,12 @@ struct DecodeParams {
     // and uses them in place of what it read from there.
     const uint16_t *k_new;
     const uint16_t *v_new;
+    // Copy-wait limit of the split-K kernel in ns (0: the default, one second), and the
+    // fault-injection switch of the timeout test (rlt_debug_fault_next_decode): non-zero
+    // leaves the first tile copy of CTA (0, 0, 0)'s warp 0 unissued, so that its wait
+    // runs out.  Zero in every ordinary call.
+    uint64_t wait_limit_ns;
+    int32_t debug_drop_copy;
 };
 
 // Tokens per tensor-core tile of the shared-prefix kernel.
@@ -73,10 +82,30 @@ struct PrefixParams {
     int32_t ctas;                // persistent CTAs sharing the num_kv_heads x work_units items
 };
 
+// Launch a kernel on `stream`; with `early`, as a programmatic dependent of the kernel
+// ahead of it in the stream (it may start before that kernel ends and must call
+// pdl_wait before touching what that kernel or any earlier one writes).
+template <typename... Exp, typename... Act>
+cudaError_t launch_kernel(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          bool early, Act &&...args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = early ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Act &&>(args)...);
+}
+
 bool prefix_supported(int head_dim, int group, int page_size);
 size_t prefix_smem_bytes(int chunk_tiles, int page_size);
 cudaError_t launch_prefix(const DecodeParams &p, const PrefixParams &pp, const void *k_bank,
-                          const void *v_bank, int64_t bank_rows, cudaStream_t stream);
+                          const void *v_bank, int64_t bank_rows, cudaStream_t stream, bool early);
 
 // Split-K plan for one decode call.
 struct DecodePlan {
@@ -106,7 +135,10 @@ rlt_status check_decode_args(const rlt_kv_pool *pool, int32_t bank, const void *
                              const void *v_new, int32_t num_q_heads, const int32_t *page_table, int32_t max_pages,
                              const int32_t *seq_lens, int32_t batch, int32_t max_seq_len, float scale,
                              const void *out, int32_t split_tokens, bool *empty);
-cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, cudaStream_t stream);
+// early: start as a programmatic dependent of the kernel ahead in the stream (the call's
+// RLT_ATTN_EARLY_START).  The combine always starts that way behind the call's own
+// partial kernels.
+cudaError_t launch_decode(const DecodeParams &p, int head_dim, int group, cudaStream_t stream, bool early);
 cudaError_t launch_combine(const DecodeParams &p, int head_dim, cudaStream_t stream);
 
 cudaError_t launch_append(uint16_t *k_bank, uint16_t *v_bank, const uint16_t *k_new,

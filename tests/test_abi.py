@@ -132,7 +132,7 @@ def test_device_entry_points_reject_bad_arguments_before_launch(lib):
     bad = rlt.rlt_kv_pool(8, 16, 10, 1, 2, 16, 128)                                     # misaligned k
     assert lib.rlt_kv_append(ctypes.byref(bad), 0, null, null, null, 1, null) == 1
     attn = lambda p, hq, split=0, ws=0: lib.rlt_paged_decode_attn(                       # noqa: E731
-        ctypes.byref(p), 0, null, null, null, hq, null, 1, null, 1, 64, 0.0, null, null, null, ws, split, null)
+        ctypes.byref(p), 0, null, null, null, hq, null, 1, null, 1, 64, 0.0, null, null, null, ws, split, 0, null)
     assert attn(pool, 3) == 1                                # Hq not a multiple of Hkv
     assert attn(pool, 6) == 3                                # group 3: no kernel
     assert attn(pool, 2, split=24) == 1                      # split not a multiple of 16
@@ -141,6 +141,14 @@ def test_device_entry_points_reject_bad_arguments_before_launch(lib):
     d96 = rlt.rlt_kv_pool(16, 16, 10, 1, 2, 16, 96)
     assert attn(d96, 2) == 3
     assert attn(pool, 2) == 1                                # null q / tables / out
+    # an unknown flag bit is refused before anything else
+    assert lib.rlt_paged_decode_attn(ctypes.byref(pool), 0, null, null, null, 2, null, 1, null, 1, 64, 0.0, null,
+                                     null, null, 0, 0, 2, null) == 1
+    assert lib.rlt_paged_decode_attn_prefix(ctypes.byref(pool), 0, null, null, null, 2, null, 1, null, 1, 64, null,
+                                            null, null, null, 0, 0, 0, 1, 0, 0.0, null, null, null, 0, 0, 0, 4,
+                                            null) == 1
+    assert lib.rlt_paged_extend_attn(ctypes.byref(pool), 0, null, 2, 1, null, 1, 1, null, null, null, null, null,
+                                     1, 1, 1, 1, 0.0, null, null, null, 0, 0, 8, null) == 1
     assert lib.rlt_latent_noise_init(null, null, null, 5, 0, ctypes.c_float(0.02), null) == 1
     assert lib.rlt_latent_noise_init(null, null, null, 0, 8, ctypes.c_float(0.02), null) == 0
     assert lib.rlt_noise_hash24(null, null, null, -1, 8, null) == 1
@@ -149,12 +157,18 @@ def test_device_entry_points_reject_bad_arguments_before_launch(lib):
     assert lib.rlt_paged_decode_workspace_size(-1, 1, 1, 128, 10, 0) == 0
 
 
+def test_fault_switch_rejects_limits_outside_its_range(lib):
+    # only refusals here: a valid limit would arm the next decode call of this thread
+    assert lib.rlt_debug_fault_next_decode(ctypes.c_uint64(0)) == 1
+    assert lib.rlt_debug_fault_next_decode(ctypes.c_uint64(2_000_000_000)) == 1
+
+
 def test_pool_dtype_other_than_bf16_is_refused(lib):
     null = ctypes.c_void_p(0)
     fp16 = rlt.rlt_kv_pool(16, 16, 10, 1, 2, 16, 128, 1)
     assert lib.rlt_kv_append(ctypes.byref(fp16), 0, null, null, null, 1, null) == 3
     assert lib.rlt_paged_decode_attn(ctypes.byref(fp16), 0, null, null, null, 2, null, 1, null, 1, 64, 0.0, null,
-                                     null, null, 0, 0, null) == 3
+                                     null, null, 0, 0, 0, null) == 3
     assert lib.rlt_paged_gather(ctypes.byref(fp16), 0, null, 1, null, 2, 10, null, null, null) == 3
 
 

@@ -67,6 +67,14 @@ def test_traffic_summary_is_dropped_when_a_kernel_source_changes(tmp_path, monke
         shutil.copy(os.path.join(bench.ROOT, "paged_kv_looped_gb300", "csrc", f),
                     tmp_path / "paged_kv_looped_gb300" / "csrc" / f)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    # the copy's summary names the copied sources' hash (as a fresh capture would), whether or not
+    # the committed summary is current
+    import hashlib
+    blob = b"".join(open(tmp_path / "paged_kv_looped_gb300" / "csrc" / f, "rb").read() for f in sources)
+    digest = hashlib.sha256(blob).hexdigest()[:16]
+    with open(tmp_path / "profiles" / "traffic_ouro.txt", "w") as fh:
+        fh.write("\n".join(f"sources_sha256_16: {digest}" if l.startswith("sources_sha256_16:") else l
+                           for l in text.splitlines()) + "\n")
     fused = fields.get("append", "plain").strip() == "fused"
     assert bench.profiled_traffic("ouro", fused) == float(fields["dram_bytes_per_call"])
     assert bench.profiled_traffic("ouro", not fused) is None        # taken with the other append form
