@@ -71,6 +71,32 @@ def layer_planes(case: W.PagedCase):
     return [(l, t) for t in range(case.num_planes) for l in range(case.num_layers) if t == 0 or rec[l]]
 
 
+def extend_roofline(case: W.PagedCase, new_lens, ms: float) -> dict:
+    """Roofline of one causal extend call: its bound is the one its arithmetic intensity selects.
+
+    flops: QK^T and PV over each new token's causal keys (4 * D * Hq per (token, key) pair);
+    bytes: the K/V rows read once per kv head (unique pages, as decode counts them), the new
+    tokens' q and out rows, the page-table entries.  Below the ridge (measured bf16 peak / measured
+    HBM peak, ~284 flop/B) the call is HBM-bound, above it tensor-bound."""
+    D, Hq = case.head_dim, case.num_q_heads
+    keys = sum(int(L) - int(n) + i + 1 for L, n in zip(case.seq_lens, new_lens) for i in range(int(n)))
+    flops = 4.0 * D * Hq * keys
+    rows = int(np.sum(new_lens))
+    nbytes = attn_bytes(case) - case.batch * Hq * D * 4 + rows * Hq * D * 4
+    hbm, _ = hbm_peak()
+    ridge = bf16_peak() * 1e12 / (hbm * 1e9)
+    t = ms * 1e-3
+    intensity = flops / nbytes
+    tensor = intensity >= ridge
+    achieved = flops / t / 1e12 if tensor else nbytes / t / 1e9
+    peak = bf16_peak() if tensor else hbm
+    return {"new_tokens_per_request": int(np.max(new_lens)) if len(new_lens) else 0,
+            "us_per_call": round(ms * 1e3, 2), "flop_per_byte": round(intensity, 1), "ridge_flop_per_byte": round(ridge, 1),
+            "bound": "tensor" if tensor else "hbm", "achieved": round(achieved, 1),
+            "unit": "TFLOP/s" if tensor else "GB/s", "peak": peak, "frac": round(achieved / peak, 4),
+            "tflops": round(flops / t / 1e12, 1), "gbs": round(nbytes / t / 1e9, 1)}
+
+
 # --------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -421,12 +447,29 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize(dev)
         assert rlt.rlt_get_device_error() == 0
         ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-        keys = sum(int(L) - int(n) + i + 1 for L, n in zip(case.seq_lens, new) for i in range(int(n)))
-        flops = 4.0 * D * Hq * keys                       # QK^T and PV, 2 flops per multiply-add
-        extend = {"new_tokens_per_request": args.extend, "us_per_call": round(ms * 1e3, 2),
-                  "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
-                  "frac_of_bf16_peak": round(flops / (ms * 1e-3) / 1e12 / bf16_peak(), 4),
-                  "kv_gbs": round(attn_bytes(case) / (ms * 1e-3) / 1e9, 1)}
+        extend = extend_roofline(case, new, ms)
+
+    # ---- the latent-noise kernel alone: a graph of back-to-back launches, events around it
+    noise_ms = None
+    if nz is not None:
+        reps = 20
+        for _ in range(3):
+            rlt.rlt_latent_noise_init(seeds, pos, nz.channels, nz.initializer_range, out=noise, stream=stream)
+        def noise_reps(st):
+            for _ in range(reps):
+                rlt.rlt_latent_noise_init(seeds, pos, nz.channels, nz.initializer_range, out=noise, stream=st)
+        if args.graph == "on":
+            ng = capture(fn=noise_reps)
+            ng.replay()
+        n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0.record(stream)
+        if args.graph == "on":
+            ng.replay()
+        else:
+            noise_reps(stream)
+        n1.record(stream)
+        torch.cuda.synchronize(dev)
+        noise_ms = n0.elapsed_time(n1) / reps
 
     # ---- end to end: this step's inputs from pinned host memory, outputs back to the host
     def ship_plan(host_bufs, dev_arrays, st):
@@ -561,7 +604,7 @@ def run_gpu(args, rank, world):
     combine = ws_bytes > 0
     launches = args.steps * (len(banks) * per_lp + (1 if nz is not None else 0))
     return dict(case=case, banks=banks, cascade=plan is not None, graph=graph is not None, attn_timing=attn_timing,
-                extend=extend,
+                extend=extend, noise_ms=noise_ms,
                 ms_total=ms_total, attn_ms=attn_ms, attn_call_ms=attn_call_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                 e2e_serial_ms=e2e_serial_ms, e2e_mode=e2e_mode, e2e_pipelined_ms=pipelined_ms,
                 clocks=clocks.summary(), launches=launches, combine=combine, ws_bytes=ws_bytes)
@@ -737,6 +780,9 @@ def main():
                     help="run only the first N layer-plane banks (small-footprint case for profilers); 0 = all")
     ap.add_argument("--batch", type=int, default=0,
                     help="run only the first N requests of the workload (small case for profilers); 0 = all")
+    ap.add_argument("--also", default="auto",
+                    help="other workloads timed after the headline one (comma list; auto = every other "
+                         "workload unless --batch/--banks slice the run; none = skip)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU time for cpu_baseline")
     ap.add_argument("--cpu-procs", type=int, default=os.cpu_count() or 1,
                     help="also time the oracle as this many processes at once (cpu_baseline.all_cores; <= 1: skip)")
@@ -756,24 +802,7 @@ def main():
         dist.init_process_group(backend="nccl")
     r = run_gpu(args, rank, world)
     case = r["case"]
-    nlp = len(r["banks"])
-    step_bytes = attn_bytes(case) * nlp + append_bytes(case) * nlp + noise_bytes(case)
-    pipe_total = r["e2e_pipelined_ms"] if r["e2e_pipelined_ms"] is not None else r["e2e_serial_ms"]
-    ms_max, e2e_ms_step, e2e_serial_step, e2e_pipe_step = max_over_ranks(
-        [r["ms_total"] / args.steps, r["e2e_ms"] / args.steps, r["e2e_serial_ms"] / args.steps,
-         pipe_total / args.steps])
-    value = job_gbs(step_bytes, world, ms_max)
-    e2e_value = job_gbs(step_bytes, world, e2e_ms_step)
-    e2e_serial = job_gbs(step_bytes, world, e2e_serial_step)
-    e2e_pipe = job_gbs(step_bytes, world, e2e_pipe_step) if r["e2e_pipelined_ms"] is not None else None
-
-    attn_isolated_ms = statistics.mean(r["attn_ms"])
-    attn_launch_ms = r["attn_call_ms"] if r["attn_call_ms"] is not None else attn_isolated_ms
-    fused = args.append == "fused"
-    a_bytes = attn_bytes(case) + (fused_append_bytes(case) if fused else 0)
-    peak, peak_kind = hbm_peak()
-    achieved = a_bytes / (attn_launch_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(case.name, fused)
+    res = summarize(r, args, world)
 
     cpu = None
     if rank == 0 and args.cpu_budget > 0:
@@ -786,39 +815,169 @@ def main():
                                           f"each on its own 8 random requests for about "
                                           f"{args.cpu_budget / 2:.1f} s; summed rate"}
 
+    # the other workloads, each at full size in the same launch settings, fewer steps: per-call
+    # and per-step figures beside the headline (the headline stays the --workload one)
+    others = {}
+    for name in other_workloads(args):
+        import copy
+        import gc
+
+        import torch
+        del r
+        gc.collect()
+        torch.cuda.empty_cache()
+        a2 = copy.copy(args)
+        a2.workload, a2.steps, a2.chunk_tiles, a2.cpu_budget = name, min(args.steps, 10), 0, 0
+        r = run_gpu(a2, rank, world)
+        others[name] = compact(summarize(r, a2, world), a2, r["case"])
+
     if rank != 0:
         return
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": round(res["value"], 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(res["ms_step"], 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 Q/K/V, random page allocation)",
         "config": config_dict(case, args),
-        "us_per_layer_plane": round(ms_max * 1e3 / nlp, 2),
-        "pct_of_peak_hbm": round(100 * value / world / peak, 2),
-        "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
-        "kv_tokens_per_s": round(world * case.kv_tokens() * nlp / (ms_max * 1e-3), 1),
-        "roofline": {"bound": "hbm",
-                     "kernel": ("rlt_paged_decode_attn_prefix (tcgen05 shared-prefix + split-K + combine)"
-                                if r["cascade"] else "rlt_paged_decode_attn (split-K partial + combine)")
-                               + (", append fused" if fused else ""),
-                     "achieved": round(achieved, 2),
-                     "achieved_logical": round((attn_bytes(case, unique=False) + (a_bytes - attn_bytes(case)))
-                                               / (attn_launch_ms * 1e-3) / 1e9, 2),
-                     "peak": peak, "peak_kind": f"{peak_kind} (HBM copy)",
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": a_bytes, "launch_us": round(attn_launch_ms * 1e3, 2),
-                     "timing": r["attn_timing"],
-                     "launch_us_event_nodes": round(attn_isolated_ms * 1e3, 2)},
+        "us_per_layer_plane": res["us_per_layer_plane"],
+        "pct_of_peak_hbm": round(100 * res["value"] / world / res["roofline"]["peak"], 2),
+        "pct_of_nominal_8tbs": round(100 * res["value"] / world / NOMINAL_HBM_GBS, 2),
+        "kv_tokens_per_s": res["kv_tokens_per_s"],
+        "roofline": res["roofline"],
         "cpu_baseline": cpu,
-        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
-                "d2h_bytes_per_step": r["d2h"], "mode": r["e2e_mode"],
-                "serial_value": round(e2e_serial, 2),
-                "pipelined_value": round(e2e_pipe, 2) if e2e_pipe is not None else None},
-        "gpu_launches": r["launches"],
-        **({"extend_attention": r["extend"]} if r["extend"] else {}),
-        "clocks": r["clocks"],
+        "e2e": res["e2e"],
+        "gpu_launches": res["launches"],
+        **({"extend_attention": res["extend"]} if res["extend"] else {}),
+        **({"noise": res["noise"]} if res["noise"] else {}),
+        "clocks": res["clocks"],
+        **({"workloads": others} if others else {}),
     }
     print(json.dumps(line))
+
+
+def other_workloads(args):
+    """Workloads timed after the headline one: every other workload in the default run (the
+    headline's own launch settings, no profiling slice), none when asked or when slicing."""
+    if args.also == "none" or args.batch or args.banks:
+        return []
+    if args.also == "auto":
+        return [w for w in W.WORKLOADS if w != args.workload]
+    return [w for w in args.also.split(",") if w and w != args.workload]
+
+
+def summarize(r, args, world):
+    """The figures of one workload's run, times taken as the maximum over ranks."""
+    case = r["case"]
+    nlp = len(r["banks"])
+    step_bytes = attn_bytes(case) * nlp + append_bytes(case) * nlp + noise_bytes(case)
+    pipe_total = r["e2e_pipelined_ms"] if r["e2e_pipelined_ms"] is not None else r["e2e_serial_ms"]
+    attn_isolated_ms = statistics.mean(r["attn_ms"])
+    attn_launch_ms = r["attn_call_ms"] if r["attn_call_ms"] is not None else attn_isolated_ms
+    ms_max, e2e_ms_step, e2e_serial_step, e2e_pipe_step, attn_launch_ms, attn_isolated_ms, noise_ms = \
+        max_over_ranks([r["ms_total"] / args.steps, r["e2e_ms"] / args.steps, r["e2e_serial_ms"] / args.steps,
+                        pipe_total / args.steps, attn_launch_ms, attn_isolated_ms, r["noise_ms"] or 0.0])
+    value = job_gbs(step_bytes, world, ms_max)
+    e2e_value = job_gbs(step_bytes, world, e2e_ms_step)
+    e2e_serial = job_gbs(step_bytes, world, e2e_serial_step)
+    e2e_pipe = job_gbs(step_bytes, world, e2e_pipe_step) if r["e2e_pipelined_ms"] is not None else None
+    fused = args.append == "fused"
+    a_bytes = attn_bytes(case) + (fused_append_bytes(case) if fused else 0)
+    peak, peak_kind = hbm_peak()
+    achieved = a_bytes / (attn_launch_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(case.name, fused)
+    roofline = {"bound": "hbm",
+                "kernel": ("rlt_paged_decode_attn_prefix (tcgen05 shared-prefix + split-K + combine)"
+                           if r["cascade"] else "rlt_paged_decode_attn (split-K partial + combine)")
+                          + (", append fused" if fused else ""),
+                "achieved": round(achieved, 2),
+                "achieved_logical": round((attn_bytes(case, unique=False) + (a_bytes - attn_bytes(case)))
+                                          / (attn_launch_ms * 1e-3) / 1e9, 2),
+                "peak": peak, "peak_kind": f"{peak_kind} (HBM copy)",
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "frac_logical": round((attn_bytes(case, unique=False) + (a_bytes - attn_bytes(case)))
+                                      / (attn_launch_ms * 1e-3) / 1e9 / peak, 4),
+                "traffic": traffic,
+                "traffic_over_algorithmic": round(traffic / a_bytes, 4) if traffic else None,
+                "algorithmic_bytes_per_launch": a_bytes, "launch_us": round(attn_launch_ms * 1e3, 2),
+                "timing": r["attn_timing"],
+                "launch_us_event_nodes": round(attn_isolated_ms * 1e3, 2)}
+    return {"value": value, "ms_step": ms_max, "us_per_layer_plane": round(ms_max * 1e3 / nlp, 2),
+            "kv_tokens_per_s": round(world * case.kv_tokens() * nlp / (ms_max * 1e-3), 1),
+            "roofline": roofline,
+            "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
+                    "d2h_bytes_per_step": r["d2h"], "mode": r["e2e_mode"],
+                    "serial_value": round(e2e_serial, 2),
+                    "pipelined_value": round(e2e_pipe, 2) if e2e_pipe is not None else None},
+            "extend": r["extend"], "noise": noise_roofline(case, noise_ms) if r["noise_ms"] else None,
+            "clocks": r["clocks"], "launches": r["launches"]}
+
+
+def compact(res, args, case):
+    """One other workload's entry: per-call attention, per step, end to end, clocks."""
+    rf = res["roofline"]
+    return {"config": config_dict(case, args)["workload"], "steps": args.steps,
+            "us_per_attention_call": rf["launch_us"], "attention_gbs_unique": rf["achieved"],
+            "frac": rf["frac"], "frac_logical": rf["frac_logical"],
+            "traffic_over_algorithmic": rf["traffic_over_algorithmic"],
+            "attention_kernel": rf["kernel"],
+            "step_gbs": round(res["value"], 2), "ms_per_step": round(res["ms_step"], 4),
+            "us_per_layer_plane": res["us_per_layer_plane"], "e2e_gbs": res["e2e"]["value"],
+            **({"noise": res["noise"]} if res["noise"] else {}), "clocks": res["clocks"]}
+
+
+def noise_roofline(case: W.PagedCase, ms: float) -> dict:
+    """The latent-noise kernel against both of its bounds: the HBM write of 4 bytes per value (plus
+    the 16-byte key of each row) and integer issue (instructions per value from the committed ncu
+    summary of the current kernel source, else null; peak = SMs x 4 schedulers x 32 lanes x SM clock
+    / instructions per value)."""
+    nz = case.noise
+    values = nz.rows * nz.channels
+    nbytes = values * 4 + nz.rows * 16
+    t = ms * 1e-3
+    hbm, _ = hbm_peak()
+    out = {"kernel": "noise_kernel (rlt_latent_noise_init)", "values": values, "us_per_call": round(ms * 1e3, 2),
+           "values_per_s": round(values / t, 1), "write_gbs": round(nbytes / t / 1e9, 1),
+           "frac_of_hbm_peak": round(nbytes / t / 1e9 / hbm, 4)}
+    ipv = profiled_noise_instructions()
+    if ipv:
+        sms, mhz = sm_count_and_clock()
+        peak_vps = sms * 4 * 32 * mhz * 1e6 / ipv
+        out["alu"] = {"inst_per_value": ipv, "peak_values_per_s": round(peak_vps, 1),
+                      "frac": round(values / t / peak_vps, 4)}
+    out["bound"] = "alu" if ipv and values / t / out["alu"]["peak_values_per_s"] > out["frac_of_hbm_peak"] else "hbm"
+    return out
+
+
+def sm_count_and_clock():
+    """SMs of the current device and the measured maximum SM clock (MHz) of the GB300s."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f)["sm_max_mhz"])
+    except (OSError, KeyError, ValueError):
+        mhz = 2070.0
+    return sms, mhz
+
+
+def profiled_noise_instructions():
+    """Thread-instructions per value of the noise kernel from profiles/noise_kernel.txt, if that
+    summary was taken on the current noise.cu."""
+    import hashlib
+    try:
+        text = open(os.path.join(ROOT, "profiles", "noise_kernel.txt")).read()
+    except OSError:
+        return None
+    f = {k.strip(): v.strip() for k, v in (l.split(":", 1) for l in text.splitlines() if ":" in l)}
+    srcs = f.get("sources", "").split()
+    if not srcs:
+        return None
+    blob = b"".join(open(os.path.join(ROOT, "paged_kv_looped_gb300", "csrc", x), "rb").read() for x in srcs)
+    if f.get("sources_sha256_16") != hashlib.sha256(blob).hexdigest()[:16]:
+        return None
+    try:
+        return float(f["thread_instructions_per_value"])
+    except (KeyError, ValueError):
+        return None
 
 
 if __name__ == "__main__":

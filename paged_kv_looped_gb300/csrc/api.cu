@@ -667,13 +667,20 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
         SideStream *side = nullptr;
         if ((st = side_stream(&side)) != RLT_OK)
             return st;
+        // The tensor-core kernel starts early on the caller's stream (a plain programmatic
+        // dependence on the kernel ahead); the split-K rest runs on the side stream with an
+        // ordinary, complete dependence on what precedes the call.  Measured on GB300: a kernel
+        // started programmatically across the fork starts no earlier than after the kernel ahead
+        // completes and keeps the combine from starting early behind it; and with the split-K
+        // grid started early its CTAs take every SM the previous call frees, so the tensor-core
+        // CTAs (a whole SM each) wait until they drain.
         e = cudaEventRecord(side->fork, cs);
         if (e == cudaSuccess)
             e = cudaStreamWaitEvent(side->stream, side->fork, 0);
         if (e == cudaSuccess)
             e = rlt::launch_prefix(p, pp, p.k_bank, p.v_bank, bank_rows, cs, early);
         if (e == cudaSuccess)
-            e = rlt::launch_decode(p_rest, pool->head_dim, group, side->stream, early);
+            e = rlt::launch_decode(p_rest, pool->head_dim, group, side->stream, false);
         if (e == cudaSuccess)
             e = cudaEventRecord(side->join, side->stream);
         if (e == cudaSuccess)
