@@ -424,6 +424,25 @@ RLT_API rlt_status rlt_paged_decode_attn(const rlt_kv_pool *pool, int32_t bank, 
                                         (flags & RLT_ATTN_EARLY_START) != 0));
 }
 
+// Tensor-core CTAs of a shared-prefix call whose unshared rests run on the split-K kernel at
+// the same time: SMs in proportion to the two kernels' tokens (the rest's length is its
+// longest, 3/4 of it on average), weighted 9:4 for the tensor-core kernel's lower rate per
+// SM on the short runs a split plan leaves it; then as few as keep the same number of items
+// on the busiest CTA, so that the items spread evenly (measured on the huginn shape: 96
+// items on 72 CTAs 32.0 us per call, on 64 CTAs with 64 items 27.9).
+static int tc_share_ctas(int64_t items, int work_units, int chunk_tiles, int32_t batch, int32_t max_rest_len, int sms)
+{
+    const double pre = (double)work_units * chunk_tiles * rlt::kPrefixTile;
+    const double rest = 0.75 * (double)batch * max_rest_len;
+    const double share = std::min(1.0, 2.25 * pre / (pre + rest));
+    int ctas = std::max(1, std::min(sms - 1, (int)std::ceil(sms * share)));
+    if (items > 0) {
+        const int64_t per = (items + ctas - 1) / ctas;
+        ctas = (int)std::max<int64_t>(1, (items + per - 1) / per);
+    }
+    return ctas;
+}
+
 // Per-CTA costs of the tensor-core kernel measured on GB300 with every SM streaming: one
 // 128-token sub-tile in steady state, and the hand-over from one run (kv head, segment,
 // member block) to the next.
@@ -469,15 +488,24 @@ RLT_API int32_t rlt_choose_chunk_tiles(const int32_t *page_table, int32_t max_pa
     }
     tiles *= num_kv_heads;
     if (!private_tails) {
-        // a split-K kernel shares the SMs: the largest power of two (4..16) that still gives
-        // every CTA at least 16 items, never below 4 tiles (each item adds a partial), nor
-        // above the longest segment
-        int chunk = 16;
-        while (chunk > 4 && tiles < (int64_t)chunk * 16 * num_ctas)
-            chunk /= 2;
-        while (chunk > 1 && chunk > longest)
-            chunk /= 2;
-        return chunk;
+        // A split-K kernel shares the SMs (tc_share_ctas gives the tensor-core kernel its
+        // CTAs): take the chunk (2..16 tiles, at most the longest segment) that leaves the
+        // fewest 128-token sub-tiles on the busiest tensor-core CTA, the larger on a tie
+        // (fewer runs, fewer partials).
+        int best = std::min(2, longest), best_load = -1;
+        for (int chunk = 2; chunk <= std::min(16, longest); ++chunk) {
+            if ((st = plan(chunk)) != RLT_OK)
+                return -st;
+            const int64_t items = (int64_t)num_kv_heads * sizes[6];
+            const int ctas = num_ctas > 1 ? tc_share_ctas(items, sizes[6], chunk, batch, sizes[5], num_ctas)
+                                          : 1;
+            const int64_t load = (items + ctas - 1) / ctas * chunk;
+            if (best_load < 0 || load <= best_load) {
+                best_load = (int)load;
+                best = chunk;
+            }
+        }
+        return std::max(1, best);
     }
     // The tensor-core kernel does the whole call, one CTA per SM, each taking a contiguous
     // run of items: the call ends with the busiest CTA.  Estimate each CTA's busy time from
@@ -638,13 +666,7 @@ RLT_API rlt_status rlt_paged_decode_attn_prefix(
     if (max_ctas > 0) {
         ctas = std::min(max_ctas, sms);
     } else if (max_rest_len > 0 && sms > 1) {
-        // both kernels at once: SMs in proportion to their tokens (the rest's length is
-        // its longest, 3/4 of it on average), weighted 9:4 for the tensor-core kernel's
-        // lower rate per SM on the short runs a split plan leaves it
-        const double pre = (double)work_units * chunk_tiles * rlt::kPrefixTile;
-        const double rest = 0.75 * (double)batch * max_rest_len;
-        const double share = std::min(1.0, 2.25 * pre / (pre + rest));
-        ctas = std::max(1, std::min(sms - 1, (int)std::ceil(sms * share)));
+        ctas = tc_share_ctas(items, work_units, chunk_tiles, batch, max_rest_len, sms);
     }
     pp.ctas = (int32_t)std::min<int64_t>(ctas, items);
 

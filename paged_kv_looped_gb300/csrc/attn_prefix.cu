@@ -922,7 +922,13 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
     }
 
     // mem: member requests; lim: each member's key count in the segment (its shared tokens)
-    struct Seg { int first, tiles, parent; std::vector<int> mem; int64_t end_token; std::vector<int64_t> lim; };
+    struct Seg {
+        int first, tiles, parent;
+        std::vector<int> mem;
+        int64_t end_token;
+        std::vector<int64_t> lim;
+        int page_row = -1;                     // whose pages the kernel reads (-1: the last member)
+    };
     std::vector<Seg> segs;
     std::vector<int> deepest(batch, -1);       // segment holding each request's last shared tile
     struct Group { std::vector<int> mem; int seg; };
@@ -1034,6 +1040,69 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
             for (int b : segs[s].mem)
                 deepest[b] = (int)s;
     }
+    // Without private tails the split-K kernel takes each request's rest in 16-token tiles,
+    // so a member's shared prefix need not end on a 128-token tile: at the segment where its
+    // sharing ends, its key limit goes on page by page while its page is the page row's (the
+    // tensor-core kernel reads the segment's tiles from the page row's pages) and another
+    // member of the segment maps that page too (a member that goes on to a deeper segment
+    // reads that part of the tile there as well).  The pages a request shares with others past its last
+    // whole shared tile are then read once per kv head here instead of once per request by
+    // the split-K kernel; the segment's last tile may end mid-tile (end token), the kernel
+    // masks each member's keys past its limit.  (With private tails every token past the
+    // shared tiles belongs to a tail segment that starts on a tile; a segment of several
+    // member blocks keeps its limits on its tiles.)
+    if (!private_tails && page_size < kPrefixTile) {
+        std::vector<int64_t> L(batch);
+        for (int b = 0; b < batch; ++b)
+            L[b] = std::min<int64_t>(std::max(seq_lens[b], 0), (int64_t)max_pages * page_size);
+        auto page_of = [&](int b, int64_t tok) { return page_table[(int64_t)b * max_pages + tok / page_size]; };
+        for (size_t s = 0; s < segs.size(); ++s) {
+            Seg &sg = segs[s];
+            if ((int)sg.mem.size() > per_block)
+                continue;                          // several member blocks: limits stay on tiles
+            const int pr = sg.mem.back();
+            for (;;) {
+                bool grew = false;
+                for (size_t i = 0; i < sg.mem.size(); ++i) {
+                    const int b = sg.mem[i];
+                    const int64_t tok = sg.lim[i];
+                    if (deepest[b] != (int)s || tok % page_size != 0 || tok + page_size > std::min(L[b], L[pr]) ||
+                        page_of(b, tok) != page_of(pr, tok))
+                        continue;
+                    bool other = false;            // a second member maps this page here
+                    for (size_t k = 0; k < sg.mem.size() && !other; ++k) {
+                        const int c = sg.mem[k];
+                        other = c != b && tok + page_size <= L[c] && page_of(c, tok) == page_of(b, tok);
+                    }
+                    if (!other)
+                        continue;
+                    sg.lim[i] = tok + page_size;
+                    grew = true;
+                }
+                if (!grew)
+                    break;
+            }
+            int64_t end = sg.end_token;
+            for (int64_t x : sg.lim)
+                end = std::max(end, x);
+            sg.end_token = end;
+            sg.tiles = (int)((end + kPrefixTile - 1) / kPrefixTile) - sg.first;
+            // members stay in ascending limit order (a member block ends at its last member's
+            // limit); the page row keeps its role even if another member's limit now exceeds
+            // its own (that member's extension follows the page row's pages)
+            sg.page_row = pr;
+            std::vector<size_t> order(sg.mem.size());
+            for (size_t i = 0; i < order.size(); ++i)
+                order[i] = i;
+            std::stable_sort(order.begin(), order.end(), [&](size_t a, size_t b) { return sg.lim[a] < sg.lim[b]; });
+            Seg sorted = sg;
+            for (size_t i = 0; i < order.size(); ++i) {
+                sorted.mem[i] = sg.mem[order[i]];
+                sorted.lim[i] = sg.lim[order[i]];
+            }
+            sg = sorted;
+        }
+    }
     std::vector<int64_t> covered(batch, 0);
     for (int b = 0; b < batch; ++b) {
         if (deepest[b] < 0)
@@ -1105,7 +1174,7 @@ extern "C" RLT_API rlt_status rlt_plan_prefix(const int32_t *page_table, int32_t
         row[rlt::kSegSlotBase] = slot_base[s];
         row[rlt::kSegMemberBegin] = (int32_t)m;
         row[rlt::kSegMemberCount] = (int32_t)segs[s].mem.size();
-        row[rlt::kSegPageRow] = segs[s].mem.back();
+        row[rlt::kSegPageRow] = segs[s].page_row >= 0 ? segs[s].page_row : segs[s].mem.back();
         row[rlt::kSegEndToken] = (int32_t)segs[s].end_token;
         row[rlt::kSegWorkBegin] = (int32_t)work_begin[s];
         for (size_t i = 0; i < segs[s].mem.size(); ++i, ++m) {

@@ -7,11 +7,12 @@
 // into the value.  The 64-bit arithmetic is exact mod 2^64 on either side, so
 // the 24 bits agree bit for bit with a CPU computation.
 //
-// One stage and one erfinvf per value, written with coalesced 16-byte stores
-// (noise_kernel); the seed and position stages are hashed once per 16 values.
-// The work is integer/SFU arithmetic plus a write of 4 bytes per value; the
-// per-channel stage is computed on 32-bit halves down to only the 24 bits that
-// are kept (stage_top24).
+// One channel stage and one inverse error function per value, written with coalesced
+// 16-byte stores (noise_kernel); the seed and position stages are hashed once per 16
+// values, and so is everything of the channel stage that depends on the row only.  The
+// work is integer arithmetic plus a write of 4 bytes per value: the channel stage runs
+// on 32-bit halves down to only the 24 bits that are kept (stage_top24), the inverse
+// error function is a degree-8 polynomial after one hardware logarithm (truncnorm).
 #include "rlt_device.cuh"
 #include "rlt_internal.h"
 
@@ -19,7 +20,7 @@ namespace rlt {
 namespace {
 
 constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ull;   // SplitMix64 increment
-constexpr int kChunk = 16;                              // channels per thread
+constexpr int kChunk = 32;                              // channels per thread
 
 // SplitMix64 output function (Steele, Lea & Flood 2014).
 __device__ __forceinline__ uint64_t mix64(uint64_t z)
@@ -35,43 +36,90 @@ __device__ __forceinline__ uint64_t stage(uint64_t h, uint64_t x)
     return mix64((h ^ x) + kGolden);
 }
 
-// stage(h, x) >> 40, with 32-bit operations only where the result needs them.  The
-// last xor-shift of mix64 (z ^= z >> 31) leaves bits 33..63 unchanged, so the top 24
-// bits are those of the second product, and of that product only the high word is
-// formed (high half of lo * lo plus the two cross terms, mod 2^32).
-__device__ __forceinline__ uint32_t stage_top24(uint64_t h, uint64_t x)
+// stage(h, c) >> 40 for one row's h and channels c < 2^32, with the parts that depend
+// only on the row computed once.  In z0 = (h ^ c) + increment the channel touches only
+// the low word, so the high word is the row's constant plus the carry k out of the low
+// word; everything the high word feeds before the second multiply (its share of
+// z ^= z >> 30 and of the first product) is kept for k = 0 and k = 1.  The last
+// xor-shift of mix64 (z ^= z >> 31) leaves bits 33..63 unchanged, so the top 24 bits
+// are those of the second product, of which only the high word is formed (high half of
+// lo * lo plus the two cross terms, mod 2^32).
+struct RowStage {
+    uint32_t h_lo;               // low word of h
+    uint32_t lo_hi[2];           // (hi0 << 2): the high word's bits in the low word of z0 >> 30
+    uint32_t mul_hi[2];          // (hi0 ^ (hi0 >> 30)) * low word of the first multiplier
+};
+
+constexpr uint32_t kMulA_lo = 0x1CE4E5B9u, kMulA_hi = 0xBF58476Du;   // 0xBF58476D1CE4E5B9
+constexpr uint32_t kMulB_lo = 0x133111EBu, kMulB_hi = 0x94D049BBu;   // 0x94D049BB133111EB
+
+__device__ __forceinline__ RowStage row_stage(uint64_t h)
 {
-    const uint64_t z0 = (h ^ x) + kGolden;
-    uint32_t lo = (uint32_t)z0, hi = (uint32_t)(z0 >> 32);
-    lo ^= __funnelshift_r(lo, hi, 30);                   // z ^= z >> 30
-    hi ^= hi >> 30;
-    const uint32_t a_lo = 0x1CE4E5B9u, a_hi = 0xBF58476Du;
-    const uint64_t p = (uint64_t)lo * a_lo;              // z *= 0xBF58476D1CE4E5B9
-    uint32_t nlo = (uint32_t)p;
-    uint32_t nhi = (uint32_t)(p >> 32) + lo * a_hi + hi * a_lo;
-    nlo ^= __funnelshift_r(nlo, nhi, 27);                // z ^= z >> 27
+    RowStage r;
+    r.h_lo = (uint32_t)h;
+    const uint32_t hi = (uint32_t)(h >> 32) + (uint32_t)(kGolden >> 32);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const uint32_t hi0 = hi + (uint32_t)k;
+        r.lo_hi[k] = hi0 << 2;
+        r.mul_hi[k] = (hi0 ^ (hi0 >> 30)) * kMulA_lo;
+    }
+    return r;
+}
+
+__device__ __forceinline__ uint32_t stage_top24(const RowStage &r, uint32_t c)
+{
+    const uint32_t lo0 = (r.h_lo ^ c) + (uint32_t)kGolden;
+    const bool k = lo0 < (uint32_t)kGolden;               // carry into the high word
+    const uint32_t lo1 = lo0 ^ (lo0 >> 30) ^ (k ? r.lo_hi[1] : r.lo_hi[0]);
+    const uint64_t prod = (uint64_t)lo1 * kMulA_lo;       // z *= 0xBF58476D1CE4E5B9
+    uint32_t nlo = (uint32_t)prod;
+    uint32_t nhi = (uint32_t)(prod >> 32) + lo1 * kMulA_hi + (k ? r.mul_hi[1] : r.mul_hi[0]);
+    nlo ^= __funnelshift_r(nlo, nhi, 27);                 // z ^= z >> 27
     nhi ^= nhi >> 27;
-    const uint32_t b_lo = 0x133111EBu, b_hi = 0x94D049BBu;
-    const uint32_t top = __umulhi(nlo, b_lo) + nlo * b_hi + nhi * b_lo;   // (z * 0x94D049BB133111EB) >> 32
+    const uint32_t top = __umulhi(nlo, kMulB_lo) + nlo * kMulB_hi + nhi * kMulB_lo;   // (z * B) >> 32
     return top >> 8;
+}
+
+// erfinv(x) / x as a polynomial in w - kPolyCenter, w = -ln((1 - x)(1 + x)): a least-squares
+// fit (relative error) to the fp64 erfinv over every argument a 24-bit uniform produces,
+// |x| <= erf(3/sqrt 2)(1 - 2^-24), i.e. w <= 5.2228.  paged_kv_looped_gb300/noise_poly_fit.py
+// makes it and checks the fp32 evaluation below on all 2^24 codes: within 1e-7 of the exact
+// noise value at initializer_range 0.02.  Highest degree first.
+constexpr float kPolyCenter = 2.6113810539245605f;
+
+__device__ __forceinline__ float erfinv_over_x(float w)
+{
+    float p = 2.000139609e-08f;
+    p = fmaf(p, w, 3.579944234e-07f);
+    p = fmaf(p, w, -3.161313771e-06f);
+    p = fmaf(p, w, -6.567394848e-06f);
+    p = fmaf(p, w, 2.152242814e-04f);
+    p = fmaf(p, w, -1.157181803e-03f);
+    p = fmaf(p, w, -4.580128938e-03f);
+    p = fmaf(p, w, 2.456647605e-01f);
+    return fmaf(p, w, 1.528826952e+00f);
 }
 
 // Truncated-normal value of a 24-bit uniform h24: u = (h24 + 1/2) / 2^24 and
 // x = amp * erfinv((2u - 1) * erf(3/sqrt 2)), amp = initializer_range * sqrt 2.
-// (2u - 1) * 2^24 = 2*h24 + 1 - 2^24 is an odd integer below 2^24 in magnitude,
-// exact in fp32, and so is its scaling by 2^-24.
+// (2u - 1) * 2^24 = 2*h24 + 1 - 2^24 is an odd integer below 2^24 in magnitude, exact in
+// fp32, and its scaling by 2^-24 * erf(3/sqrt 2) rounds once.  The logarithm is the
+// hardware base-2 one (its error moves w by ~1e-7; the polynomial's slope is below 0.3).
 __device__ __forceinline__ float truncnorm(uint32_t h24, float amp)
 {
-    const float erf3 = 0.99730020393673981f;             // erf(3 / sqrt(2))
-    const float t = (float)((int)(2u * h24 + 1u) - (1 << 24)) * 0x1p-24f;
-    return amp * erfinvf(t * erf3);
+    const float kScale = 0x1p-24f * 0.99730020393673981f;   // 2^-24 * erf(3 / sqrt(2))
+    const float x = (float)((int)(2u * h24 + 1u) - (1 << 24)) * kScale;
+    const float ax = fabsf(x);
+    const float w = fmaf(-0.69314718055994531f, __log2f((1.f - ax) * (1.f + ax)), -kPolyCenter);
+    return amp * (x * erfinv_over_x(w));
 }
 
-// A warp makes a tile of 512 channels of one row: lane l takes channels
-// 128k + 4l .. 128k + 4l + 3 for k = 0..3, so each 16-byte store of the warp
+// A warp makes a tile of 1024 channels of one row: lane l takes channels
+// 128k + 4l .. 128k + 4l + 3 for k = 0..7, so each 16-byte store of the warp
 // fills 512 contiguous bytes, and the seed and position stages are hashed once
-// per 16 values.
-constexpr int kTile = 512;
+// per 32 values.
+constexpr int kTile = 32 * kChunk;
 
 template <bool kHashOnly>
 __global__ void __launch_bounds__(256)
@@ -82,10 +130,11 @@ __global__ void __launch_bounds__(256)
     const int lane = threadIdx.x & 31;
     const int64_t total = n_rows * tiles_per_row;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const bool narrow = total <= (int64_t)UINT32_MAX;     // 32-bit division suffices
     for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < total; t += warps) {
-        const int64_t r = t / tiles_per_row;
+        const int64_t r = narrow ? (int64_t)((uint32_t)t / (uint32_t)tiles_per_row) : t / tiles_per_row;
         const int32_t cb = (int32_t)(t - r * tiles_per_row) * kTile;
-        const uint64_t h_row = stage(stage(0ull, seeds[r]), (uint64_t)positions[r]);
+        const RowStage rs = row_stage(stage(stage(0ull, seeds[r]), (uint64_t)positions[r]));
         const int64_t row_base = r * channels;
 #pragma unroll
         for (int k = 0; k < kChunk / 4; ++k) {
@@ -95,7 +144,7 @@ __global__ void __launch_bounds__(256)
             uint32_t h24[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                h24[i] = stage_top24(h_row, (uint64_t)(int64_t)(c0 + i));
+                h24[i] = stage_top24(rs, (uint32_t)(c0 + i));
             const bool full = vec_ok && c0 + 4 <= channels;
             if constexpr (kHashOnly) {
                 if (full)

@@ -1,0 +1,44 @@
+"""Fit of the polynomial the noise kernel (csrc/noise.cu) uses for erfinv(x) / x.
+
+The latent noise maps a 24-bit uniform to x = erf(3/sqrt 2) (2u - 1) and returns
+initializer_range * sqrt(2) * erfinv(x).  On the GPU, erfinv(x) = x g(w) with
+w = -ln((1 - x)(1 + x)), and g is a degree-8 polynomial in w - c fitted here by least
+squares in relative error against scipy's fp64 erfinv over w in [0, w_max], w_max the
+largest w any 24-bit code produces (|x| <= erf(3/sqrt 2)(1 - 2^-24)).  The script then
+evaluates the kernel's fp32 path (the product, the log, Horner) on all 2^24 codes and
+prints the worst absolute error of the noise value at initializer_range 0.02 against the
+exact truncated-normal value, and the coefficients (highest degree first) and c.
+
+    python paged_kv_looped_gb300/noise_poly_fit.py
+"""
+import numpy as np
+from scipy.special import erf, erfinv
+
+
+def fit(deg: int = 8):
+    erf3 = erf(3 / np.sqrt(2))
+    h = np.arange(1 << 24, dtype=np.int64)
+    x32 = ((2 * h + 1 - (1 << 24)).astype(np.float32) * np.float32(2.0 ** -24 * erf3)).astype(np.float32)
+    ax = np.abs(x32)
+    y32 = ((np.float32(1) - ax) * (np.float32(1) + ax)).astype(np.float32)
+    w = (-np.float32(np.log(2)) * np.log2(y32.astype(np.float64)).astype(np.float32)).astype(np.float32)
+    w_max = float(w.max())
+    c = np.float32(0.5 * w_max)
+    grid = np.linspace(0.0, w_max, 40001)
+    xg = np.sqrt(-np.expm1(-grid))
+    g = np.where(xg > 0, erfinv(xg) / np.where(xg > 0, xg, 1), np.sqrt(np.pi) / 2)
+    coef, *_ = np.linalg.lstsq(np.vander(grid - float(c), deg + 1) / g[:, None], np.ones_like(g), rcond=None)
+    cf = [np.float32(a) for a in coef]
+    p = np.full_like(w, cf[0])
+    for a in cf[1:]:
+        p = (p * (w - c).astype(np.float32) + a).astype(np.float32)
+    amp = np.float32(0.02 * np.sqrt(2))
+    val = (amp * (x32 * p).astype(np.float32)).astype(np.float32)
+    exact = 0.02 * np.sqrt(2) * erfinv((2 * (h + 0.5) / 2.0 ** 24 - 1) * erf3)
+    return cf, float(c), float(np.abs(val - exact).max())
+
+
+if __name__ == "__main__":
+    cf, c, err = fit()
+    print(f"c = {c!r}  worst |value - exact| at initializer_range 0.02: {err:.3e}")
+    print(", ".join(f"{float(a):.9e}f" for a in cf))

@@ -38,44 +38,70 @@ def common_tiles(pt, sl, ps, b, c):
     return t
 
 
-def check_plan(case, chunk_tiles=4, G=1):
+def common_pages(pt, sl, ps, b, c):
+    """Leading pages b and c map alike, each page whole inside both requests."""
+    n = min(int(sl[b]), int(sl[c])) // ps
+    j = 0
+    while j < n and pt[b, j] == pt[c, j]:
+        j += 1
+    return j
+
+
+def check_plan(case, chunk_tiles=4, G=1, exact_pages=True):
+    """exact_pages: every request's pages shared with others form one chain (a radix tree over
+    one prompt), so its covered prefix is exactly its longest page-for-page run with another
+    request; otherwise it lies between its longest whole-tile run and that."""
     pt, sl, ps = case.page_table, case.seq_lens, case.page_size
     plan = rlt.rlt_plan_prefix(pt, sl, ps, chunk_tiles, False, G)
     per_block = 128 // G
     assert plan.max_rest_len == max(int(sl[b]) - int(plan.request_prefix[b, 0]) for b in range(case.batch))
     B = case.batch
     cp = np.zeros((B, B), int)
+    cpg = np.zeros((B, B), int)
     for b in range(B):
         for c in range(B):
             if b != c:
                 cp[b, c] = common_tiles(pt, sl, ps, b, c)
-    # each request's covered prefix = its longest shared run with any other request
+                cpg[b, c] = common_pages(pt, sl, ps, b, c)
+    # each request's covered prefix: its longest shared run of whole 128-token tiles with any
+    # other request, continued page by page (pages below a tile) while it still shares them
     for b in range(B):
-        assert plan.request_prefix[b, 0] == TILE * (cp[b].max() if B > 1 else 0), b
-    # segments: at tile t the members whose limit lies past t share it page for page
-    # with the page row, and nobody else does
+        cov = int(plan.request_prefix[b, 0])
+        tiles = TILE * (cp[b].max() if B > 1 else 0)
+        pages = ps * (cpg[b].max() if B > 1 else 0) if ps < TILE else tiles
+        assert cov % min(ps, TILE) == 0 and tiles <= cov <= max(tiles, pages), b
+        if exact_pages:
+            assert cov == max(tiles, pages), b
+    # segments: at tile t the members whose limit lies past t share its pages below their
+    # limit with the page row
     seg_of_tile = {}
     for s in range(plan.num_segments):
         first, n, base, mb, mc, row, end, work = plan.segments[s]
-        assert end == (first + n) * TILE
+        assert (first + n - 1) * TILE < end <= (first + n) * TILE
         mem = plan.members[mb: mb + mc]
         lim = plan.member_limit[mb: mb + mc]
-        assert mc >= 2 and row == mem[-1] and lim[-1] == end
+        assert mc >= 2 and row in mem and lim[-1] == end
         assert list(lim) == sorted(lim) and len(set(mem)) == mc
-        assert all(first * TILE < x <= end and x % TILE == 0 for x in lim)
+        assert all(first * TILE < x <= end and x % min(ps, TILE) == 0 for x in lim)
         if len(set(lim)) > 1:
             assert mc <= per_block                 # a merged chain fits one member block
         for t in range(first, first + n):
             live = {int(b) for b, x in zip(mem, lim) if x > t * TILE}
-            want = {int(row)} | {c for c in range(B) if c != row and cp[row, c] >= t + 1}
-            assert live == want, (s, t)
-            for b in live:
-                assert tile_key(pt, b, t, ps) == tile_key(pt, row, t, ps)
-                seg_of_tile.setdefault(b, []).append((t, s))
+            # every request sharing the row's whole tile t is a live member
+            assert {c for c in range(B) if c != row and cp[row, c] >= t + 1} <= live, (s, t)
+            for b, x in zip(mem, lim):
+                if x <= t * TILE:
+                    continue
+                if ps >= TILE:
+                    assert tile_key(pt, b, t, ps) == tile_key(pt, row, t, ps)
+                else:
+                    for j in range(t * TILE // ps, min(x, (t + 1) * TILE) // ps):
+                        assert pt[b, j] == pt[row, j], (s, t, b, j)
+                seg_of_tile.setdefault(int(b), []).append((t, s))
     # along each request's path: tiles 0..n-1 in order, partial slots contiguous from 0
     for b in range(B):
         tiles = sorted(seg_of_tile.get(b, []))
-        assert [t for t, _ in tiles] == list(range(plan.request_prefix[b, 0] // TILE))
+        assert [t for t, _ in tiles] == list(range(-(-int(plan.request_prefix[b, 0]) // TILE)))
         slots = []
         for s in dict.fromkeys(s for _, s in tiles):
             first, n, base = plan.segments[s][:3]
@@ -110,7 +136,8 @@ def test_chain_merge_respects_member_blocks(G):
     # members stay segments of their own, every member reading all their tiles
     case = W.custom(B=5, Hq=8, Hkv=8, D=128, ps=16, seq_lens=[3000, 2600, 4100, 1700, 2222], shared_frac=0.8,
                     seed=11)
-    plan = check_plan(case, 2, G)
+    # (limits go on page by page only in segments of one member block)
+    plan = check_plan(case, 2, G, exact_pages=5 <= 128 // G)
     if 5 <= 128 // G:
         assert plan.num_segments == 1
     else:
@@ -148,8 +175,10 @@ def test_plan_of_two_trees_and_loners():
                        seq_lens=np.array(lens, np.int32), page_table=pt, new_slots=np.zeros(len(lens), np.int64))
     plan = check_plan(case)
     assert plan.request_prefix[7, 0] == 0 and plan.request_prefix[8, 0] == 0
-    assert plan.request_prefix[0, 0] == 640                 # 700 tokens -> 5 whole tiles
-    assert plan.request_prefix[4, 0] == 1280
+    # the shared prompts end mid-tile: every whole page of them is covered (700 tokens -> 43
+    # pages of 16 = 5 whole tiles and 3 pages; 1400 -> 87 pages = 10 tiles and 7 pages)
+    assert plan.request_prefix[0, 0] == 43 * ps
+    assert plan.request_prefix[4, 0] == 87 * ps
 
 
 @pytest.mark.parametrize("ps", [32, 64, 128, 256])
@@ -173,17 +202,23 @@ def test_private_tails_cover_every_token(name):
     plan = rlt.rlt_plan_prefix(pt, sl, ps, 4, private_tails=True)
     assert plan.max_rest_len == 0
     assert np.array_equal(plan.request_prefix[:, 0], sl)
-    # the shared segments are unchanged; one tail per request follows them
+    # the shared segments are those of the plan without tails, cut back to whole tiles (a
+    # tail starts on a tile); one tail per request follows them
     n = shared.num_segments
-    assert np.array_equal(plan.segments[:n, :7], shared.segments[:, :7])
+    assert np.array_equal(plan.segments[:n, [0, 3, 4, 5]], shared.segments[:, [0, 3, 4, 5]])
+    assert np.all(plan.segments[:n, 6] % TILE == 0) and np.all(plan.segments[:n, 6] <= shared.segments[:, 6])
+    covered = {}                                  # each request's shared tokens, whole tiles
+    for first, ntiles, base, mb, mc, row, end, work in plan.segments[:n]:
+        for b, lim in zip(plan.members[mb: mb + mc], plan.member_limit[mb: mb + mc]):
+            covered[int(b)] = max(covered.get(int(b), 0), int(lim))
+            assert lim % TILE == 0
     tails = plan.segments[n:]
-    assert len(tails) == sum(1 for b in range(case.batch) if sl[b] > shared.request_prefix[b, 0])
+    assert len(tails) == sum(1 for b in range(case.batch) if sl[b] > covered.get(b, 0))
     for first, ntiles, base, mb, mc, row, end, work in tails:
-        b = plan.members[mb]
+        b = int(plan.members[mb])
         assert mc == 1 and row == b and end == sl[b]
-        assert first * TILE == shared.request_prefix[b, 0]
+        assert first * TILE == covered.get(b, 0) == shared.request_prefix[b, 0] // TILE * TILE
         assert (first + ntiles) * TILE >= end > (first + ntiles - 1) * TILE
-        assert base == shared.request_prefix[b, 1]
         assert plan.request_prefix[b, 1] == base + -(-ntiles // 4) * copies(1, 1)
 
 
@@ -274,16 +309,23 @@ def test_choose_chunk_tiles_custom_batches(G):
         best = min(costs.values())
         want = min(max(c for c, v in costs.items() if v <= best + 1e-6), longest)
         assert got == want
-        # without private tails: the count rule (16 items per CTA, 4..16 tiles, power of two)
+        # without private tails: the chunk (2..16, at most the longest segment) with the fewest
+        # sub-tiles on the busiest tensor-core CTA when the CTAs are the SMs' share the call
+        # gives that kernel beside the split-K rest, items spread evenly; the larger on a tie
         got2 = rlt.rlt_choose_chunk_tiles(case.page_table, case.seq_lens, case.page_size, G, False, 8, ctas)
         p1 = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, 16, 1, False, G)
-        tiles = sum(int(s[1]) * -(-int(s[4]) // (128 // G)) for s in p1.segments) * 8
-        chunk = 16
-        while chunk > 4 and tiles < chunk * 16 * ctas:
-            chunk //= 2
-        while chunk > 1 and chunk > max([int(s[1]) for s in p1.segments] + [1]):
-            chunk //= 2
-        assert got2 == chunk
+        longest2 = max([int(s[1]) for s in p1.segments] + [1])
+        loads = {}
+        for c in range(2, min(16, longest2) + 1):
+            pc = rlt.rlt_plan_prefix(case.page_table, case.seq_lens, 16, c, False, G)
+            items = 8 * pc.work_units
+            share = min(1.0, 2.25 * pc.work_units * c * 128 / (pc.work_units * c * 128 + 0.75 * case.batch
+                                                                 * pc.max_rest_len))
+            n = max(1, min(ctas - 1, int(np.ceil(ctas * share))))
+            per = -(-items // n)
+            n = max(1, -(-items // per))
+            loads[c] = -(-items // n) * c
+        assert got2 == max(c for c, v in loads.items() if v == min(loads.values()))
 
 
 def test_choose_chunk_tiles_rejects_bad_arguments():
