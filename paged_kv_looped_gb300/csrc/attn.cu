@@ -783,16 +783,60 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_warp_kernel(co
     const int total = n_pre + n;                 // <= prefix_slots + max_splits <= 32
     const int64_t row = bh * p.part_stride;
     const int my_slot = lane < n_pre ? lane : p.prefix_slots + (lane - n_pre);
+    auto slot_part = [&](int s) -> const float * {
+        return p.o_part + (row + (s < n_pre ? s : p.prefix_slots + (s - n_pre))) * D + lane * DPL;
+    };
+    float acc[DPL];
+#pragma unroll
+    for (int d = 0; d < DPL; ++d)
+        acc[d] = 0.f;
+    if (total <= kLoads) {
+        // every slot's partial is read together with the log-sum-exps (one round trip); a slot
+        // without a partial may hold anything, so it is skipped, never scaled by zero
+        float v[kLoads][DPL];
+#pragma unroll
+        for (int i = 0; i < kLoads; ++i) {
+            if (i < total) {
+                if constexpr (DPL == 4) {
+                    const float4 x = __ldcg(reinterpret_cast<const float4 *>(slot_part(i)));
+                    v[i][0] = x.x; v[i][1] = x.y; v[i][2] = x.z; v[i][3] = x.w;
+                } else {
+                    const float2 x = __ldcg(reinterpret_cast<const float2 *>(slot_part(i)));
+                    v[i][0] = x.x; v[i][1] = x.y;
+                }
+            }
+        }
+        const float l = lane < total ? __ldcg(p.lse_part + row + my_slot) : -CUDART_INF_F;
+        const float M = warp_max_xor(l, 1);
+        const float w = l != -CUDART_INF_F ? exp2f(l - M) : 0.f;
+        const float ls = warp_sum_xor(w, 1);
+#pragma unroll
+        for (int i = 0; i < kLoads; ++i) {
+            const float wi = __shfl_sync(kFullMask, w, i);
+            if (i < total && wi > 0.f) {
+#pragma unroll
+                for (int d = 0; d < DPL; ++d)
+                    acc[d] = fmaf(wi, v[i][d], acc[d]);
+            }
+        }
+        const float inv = ls > 0.f ? 1.f / ls : 0.f;
+        if constexpr (DPL == 4) {
+            uint2 x;
+            x.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            x.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+            *reinterpret_cast<uint2 *>(o) = x;
+        } else {
+            *reinterpret_cast<uint32_t *>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        }
+        if (lane == 0 && p.lse_out != nullptr)
+            p.lse_out[bh] = ls > 0.f ? (M + log2f(ls)) * kLn2 : -CUDART_INF_F;
+        return;
+    }
     const float l = lane < total ? __ldcg(p.lse_part + row + my_slot) : -CUDART_INF_F;
     const float M = warp_max_xor(l, 1);
     const float w = l != -CUDART_INF_F ? exp2f(l - M) : 0.f;
     const float ls = warp_sum_xor(w, 1);
     unsigned live = __ballot_sync(kFullMask, l != -CUDART_INF_F);
-
-    float acc[DPL];
-#pragma unroll
-    for (int d = 0; d < DPL; ++d)
-        acc[d] = 0.f;
     while (live != 0u) {
         int sl[kLoads];
 #pragma unroll
