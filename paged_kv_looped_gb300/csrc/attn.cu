@@ -27,6 +27,7 @@
 
 #include "rlt_device.cuh"
 #include "rlt_internal.h"
+#include "rlt_merge.cuh"
 
 namespace rlt {
 namespace {
@@ -34,7 +35,6 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 2;                   // copy ring depth per warp
-constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D, int G>
 struct Cfg {
@@ -49,37 +49,6 @@ struct Cfg {
     static constexpr int kBarOffset = kRegionBytes + kPBytes;
     static constexpr int kSmemBytes = kBarOffset + kWarps * kStages * 8;
 };
-
-// Tokens [tok0, L) of request b that the split-K kernels cover, and n_pre, the
-// partials the shared-prefix kernel wrote for it.  seq_lens[b] is clamped to
-// the page-table row and the split grid (a clamp is recorded as an error).
-struct Span {
-    int tok0, L, n_pre;
-};
-
-__device__ __forceinline__ Span request_span(const DecodeParams &p, int b, bool report)
-{
-    int len = p.seq_lens[b];
-    bool bad = false;
-    const int64_t cap_pages = (int64_t)p.max_pages * p.page_size;
-    if (len < 0 || len > cap_pages) {
-        len = len < 0 ? 0 : (int)cap_pages;
-        bad = true;
-    }
-    Span sp{0, len, 0};
-    if (p.request_prefix != nullptr) {
-        sp.tok0 = min(max(p.request_prefix[2 * b], 0), len);
-        sp.n_pre = p.request_prefix[2 * b + 1];
-    }
-    const int64_t cap_grid = (int64_t)p.max_splits * p.tiles_per_split * kTileTokens;
-    if (sp.L - sp.tok0 > cap_grid) {
-        sp.L = (int)(sp.tok0 + cap_grid);
-        bad = true;
-    }
-    if (bad && report)
-        record_error(p.err, RLT_DEVERR_BAD_LEN);
-    return sp;
-}
 
 template <int DPL>
 __device__ __forceinline__ void load_frag(const unsigned char *src, float (&f)[DPL])
@@ -349,19 +318,22 @@ __device__ __forceinline__ void pv_tile(const unsigned char *vs, const float *pb
     }
 }
 
-template <int D, int G>
+template <int D, int G, bool kFault>
 __device__ __forceinline__ void decode_partial_body(const DecodeParams &p);
 
 // The split-K kernel.  In shared-prefix mode it covers each request's tokens
 // past its shared segments and runs beside the tensor-core kernel, on a second
-// stream; the combine waits for both.
-template <int D, int G>
+// stream; the combine waits for both.  kFault: the instance that the timeout
+// test's fault switch launches (one copy left unissued, the wait limit from the
+// call); every other call runs the instance without either, whose registers
+// the switch does not disturb.
+template <int D, int G, bool kFault>
 __global__ void __launch_bounds__(kThreads) decode_partial_kernel(const DecodeParams p)
 {
-    decode_partial_body<D, G>(p);
+    decode_partial_body<D, G, kFault>(p);
 }
 
-template <int D, int G>
+template <int D, int G, bool kFault>
 __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
 {
     using C = Cfg<D, G>;
@@ -460,7 +432,7 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
             unsigned char *dst = pipe + (i % kStages) * C::kStageBytes;
             const int64_t row = ((int64_t)page * p.num_kv_heads + g) * p.page_size + off;
             mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
-            if (p.debug_drop_copy != 0 && i == 0 && warp == 0 && split == 0 && g == 0 && b == 0) {
+            if (kFault && i == 0 && warp == 0 && split == 0 && g == 0 && b == 0) {
                 // fault injection (timeout test only): this stage's bytes never arrive
             } else if (i != i_new) {
                 bulk_load(dst, p.k_bank + row * D, C::kTileBytes, bar);
@@ -518,7 +490,7 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
     }
 
     uint32_t phase = 0;                        // bit s: parity of stage s's next phase
-    const uint64_t wait_ns = p.wait_limit_ns != 0 ? p.wait_limit_ns : kWaitLimitNs;
+    const uint64_t wait_ns = kFault ? p.wait_limit_ns : kWaitLimitNs;
     int failed_at = -1;
 
     for (int i = 0; i < my_count; ++i) {
@@ -547,11 +519,27 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
             }
 
             // Partial dot products of this lane's dims for its half's 8 rows.
+            // At head_dim 128 with one or two query heads per kv head the 8 rows' K fragments are read
+            // first, so that their shared-memory loads overlap (measured on the G = 1 ouro
+            // workload: 177.9 -> 175.6 us per call); larger groups have the registers busy.
             float sc[G][8];
+            constexpr int kAhead = (D == 128 && G <= 2) ? 8 : 1;
+            uint64_t k_ahead[kAhead][DPL / 2];
+            if constexpr (kAhead == 8) {
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    load_frag2<DPL>(ks + ((half * 8 + r) * D + j * DPL) * 2, k_ahead[r]);
+            }
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 uint64_t kf[DPL / 2];
-                load_frag2<DPL>(ks + ((half * 8 + r) * D + j * DPL) * 2, kf);
+                if constexpr (kAhead == 8) {
+#pragma unroll
+                    for (int d = 0; d < DPL / 2; ++d)
+                        kf[d] = k_ahead[r][d];
+                } else {
+                    load_frag2<DPL>(ks + ((half * 8 + r) * D + j * DPL) * 2, kf);
+                }
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     uint64_t a = f2_mul(q[h][0], kf[0]);
@@ -723,14 +711,13 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
 {
     __shared__ MergeSmem<D> sm;
     pdl_launch_dependents();
-    pdl_wait();                                  // the partial kernels of this call are done
     const int64_t bh = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = (int)(bh / p.num_q_heads);
-    const Span sp = request_span(p, b, false);
+    const Span sp = request_span(p, b, false);   // inputs of the call: read before the wait
     const int n_pre = sp.n_pre;
-    const int n_tiles = (sp.L - sp.tok0 + kTileTokens - 1) / kTileTokens;
-    const int n = (n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    const int n = split_count(p, sp);
+    pdl_wait();                                  // the partial kernels of this call are done
     if (n_pre == 0 && n == 1)
         return;                                  // written by the partial kernel
     if (n_pre + n == 0) {                        // empty request: out = 0, lse = -inf
@@ -751,138 +738,21 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
 template <int D, int kLoads>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_warp_kernel(const DecodeParams p)
 {
-    constexpr int DPL = D / 32;
     pdl_launch_dependents();
-    pdl_wait();                                  // the partial kernels of this call are done
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t bh = (int64_t)blockIdx.x * kCombineWarps + warp;
-    if (bh >= (int64_t)p.batch * p.num_q_heads)
-        return;
-    const int b = (int)(bh / p.num_q_heads);
-    const Span sp = request_span(p, b, false);
-    int n_pre = sp.n_pre;
-    if (n_pre < 0 || n_pre > p.prefix_slots) {   // a plan inconsistent with the workspace
-        if (lane == 0)
-            record_error(p.err, RLT_DEVERR_BAD_SLOT);
-        n_pre = n_pre < 0 ? 0 : p.prefix_slots;
+    const bool live = bh < (int64_t)p.batch * p.num_q_heads;
+    // the lengths and the plan are inputs of the call: read before the wait
+    int n_pre = 0, n = 0;
+    if (live) {
+        const Span sp = request_span(p, (int)(bh / p.num_q_heads), false);
+        n_pre = prefix_partials(p, sp, lane == 0);
+        n = split_count(p, sp);
     }
-    const int n_tiles = (sp.L - sp.tok0 + kTileTokens - 1) / kTileTokens;
-    const int n = (n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
-    if (n_pre == 0 && n == 1)
-        return;                                  // written by the partial kernel
-    uint16_t *o = p.out + bh * D + lane * DPL;
-    if (n_pre + n == 0) {                        // empty request: out = 0, lse = -inf
-        if constexpr (DPL == 4)
-            *reinterpret_cast<uint2 *>(o) = make_uint2(0u, 0u);
-        else
-            *reinterpret_cast<uint32_t *>(o) = 0u;
-        if (lane == 0 && p.lse_out != nullptr)
-            p.lse_out[bh] = -CUDART_INF_F;
-        return;
-    }
-    const int total = n_pre + n;                 // <= prefix_slots + max_splits <= 32
-    const int64_t row = bh * p.part_stride;
-    const int my_slot = lane < n_pre ? lane : p.prefix_slots + (lane - n_pre);
-    auto slot_part = [&](int s) -> const float * {
-        return p.o_part + (row + (s < n_pre ? s : p.prefix_slots + (s - n_pre))) * D + lane * DPL;
-    };
-    float acc[DPL];
-#pragma unroll
-    for (int d = 0; d < DPL; ++d)
-        acc[d] = 0.f;
-    if (total <= kLoads) {
-        // every slot's partial is read together with the log-sum-exps (one round trip); a slot
-        // without a partial may hold anything, so it is skipped, never scaled by zero
-        float v[kLoads][DPL];
-#pragma unroll
-        for (int i = 0; i < kLoads; ++i) {
-            if (i < total) {
-                if constexpr (DPL == 4) {
-                    const float4 x = __ldcg(reinterpret_cast<const float4 *>(slot_part(i)));
-                    v[i][0] = x.x; v[i][1] = x.y; v[i][2] = x.z; v[i][3] = x.w;
-                } else {
-                    const float2 x = __ldcg(reinterpret_cast<const float2 *>(slot_part(i)));
-                    v[i][0] = x.x; v[i][1] = x.y;
-                }
-            }
-        }
-        const float l = lane < total ? __ldcg(p.lse_part + row + my_slot) : -CUDART_INF_F;
-        const float M = warp_max_xor(l, 1);
-        const float w = l != -CUDART_INF_F ? exp2f(l - M) : 0.f;
-        const float ls = warp_sum_xor(w, 1);
-#pragma unroll
-        for (int i = 0; i < kLoads; ++i) {
-            const float wi = __shfl_sync(kFullMask, w, i);
-            if (i < total && wi > 0.f) {
-#pragma unroll
-                for (int d = 0; d < DPL; ++d)
-                    acc[d] = fmaf(wi, v[i][d], acc[d]);
-            }
-        }
-        const float inv = ls > 0.f ? 1.f / ls : 0.f;
-        if constexpr (DPL == 4) {
-            uint2 x;
-            x.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-            x.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-            *reinterpret_cast<uint2 *>(o) = x;
-        } else {
-            *reinterpret_cast<uint32_t *>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        }
-        if (lane == 0 && p.lse_out != nullptr)
-            p.lse_out[bh] = ls > 0.f ? (M + log2f(ls)) * kLn2 : -CUDART_INF_F;
-        return;
-    }
-    const float l = lane < total ? __ldcg(p.lse_part + row + my_slot) : -CUDART_INF_F;
-    const float M = warp_max_xor(l, 1);
-    const float w = l != -CUDART_INF_F ? exp2f(l - M) : 0.f;
-    const float ls = warp_sum_xor(w, 1);
-    unsigned live = __ballot_sync(kFullMask, l != -CUDART_INF_F);
-    while (live != 0u) {
-        int sl[kLoads];
-#pragma unroll
-        for (int i = 0; i < kLoads; ++i) {
-            sl[i] = live != 0u ? __ffs(live) - 1 : -1;
-            live &= live - 1u;
-        }
-        float v[kLoads][DPL];
-#pragma unroll
-        for (int i = 0; i < kLoads; ++i) {
-            const int s = sl[i] >= 0 ? sl[i] : 0;
-            const int slot = s < n_pre ? s : p.prefix_slots + (s - n_pre);
-            const float *op = p.o_part + (row + slot) * D + lane * DPL;
-            if constexpr (DPL == 4) {
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (sl[i] >= 0)
-                    x = __ldcg(reinterpret_cast<const float4 *>(op));
-                v[i][0] = x.x; v[i][1] = x.y; v[i][2] = x.z; v[i][3] = x.w;
-            } else {
-                float2 x = make_float2(0.f, 0.f);
-                if (sl[i] >= 0)
-                    x = __ldcg(reinterpret_cast<const float2 *>(op));
-                v[i][0] = x.x; v[i][1] = x.y;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < kLoads; ++i) {
-            const float wi = __shfl_sync(kFullMask, w, sl[i] >= 0 ? sl[i] : 0);
-            if (sl[i] >= 0) {
-#pragma unroll
-                for (int d = 0; d < DPL; ++d)
-                    acc[d] = fmaf(wi, v[i][d], acc[d]);
-            }
-        }
-    }
-    const float inv = ls > 0.f ? 1.f / ls : 0.f;
-    if constexpr (DPL == 4) {
-        uint2 x;
-        x.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        x.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-        *reinterpret_cast<uint2 *>(o) = x;
-    } else {
-        *reinterpret_cast<uint32_t *>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    }
-    if (lane == 0 && p.lse_out != nullptr)
-        p.lse_out[bh] = ls > 0.f ? (M + log2f(ls)) * kLn2 : -CUDART_INF_F;
+    pdl_wait();                                  // the partial kernels of this call are done
+    if (!live || (n_pre == 0 && n == 1))
+        return;                                  // (written by the partial kernel)
+    merge_row_warp<D, kLoads>(p, bh, n_pre, n, lane);
 }
 
 template <int D>
@@ -911,19 +781,20 @@ cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream, bool early)
 {
     using C = Cfg<D, G>;
     static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
-    auto kernel = decode_partial_kernel<D, G>;
+    const bool fault = p.debug_drop_copy != 0;
+    auto kernel = fault ? decode_partial_kernel<D, G, true> : decode_partial_kernel<D, G, false>;
     // The shared-memory opt-in is per function and device: set it once per device.
-    static std::atomic<uint64_t> configured{0};
+    static std::atomic<uint64_t> configured[2]{{0}, {0}};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
-    if (bit == 0 || (configured.load(std::memory_order_acquire) & bit) == 0) {
+    if (bit == 0 || (configured[fault].load(std::memory_order_acquire) & bit) == 0) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess)
             return e;
-        configured.fetch_or(bit, std::memory_order_acq_rel);
+        configured[fault].fetch_or(bit, std::memory_order_acq_rel);
     }
     const dim3 grid(p.max_splits, p.num_kv_heads, p.batch);
     e = launch_kernel(kernel, grid, dim3(kThreads), C::kSmemBytes, stream, early, p);

@@ -45,10 +45,11 @@ struct DecodeParams {
     // and uses them in place of what it read from there.
     const uint16_t *k_new;
     const uint16_t *v_new;
-    // Copy-wait limit of the split-K kernel in ns (0: the default, one second), and the
-    // fault-injection switch of the timeout test (rlt_debug_fault_next_decode): non-zero
-    // leaves the first tile copy of CTA (0, 0, 0)'s warp 0 unissued, so that its wait
-    // runs out.  Zero in every ordinary call.
+    // The fault-injection switch of the timeout test (rlt_debug_fault_next_decode): non-zero
+    // launches the split-K kernel's fault instance, which leaves the first tile copy of CTA
+    // (0, 0, 0)'s warp 0 unissued, so that its wait runs out, and gives every copy wait the
+    // limit wait_limit_ns.  Zero in every ordinary call (the waits take the one-second
+    // default).
     uint64_t wait_limit_ns;
     int32_t debug_drop_copy;
 };
