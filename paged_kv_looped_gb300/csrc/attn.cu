@@ -435,8 +435,8 @@ __device__ __forceinline__ void decode_partial_body(const DecodeParams &p)
             if (kFault && i == 0 && warp == 0 && split == 0 && g == 0 && b == 0) {
                 // fault injection (timeout test only): this stage's bytes never arrive
             } else if (i != i_new) {
-                bulk_load(dst, p.k_bank + row * D, C::kTileBytes, bar);
-                bulk_load(dst + C::kTileBytes, p.v_bank + row * D, C::kTileBytes, bar);
+                bulk_load_once(dst, p.k_bank + row * D, C::kTileBytes, bar);
+                bulk_load_once(dst + C::kTileBytes, p.v_bank + row * D, C::kTileBytes, bar);
             } else {
                 constexpr uint32_t kRow = D * 2;
                 const int64_t nrow = ((int64_t)b * p.num_kv_heads + g) * D;

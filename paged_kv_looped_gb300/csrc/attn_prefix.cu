@@ -108,6 +108,7 @@ struct RunDesc {
     int64_t tok_begin, tok_end;
     int32_t g, nsub, page_row, n_mem, slot, nchunks, F;
     int32_t tail;                            // a one-member segment: a request's private tail
+    int32_t once;                            // one member block covers the segment: its tiles are read once
 };
 static_assert(sizeof(RunDesc) <= 64, "descriptor slot");
 
@@ -145,6 +146,7 @@ __device__ __forceinline__ Run decode_run(const PrefixParams &pp, int G, int ite
     r.member_begin = sd[kSegMemberBegin] + m0;
     r.d.page_row = sd[kSegPageRow];
     r.d.tail = sd[kSegMemberCount] == 1;
+    r.d.once = sd[kSegMemberCount] <= per_block;
     r.d.slot = sd[kSegSlotBase] + chunk0 * r.d.F;
     const int t_first = sd[kSegFirstTile] + chunk0 * pp.chunk_tiles;
     const int t_last = sd[kSegFirstTile] + min(num_tiles, (chunk0 + r.d.nchunks) * pp.chunk_tiles);
@@ -400,6 +402,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const int64_t nt = nt_next;
             const int nt_b = cur.page_row, nt_g = cur.g;
             const int64_t sub_begin = cur.tok_begin + (int64_t)j * kSub, tok_end = cur.tok_end;
+            const bool once = cur.once != 0;
             if (j + 1 < cur.nsub) {
                 row_next = lane_row(cur, ++j);
             } else {
@@ -438,9 +441,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
                 asm volatile("fence.proxy.async.global;" ::: "memory");
             }
-            if (lane < 2 * nbox)
-                tc::tma_load_2d(ring + st * kKVBytes + (lane & 1) * kHalfKV + (lane >> 1) * BR * 128, map,
-                                (lane & 1) * 64, row, &fullx[st]);
+            if (lane < 2 * nbox) {
+                void *dst = ring + st * kKVBytes + (lane & 1) * kHalfKV + (lane >> 1) * BR * 128;
+                if (once)
+                    tc::tma_load_2d_once(dst, map, (lane & 1) * 64, row, &fullx[st]);
+                else
+                    tc::tma_load_2d(dst, map, (lane & 1) * 64, row, &fullx[st]);
+            }
             ++n;
         }
         if (!ok) {

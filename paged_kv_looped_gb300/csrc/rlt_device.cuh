@@ -175,6 +175,21 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
+// The same copy for data read once per call (a request's own K/V rows): its L2 lines are
+// marked evict-first, so that what the call reads again soon -- the partials the combine
+// merges, q, page tables, plans -- keeps its place in L2.  The policy is made in place (one
+// instruction), so no register carries it through a loop.
+__device__ __forceinline__ void bulk_load_once(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\t"
+        "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], pol;\n\t}" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ------------------------------------------- programmatic dependent launch
 // A kernel launched with programmatic stream serialization may start before the
 // kernel ahead of it in the stream has finished.  launch_dependents lets the

@@ -35,6 +35,21 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// The same load for rows read once per call (a segment's tiles when one member block covers
+// all its members): the L2 lines are marked evict-first, so that what is read again soon --
+// partials, q, page tables, plans -- keeps its place in L2.  The policy is made in place.
+__device__ __forceinline__ void tma_load_2d_once(void *dst, const CUtensorMap *map, int32_t x, int32_t y,
+                                                 uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\t"
+        "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], pol;\n\t}" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Byte offset of element (row, k) of a 64-element-wide swizzled column block.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t k)
 {
