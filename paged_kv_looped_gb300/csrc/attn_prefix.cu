@@ -48,7 +48,7 @@ namespace {
 //              touch) and the columns half w/4 of each sub-tile; the two warps of a
 //              row quarter swap row maxima and sums through shared memory.  They
 //              also write the next run's Q rows into TMEM.
-//   warp 8/9   TMA copies of V / K sub-tiles (128 tokens) into 4- / 2-slot rings
+//   warp 8/9   TMA copies of V / K sub-tiles (128 tokens) into 3-slot rings
 //   warp 10    MMA issue: S into 2 TMEM S/P buffers, O += P V into the O buffer
 //   warp 11    scheduler: decodes the runs into a 4-deep ring of descriptors in
 //              shared memory, with the members' request ids
@@ -56,7 +56,7 @@ constexpr int kSoftWarps = 8;
 constexpr int kLoadVWarp = 8, kLoadKWarp = 9, kMmaWarp = 10, kSchedWarp = 11;
 constexpr int kPThreads = 12 * 32;
 constexpr int kSub = 128;                   // tokens per sub-tile (= one planner tile)
-constexpr int kStagesK = 2, kStagesV = 4;   // ring depths (sub-tiles); a K slot frees sooner
+constexpr int kStagesK = 3, kStagesV = 3;   // ring depths (sub-tiles), measured against 2/4, 2/3, 2/2
 constexpr int kHalfKV = kSub * 128;         // one 64-dim column block of a sub-tile (128 rows x 128 B)
 constexpr int kKVBytes = 2 * kHalfKV;       // K (or V) of one sub-tile
 constexpr int kSBufs = 2;                   // S/P buffers in TMEM
