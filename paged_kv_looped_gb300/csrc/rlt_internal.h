@@ -62,10 +62,13 @@ constexpr int kPrefixTile = 128;
 // each copy taking 1/F of every 128-token sub-tile's keys and writing its own
 // partial, so that the softmax work of a few rows is spread over all four SM
 // sub-partitions.  F follows from the rows of a segment's first (fullest)
-// member block; planner and kernel must agree on it.
+// member block; planner and kernel must agree on it.  Four copies only for up to 8
+// rows (a private tail at G = 8): measured on GB300, 16 rows (huginn's sessions at
+// G = 1) run faster as two copies of half the keys each than as four (25.22 against
+// 25.40 us per call), 8 rows slower (longctx 118.0 against 113.8).
 __host__ __device__ inline int prefix_replication(int rows)
 {
-    return rows <= 32 ? 4 : rows <= 64 ? 2 : 1;
+    return rows <= 8 ? 4 : rows <= 64 ? 2 : 1;
 }
 
 // Fields of one segment of a prefix plan (rlt_plan_prefix).

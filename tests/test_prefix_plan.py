@@ -18,9 +18,9 @@ TILE = 128
 
 def copies(members, G):
     """Copies of a segment's query rows in the tensor-core kernel: its first member block's
-    rows spread over the four TMEM lane quarters (4 copies of <= 32 rows, 2 of <= 64)."""
+    rows spread over the four TMEM lane quarters (4 copies of <= 8 rows, 2 of <= 64)."""
     rows = min(members, 128 // G) * G
-    return 4 if rows <= 32 else 2 if rows <= 64 else 1
+    return 4 if rows <= 8 else 2 if rows <= 64 else 1
 
 
 def tile_key(pt, b, t, ps):
