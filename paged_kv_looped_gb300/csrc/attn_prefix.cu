@@ -79,7 +79,8 @@ enum PrefixBar {
     kBarOFree = kBarQFull + kQBufs,         // O read out by all 4 softmax warps
     kBarDescFull = kBarOFree + 1,           // descriptor i published
     kBarDescFree = kBarDescFull + kDescs,   // descriptor i copied by every consumer
-    kBarPair = kBarDescFree + kDescs,       // the two softmax warps of row quarter i meet
+    kBarMemFull = kBarDescFree + kDescs,    // descriptor i's member rows and limits written
+    kBarPair = kBarMemFull + kDescs,        // the two softmax warps of row quarter i meet
     kNumBars = kBarPair + 4
 };
 constexpr int kFlagOff = kBarOff + kNumBars * 8;   // TMEM base address, abort flag
@@ -118,21 +119,41 @@ struct Run {
     int next_item;
 };
 
-// The run that starts at work item `item` of a CTA whose items end at item_end.
-__device__ __forceinline__ Run decode_run(const PrefixParams &pp, int G, int item, int item_end)
+// The run that starts at work item `item` of a CTA whose items end at item_end; called by
+// all 32 lanes of a warp (every lane gets the same run).  Its segment is the last one whose
+// first work unit is <= the item's (work units ascend with the segment index): the lanes read
+// the rows of 32 segments at once and a ballot picks it, so the plan costs one round trip per
+// 32 segments searched instead of one per halving step.
+__device__ __forceinline__ Run decode_run(const PrefixParams &pp, int G, int item, int item_end, int lane)
 {
     Run r;
     r.d.g = item / pp.work_units;
     const int unit = item - r.d.g * pp.work_units;
-    int lo = 0, hi = pp.num_segments - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (pp.segments[mid * kSegFields + kSegWorkBegin] <= unit)
-            lo = mid;
-        else
-            hi = mid - 1;
+    int32_t sd[kSegFields];
+#pragma unroll
+    for (int f = 0; f < kSegFields; ++f)
+        sd[f] = 0;
+    for (int base = 0; base < pp.num_segments; base += 32) {
+        const int s = base + lane;
+        int32_t row[kSegFields];
+#pragma unroll
+        for (int f = 0; f < kSegFields; ++f)
+            row[f] = s < pp.num_segments ? pp.segments[s * kSegFields + f] : 0;
+        const unsigned le = __ballot_sync(kFullMask, s < pp.num_segments && row[kSegWorkBegin] <= unit);
+        if (le != 0u) {
+            const int src = 31 - __clz(le);
+#pragma unroll
+            for (int f = 0; f < kSegFields; ++f)
+                sd[f] = __shfl_sync(kFullMask, row[f], src);
+        }
+        if (le != kFullMask)
+            break;                               // a later segment starts past this unit
     }
-    const int32_t *sd = pp.segments + lo * kSegFields;
+    if (pp.num_segments > 0 && __shfl_sync(kFullMask, pp.segments[kSegWorkBegin], 0) > unit) {
+#pragma unroll
+        for (int f = 0; f < kSegFields; ++f)     // (a malformed plan: segment 0, as a search would)
+            sd[f] = pp.segments[f];
+    }
     const int num_tiles = sd[kSegNumTiles];
     const int nchunks_seg = max(1, (num_tiles + pp.chunk_tiles - 1) / pp.chunk_tiles);
     const int local = max(0, unit - sd[kSegWorkBegin]);
@@ -161,10 +182,10 @@ __device__ __forceinline__ Run decode_run(const PrefixParams &pp, int G, int ite
 }
 
 // The next run with work at or after *item; false when the CTA's items are done.
-__device__ __forceinline__ bool next_run(const PrefixParams &pp, int G, int &item, int item_end, Run &r)
+__device__ __forceinline__ bool next_run(const PrefixParams &pp, int G, int &item, int item_end, Run &r, int lane)
 {
     while (item < item_end) {
-        r = decode_run(pp, G, item, item_end);
+        r = decode_run(pp, G, item, item_end, lane);
         item = r.next_item;
         if (r.d.nsub > 0)
             return true;
@@ -186,6 +207,9 @@ __device__ __forceinline__ bool take_desc(uint64_t *bars, const unsigned char *b
                                           int lane)
 {
     if (!warp_wait(&bars[kBarDescFull + r % kDescs], (r / kDescs) & 1u, abort))
+        return false;
+    // the softmax warps also need the member rows, published after the descriptor
+    if (row >= 0 && !warp_wait(&bars[kBarMemFull + r % kDescs], (r / kDescs) & 1u, abort))
         return false;
     out = reinterpret_cast<const RunDesc *>(base + kDescOff)[r % kDescs];
     const int mrow = row < 0 ? -1 : (row % (128 / max(out.F, 1))) / G;
@@ -294,6 +318,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         for (int i = 0; i < kDescs; ++i) {
             mbar_init(&bars[kBarDescFull + i], 1);
             mbar_init(&bars[kBarDescFree + i], kDescConsumers);
+            mbar_init(&bars[kBarMemFull + i], 1);
         }
         for (int i = 0; i < 4; ++i)
             mbar_init(&bars[kBarPair + i], 2);
@@ -321,11 +346,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 !(ok = warp_wait(&bars[kBarDescFree + d % kDescs], ((d - kDescs) / kDescs) & 1u, abort_flag)))
                 break;
             Run r;
-            const bool has = next_run(pp, G, item, item_end, r);
+            const bool has = next_run(pp, G, item, item_end, r, lane);
             if (!has)
                 r.d.nsub = 0;                    // the terminal descriptor
-            if (lane == 0)
+            if (lane == 0) {
                 descs[d % kDescs] = r.d;
+                // the copies and MMAs need only the descriptor: publish it before the members
+                mbar_arrive(&bars[kBarDescFull + d % kDescs]);
+            }
             for (int i = lane; has && i < r.d.n_mem; i += 32) {
                 int b = pp.members[r.member_begin + i];
                 if (b < 0 || b >= pp.num_rows) {
@@ -338,7 +366,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&bars[kBarDescFull + d % kDescs]);
+                mbar_arrive(&bars[kBarMemFull + d % kDescs]);
             // Fused append, checked once the descriptor is out: a member whose newest token
             // lies in tiles it shares would need a slot of a shared (read-only) page; flagged,
             // not written.  (The slot stays readable until every consumer has released it.)
