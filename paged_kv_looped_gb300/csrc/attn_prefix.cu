@@ -57,6 +57,7 @@ constexpr int kLoadVWarp = 8, kLoadKWarp = 9, kMmaWarp = 10, kSchedWarp = 11;
 constexpr int kPThreads = 12 * 32;
 constexpr int kSub = 128;                   // tokens per sub-tile (= one planner tile)
 constexpr int kStagesK = 3, kStagesV = 3;   // ring depths (sub-tiles), measured against 2/4, 2/3, 2/2
+constexpr int kPrefetch = 3;                 // sub-tiles fetched into L2 ahead of the ring
 constexpr int kHalfKV = kSub * 128;         // one 64-dim column block of a sub-tile (128 rows x 128 B)
 constexpr int kKVBytes = 2 * kHalfKV;       // K (or V) of one sub-tile
 constexpr int kSBufs = 2;                   // S/P buffers in TMEM
@@ -430,6 +431,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const int64_t nt = nt_next;
             const int nt_b = cur.page_row, nt_g = cur.g;
             const int64_t sub_begin = cur.tok_begin + (int64_t)j * kSub, tok_end = cur.tok_end;
+            // With l2_ahead, sub-tiles past the ring are fetched into L2 ahead of their copies:
+            // at a run's start the kPrefetch after the ring's first fill, then one per sub-tile,
+            // kPrefetch ahead of the ring, so that each copy into a freed slot reads L2 and a
+            // CTA's few sub-tiles are all requested at once, before the kernel ahead finishes.
+            int pf_row[kPrefetch];
+#pragma unroll
+            for (int k = 0; k < kPrefetch; ++k) {
+                const int t = j == 0 ? stages + k : (k == kPrefetch - 1 ? j + stages + k : -1);
+                pf_row[k] = pp.l2_ahead != 0 && t >= 0 && t < cur.nsub ? lane_row(cur, t) : -1;
+            }
             const bool once = cur.once != 0;
             if (j + 1 < cur.nsub) {
                 row_next = lane_row(cur, ++j);
@@ -476,6 +487,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 else
                     tc::tma_load_2d(dst, map, (lane & 1) * 64, row, &fullx[st]);
             }
+#pragma unroll
+            for (int k = 0; k < kPrefetch; ++k)
+                if (pf_row[k] >= 0)
+                    tc::tma_prefetch_l2_2d(map, (lane & 1) * 64, pf_row[k]);
             ++n;
         }
         if (!ok) {

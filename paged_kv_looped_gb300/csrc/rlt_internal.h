@@ -84,6 +84,10 @@ struct PrefixParams {
     int32_t chunk_tiles;         // 128-token tiles per CTA
     int32_t work_units;          // (segment, member block, chunk) units per kv head
     int32_t ctas;                // persistent CTAs sharing the num_kv_heads x work_units items
+    // Non-zero: the copy warps fetch sub-tiles into L2 kPrefetch ahead of their rings (the call
+    // with a split-K rest, whose CTAs hold few sub-tiles each; measured slower when a CTA
+    // streams long runs, where the rings already keep the copy bandwidth busy).
+    int32_t l2_ahead;
 };
 
 // Launch a kernel on `stream`; with `early`, as a programmatic dependent of the kernel

@@ -50,6 +50,16 @@ __device__ __forceinline__ void tma_load_2d_once(void *dst, const CUtensorMap *m
         : "memory");
 }
 
+// The box at (x = innermost element, y = row) fetched into L2 only: no shared memory, no
+// completion to wait for; a later tiled load of the same box then reads it from L2.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t x, int32_t y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Byte offset of element (row, k) of a 64-element-wide swizzled column block.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t k)
 {
