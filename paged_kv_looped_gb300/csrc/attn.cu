@@ -226,13 +226,13 @@ __device__ void merge_row(const DecodeParams &p, int64_t bh, int n_pre, int n, M
             }
         }
         __syncthreads();
-        // warps take the live partials in turn, eight loads in flight
+        // warps take the live partials in turn, sixteen loads in flight
         const int nl = live_off[32];
-        for (int k0 = warp * 8; k0 < nl; k0 += kCombineWarps * 8) {
-            float o[8][DPL];
-            float wk[8];
+        for (int k0 = warp * 16; k0 < nl; k0 += kCombineWarps * 16) {
+            float o[16][DPL];
+            float wk[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 16; ++i) {
                 const int k = k0 + i;
                 wk[i] = k < nl ? live_w[k] : 0.f;
                 const float *op = p.o_part + slot_of(k < nl ? live_slot[k] : 0) * D + lane * DPL;
@@ -249,7 +249,7 @@ __device__ void merge_row(const DecodeParams &p, int64_t bh, int n_pre, int n, M
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 16; ++i) {
                 ls += wk[i];
 #pragma unroll
                 for (int d = 0; d < DPL; ++d)

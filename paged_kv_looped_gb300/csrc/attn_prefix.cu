@@ -281,7 +281,10 @@ __device__ __forceinline__ bool pair_sync(uint64_t *bar, int &k, const volatile 
 
 // kAppend: the call fuses the append and runs every request's private tail here (no
 // split-K rest), so the producers store each tail's new rows before copying them.
-template <bool kAppend>
+// kL2Ahead: the copy warps prefetch sub-tiles into L2 ahead of their rings (a separate
+// instance, so that the others carry none of its code: with it compiled in but switched off
+// the long-context call measured 1.5-3 us slower).
+template <bool kAppend, bool kL2Ahead>
 __global__ void __launch_bounds__(kPThreads, 1)
     decode_prefix_kernel(const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const DecodeParams p,
@@ -439,7 +442,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
             for (int k = 0; k < kPrefetch; ++k) {
                 const int t = j == 0 ? stages + k : (k == kPrefetch - 1 ? j + stages + k : -1);
-                pf_row[k] = pp.l2_ahead != 0 && t >= 0 && t < cur.nsub ? lane_row(cur, t) : -1;
+                pf_row[k] = kL2Ahead && t >= 0 && t < cur.nsub ? lane_row(cur, t) : -1;
             }
             const bool once = cur.once != 0;
             if (j + 1 < cur.nsub) {
@@ -487,10 +490,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 else
                     tc::tma_load_2d(dst, map, (lane & 1) * 64, row, &fullx[st]);
             }
+            if constexpr (kL2Ahead) {
 #pragma unroll
-            for (int k = 0; k < kPrefetch; ++k)
-                if (pf_row[k] >= 0)
-                    tc::tma_prefetch_l2_2d(map, (lane & 1) * 64, pf_row[k]);
+                for (int k = 0; k < kPrefetch; ++k)
+                    if (pf_row[k] >= 0)
+                        tc::tma_prefetch_l2_2d(map, (lane & 1) * 64, pf_row[k]);
+            }
             ++n;
         }
         if (!ok) {
@@ -909,19 +914,22 @@ cudaError_t launch_prefix(const DecodeParams &p, const PrefixParams &pp, const v
     CUtensorMap kmap, vmap;
     if (!make_map(&kmap, k_bank, bank_rows, box_rows) || !make_map(&vmap, v_bank, bank_rows, box_rows))
         return cudaErrorInvalidValue;
-    static std::atomic<uint64_t> configured[2]{{0}, {0}};
+    static std::atomic<uint64_t> configured[3]{{0}, {0}, {0}};
     const bool append = p.k_new != nullptr;
-    auto kernel = append ? decode_prefix_kernel<true> : decode_prefix_kernel<false>;
+    const int which = append ? 0 : pp.l2_ahead != 0 ? 2 : 1;   // (the fused append runs no split-K rest)
+    auto kernel = which == 0   ? decode_prefix_kernel<true, false>
+                  : which == 1 ? decode_prefix_kernel<false, false>
+                               : decode_prefix_kernel<false, true>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
-    if (bit == 0 || (configured[append].load() & bit) == 0) {
+    if (bit == 0 || (configured[which].load() & bit) == 0) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemP);
         if (e != cudaSuccess)
             return e;
-        configured[append].fetch_or(bit);
+        configured[which].fetch_or(bit);
     }
     if (pp.ctas < 1)
         return cudaErrorInvalidValue;

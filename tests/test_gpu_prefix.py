@@ -188,3 +188,18 @@ def test_huginn_full_size_all_tensor_core_few_ctas(cuda_device):
     assert plan.max_rest_len == 0
     ref, ref_lse = oracle.decode_attn(h.q, h.k_pool, h.v_pool, case.page_table, case.seq_lens)
     check(got, ref, lse, ref_lse)
+
+
+@pytest.mark.parametrize("batch,tails", [(40, True), (70, True), (100, True)])
+def test_many_segments(cuda_device, batch, tails):
+    # more segments than one warp has lanes (one shared chain plus a private tail per request):
+    # the scheduler's segment search reads the plan's rows 32 at a time, and a run's segment may
+    # lie in any group of 32
+    rng = np.random.default_rng(batch)
+    lens = rng.integers(150, 700, size=batch)
+    case = W.custom(B=batch, Hq=4, Hkv=2, D=128, ps=16, seq_lens=lens, shared_frac=0.6, seed=batch + tails)
+    h = W.host_tensors(case)
+    plan, got, lse, _, _ = run_both(case, h, cuda_device, 2, private_tails=tails, max_ctas=7)
+    assert plan.num_segments > 32
+    ref, ref_lse = oracle.decode_attn(h.q, h.k_pool, h.v_pool, case.page_table, case.seq_lens)
+    check(got, ref, lse, ref_lse)
