@@ -2,7 +2,7 @@
 
 The latent noise maps a 24-bit uniform to x = erf(3/sqrt 2) (2u - 1) and returns
 initializer_range * sqrt(2) * erfinv(x).  On the GPU, erfinv(x) = x g(w) with
-w = -ln((1 - x)(1 + x)), and g is a degree-8 polynomial in w - c fitted here by least
+w = -ln((1 - x)(1 + x)), and g is a degree-7 polynomial in w - c fitted here by least
 squares in relative error against scipy's fp64 erfinv over w in [0, w_max], w_max the
 largest w any 24-bit code produces (|x| <= erf(3/sqrt 2)(1 - 2^-24)).  The script then
 evaluates the kernel's fp32 path (the product, the log, Horner) on all 2^24 codes and
@@ -15,7 +15,7 @@ import numpy as np
 from scipy.special import erf, erfinv
 
 
-def fit(deg: int = 8):
+def fit(deg: int = 7):
     erf3 = erf(3 / np.sqrt(2))
     h = np.arange(1 << 24, dtype=np.int64)
     x32 = ((2 * h + 1 - (1 << 24)).astype(np.float32) * np.float32(2.0 ** -24 * erf3)).astype(np.float32)
