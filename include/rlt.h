@@ -81,7 +81,7 @@ typedef enum rlt_status {
     RLT_OK = 0,
     RLT_ERR_INVALID_ARG = 1,          /* null pointer, negative size, misaligned buffer */
     RLT_ERR_OUT_OF_RANGE = 2,         /* bank, page, slot or length outside the pool */
-    RLT_ERR_UNSUPPORTED = 3,          /* a shape this build has no kernel for */
+    RLT_ERR_UNSUPPORTED = 3,          /* a shape the library has no kernel for */
     RLT_ERR_WORKSPACE_TOO_SMALL = 4,  /* see rlt_paged_decode_workspace_size */
     RLT_ERR_CUDA = 5                  /* the CUDA runtime reported an error */
 } rlt_status;
