@@ -82,3 +82,21 @@ def test_traffic_summary_is_dropped_when_a_kernel_source_changes(tmp_path, monke
     with open(tmp_path / "paged_kv_looped_gb300" / "csrc" / sources[0], "a") as fh:
         fh.write("\n// edited\n")
     assert bench.profiled_traffic("ouro", fused) is None
+
+
+def test_noise_roofline_takes_the_issue_bound_from_the_current_profile(monkeypatch):
+    # the committed ncu summary of the noise kernel was taken on the current noise.cu: the bench
+    # reports the kernel against integer issue (SMs x 4 schedulers x 32 lanes x clock / the
+    # profiled instructions per value) as well as against its HBM write
+    ipv = bench.profiled_noise_instructions()
+    assert ipv is not None and 20 < ipv < 100
+    monkeypatch.setattr(bench, "sm_count_and_clock", lambda: (152, 2070.0))
+    case = W.config("longctx")
+    values = case.noise.rows * case.noise.channels
+    peak = 152 * 4 * 32 * 2070e6 / ipv
+    ms = values / (0.7 * peak) * 1e3                     # a launch at 70 % of the issue bound
+    r = bench.noise_roofline(case, ms)
+    assert r["values"] == values
+    assert abs(r["alu"]["frac"] - 0.7) < 1e-3
+    assert r["bound"] == "alu"                           # 4 bytes per value write far below the copy peak
+    assert r["frac_of_hbm_peak"] < r["alu"]["frac"]
